@@ -1,0 +1,213 @@
+"""ctypes binding of libdecattn.so (include/decattn.h): argument marshalling only.
+
+Every function here takes torch tensors for device memory, passes their data pointers, sizes and the
+current CUDA stream to the C entry point of the same name (without the ``da_`` prefix), and raises
+``DecAttnError`` with the library's message when the call returns nonzero. No arithmetic of the step
+happens in Python: if the library is missing, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdecattn.so")
+
+DA_OK = 0
+DA_ERR_INVALID_ARG = -1
+DA_ERR_UNSUPPORTED = -2
+DA_ERR_CUDA = -3
+DA_ERR_DEVICE_INDEX = -4
+DA_ERR_TIMEOUT = -5
+
+DA_ROPE_DEFAULT, DA_ROPE_LINEAR, DA_ROPE_LLAMA3, DA_ROPE_LONGROPE, DA_ROPE_YARN = range(5)
+DA_BF16, DA_FP32 = 0, 1
+ROPE_KINDS = {"default": DA_ROPE_DEFAULT, "linear": DA_ROPE_LINEAR, "llama3": DA_ROPE_LLAMA3,
+              "longrope": DA_ROPE_LONGROPE, "yarn": DA_ROPE_YARN}
+DTYPES = {torch.bfloat16: DA_BF16, torch.float32: DA_FP32}
+
+
+class DecAttnError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"decattn error {code}: {msg}")
+        self.code = code
+
+
+class DaRopeScaling(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("theta", ctypes.c_double), ("rotary_dim", ctypes.c_int),
+                ("factor", ctypes.c_double), ("low_freq_factor", ctypes.c_double),
+                ("high_freq_factor", ctypes.c_double), ("original_max_position_embeddings", ctypes.c_int),
+                ("max_position_embeddings", ctypes.c_int), ("short_factor", ctypes.POINTER(ctypes.c_double)),
+                ("long_factor", ctypes.POINTER(ctypes.c_double)), ("attention_factor", ctypes.c_double),
+                ("beta_fast", ctypes.c_double), ("beta_slow", ctypes.c_double), ("mscale", ctypes.c_double),
+                ("mscale_all_dim", ctypes.c_double), ("truncate", ctypes.c_int)]
+
+
+class DaLayer(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("head_dim", ctypes.c_int), ("num_attention_heads", ctypes.c_int),
+                ("num_key_value_heads", ctypes.c_int), ("rotary_dim", ctypes.c_int),
+                ("q_norm_w", ctypes.c_void_p), ("k_norm_w", ctypes.c_void_p), ("eps", ctypes.c_double),
+                ("window", ctypes.c_int), ("softcap", ctypes.c_float), ("scale", ctypes.c_float)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "da_rope_tables_build": (I, [ctypes.POINTER(DaRopeScaling), P, P, I, P, P, P]),
+        "da_kv_cache_update": (I, [ctypes.POINTER(DaLayer), P, P, P, I, P, P, P, P, P, P, P, I, I, P]),
+        "da_attn_prefill": (I, [ctypes.POINTER(DaLayer), P, I, P, P, I, I, I, P, P, P, I, P, P, P, Z, P]),
+        "da_attn_decode": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, I, P, P, P, P, P, Z, P]),
+        "da_decode_workspace_bytes": (Z, [ctypes.POINTER(DaLayer), I, I]),
+        "da_check_device_error": (I, [P]),
+        "da_last_error": (ctypes.c_char_p, []),
+        "da_version": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+def last_error() -> str:
+    return LIB.da_last_error().decode()
+
+
+def version() -> int:
+    return int(LIB.da_version())
+
+
+def _check(rc):
+    if rc != DA_OK:
+        raise DecAttnError(rc, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------------------------------ configs
+
+def rope_scaling(theta, rotary_dim, scaling=None, max_position_embeddings=0):
+    """DaRopeScaling from config.json's rope_theta and rope_scaling dict (rope_type or type).
+
+    Returns (struct, keepalive) -- keep the second value alive while the struct is in use (it owns the
+    LongRoPE factor arrays)."""
+    s = dict(scaling or {})
+    kind = s.get("rope_type", s.get("type", "default"))
+    if kind not in ROPE_KINDS:
+        raise DecAttnError(DA_ERR_UNSUPPORTED, f"RoPE type {kind!r} is not implemented")
+    rs = DaRopeScaling()
+    rs.kind = ROPE_KINDS[kind]
+    rs.theta = float(theta)
+    rs.rotary_dim = int(rotary_dim)
+    rs.factor = float(s.get("factor") or 0.0)
+    rs.low_freq_factor = float(s.get("low_freq_factor") or 0.0)
+    rs.high_freq_factor = float(s.get("high_freq_factor") or 0.0)
+    rs.original_max_position_embeddings = int(s.get("original_max_position_embeddings") or 0)
+    rs.max_position_embeddings = int(max_position_embeddings or 0)
+    rs.attention_factor = float(s.get("attention_factor") or 0.0)
+    rs.beta_fast = float(s.get("beta_fast") or 0.0)
+    rs.beta_slow = float(s.get("beta_slow") or 0.0)
+    rs.mscale = float(s.get("mscale") or 0.0)
+    rs.mscale_all_dim = float(s.get("mscale_all_dim") or 0.0)
+    rs.truncate = 1 if s.get("truncate", True) else 0
+    keep = []
+    if kind == "longrope":
+        for name in ("short_factor", "long_factor"):
+            vals = [float(x) for x in s[name]]
+            if len(vals) != int(rotary_dim) // 2:
+                raise DecAttnError(DA_ERR_INVALID_ARG, f"longrope {name} holds {len(vals)} values, rotary_dim/2 = "
+                                                       f"{int(rotary_dim) // 2}")
+            arr = (ctypes.c_double * len(vals))(*vals)
+            keep.append(arr)
+            setattr(rs, name, ctypes.cast(arr, ctypes.POINTER(ctypes.c_double)))
+    return rs, keep
+
+
+def layer(dtype, head_dim, num_attention_heads, num_key_value_heads, rotary_dim=None, q_norm_w=None,
+          k_norm_w=None, eps=1e-6, window=0, softcap=0.0, scale=0.0):
+    """DaLayer for one layer; q_norm_w/k_norm_w are fp32 device tensors [head_dim] or None."""
+    L = DaLayer()
+    L.dtype = DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    L.head_dim = int(head_dim)
+    L.num_attention_heads = int(num_attention_heads)
+    L.num_key_value_heads = int(num_key_value_heads)
+    L.rotary_dim = int(rotary_dim if rotary_dim is not None else head_dim)
+    L.q_norm_w = q_norm_w.data_ptr() if q_norm_w is not None else None
+    L.k_norm_w = k_norm_w.data_ptr() if k_norm_w is not None else None
+    L.eps = float(eps)
+    L.window = int(window)
+    L.softcap = float(softcap)
+    L.scale = float(scale)
+    return L
+
+
+def window_for_layer(config: dict, layer_idx: int) -> int:
+    """The layer's sliding window as DecoderConfig.window reads it (page "42. More models", section "What
+    differs between model families"): sliding_window if layer_types marks the layer "sliding_attention",
+    else 0. Without layer_types, Mistral windows every layer and Qwen2 (use_sliding_window) the layers
+    from max_window_layers on."""
+    window = config.get("sliding_window") or 0
+    types = config.get("layer_types")
+    n = config.get("num_hidden_layers", layer_idx + 1)
+    if types is None and window:
+        kind = config.get("model_type")
+        if kind == "mistral":
+            types = ["sliding_attention"] * n
+        elif kind == "qwen2" and config.get("use_sliding_window"):
+            start = config.get("max_window_layers", n)
+            types = ["full_attention" if i < start else "sliding_attention" for i in range(n)]
+    if not types or "sliding_attention" not in types:
+        return 0
+    return window if types[layer_idx] == "sliding_attention" else 0
+
+
+# ------------------------------------------------------------------------------------------ entry points
+
+def rope_tables_build(rs, positions, seq_len, n, cos, sin, stream=None):
+    _check(LIB.da_rope_tables_build(ctypes.byref(rs), _ptr(positions), _ptr(seq_len), int(n), _ptr(cos), _ptr(sin),
+                                    _stream(stream)))
+
+
+def kv_cache_update(L, q, k, v, n, rows, positions, cos, sin, q_rot, k_cache, v_cache, num_rows, max_len,
+                    stream=None):
+    _check(LIB.da_kv_cache_update(ctypes.byref(L), _ptr(q), _ptr(k), _ptr(v), int(n), _ptr(rows), _ptr(positions),
+                                  _ptr(cos), _ptr(sin), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), int(num_rows),
+                                  int(max_len), _stream(stream)))
+
+
+def attn_prefill(L, q_rot, n_tokens, k_cache, v_cache, num_rows, max_len, n_seqs, q_start, rows, first_pos,
+                 max_q_len, key_positions, out, workspace=None, ws_bytes=0, stream=None):
+    _check(LIB.da_attn_prefill(ctypes.byref(L), _ptr(q_rot), int(n_tokens), _ptr(k_cache), _ptr(v_cache),
+                               int(num_rows), int(max_len), int(n_seqs), _ptr(q_start), _ptr(rows), _ptr(first_pos),
+                               int(max_q_len), _ptr(key_positions), _ptr(out), _ptr(workspace), int(ws_bytes),
+                               _stream(stream)))
+
+
+def attn_decode(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, positions, key_positions, out,
+                workspace, ws_bytes, stream=None):
+    _check(LIB.da_attn_decode(ctypes.byref(L), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), int(num_rows),
+                              int(max_len), int(n_seqs), _ptr(rows), _ptr(positions), _ptr(key_positions), _ptr(out),
+                              _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def decode_workspace_bytes(L, n_seqs, max_len) -> int:
+    return int(LIB.da_decode_workspace_bytes(ctypes.byref(L), int(n_seqs), int(max_len)))
+
+
+def check_device_error(stream=None):
+    _check(LIB.da_check_device_error(_stream(stream)))

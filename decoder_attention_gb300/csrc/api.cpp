@@ -1,0 +1,400 @@
+// Host side of the C ABI declared in include/decattn.h: argument checks, fp64 RoPE frequency math,
+// tensor-map encoding and dispatch to the kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "decattn.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return DA_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------------------------------ layer checks
+
+int check_layer(const da_layer* L) {
+  if (!L) return fail(DA_ERR_INVALID_ARG, "layer is NULL");
+  if (L->dtype != DA_BF16 && L->dtype != DA_FP32) return fail(DA_ERR_INVALID_ARG, "dtype %d is not DA_BF16 or DA_FP32", L->dtype);
+  if (L->head_dim != 64 && L->head_dim != 128)
+    return fail(DA_ERR_UNSUPPORTED, "head_dim %d is not implemented (64 or 128)", L->head_dim);
+  if (L->num_attention_heads < 1 || L->num_key_value_heads < 1)
+    return fail(DA_ERR_INVALID_ARG, "head counts must be positive (Hq %d, Hkv %d)", L->num_attention_heads, L->num_key_value_heads);
+  if (L->num_attention_heads % L->num_key_value_heads)
+    return fail(DA_ERR_INVALID_ARG, "num_attention_heads %d is not a multiple of num_key_value_heads %d",
+                L->num_attention_heads, L->num_key_value_heads);
+  if (L->rotary_dim < 2 || L->rotary_dim > L->head_dim || (L->rotary_dim & 1))
+    return fail(DA_ERR_INVALID_ARG, "rotary_dim %d must be even and in [2, head_dim=%d]", L->rotary_dim, L->head_dim);
+  if ((L->q_norm_w == nullptr) != (L->k_norm_w == nullptr))
+    return fail(DA_ERR_INVALID_ARG, "q_norm_w and k_norm_w must be both set or both NULL");
+  if (!(L->eps >= 0.0) || !std::isfinite(L->eps)) return fail(DA_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (L->window < 0) return fail(DA_ERR_INVALID_ARG, "window %d must be >= 0", L->window);
+  if (!(L->softcap >= 0.f) || !std::isfinite(L->softcap)) return fail(DA_ERR_INVALID_ARG, "softcap must be finite and >= 0");
+  if (!(L->scale >= 0.f) || !std::isfinite(L->scale)) return fail(DA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  return DA_OK;
+}
+
+float layer_scale(const da_layer* L) { return L->scale > 0.f ? L->scale : 1.0f / std::sqrt(static_cast<float>(L->head_dim)); }
+
+// ------------------------------------------------------------------------------------------ frequencies
+// Page "42. More models: a registry, scaled RoPE, sliding windows and latent attention", section
+// "Scaled RoPE" (rope_inv_freq), and "Model resolution" (Overview) for LongRoPE, restated in fp64.
+
+int compute_freqs(const da_rope_scaling* rs, da::RopeFreqs* f) {
+  if (!rs) return fail(DA_ERR_INVALID_ARG, "rope scaling is NULL");
+  const int r = rs->rotary_dim;
+  if (r < 2 || r > 2 * da::kMaxRotHalf || (r & 1))
+    return fail(DA_ERR_INVALID_ARG, "rotary_dim %d must be even and in [2, %d]", r, 2 * da::kMaxRotHalf);
+  if (!(rs->theta > 1.0) || !std::isfinite(rs->theta)) return fail(DA_ERR_INVALID_ARG, "rope theta must be finite and > 1");
+  const int half = r / 2;
+  std::memset(f, 0, sizeof(*f));
+  f->half = half;
+  f->switch_len = 0x7fffffff;
+  f->use_seq_len = 0;
+  f->af = 1.0;
+  double base[da::kMaxRotHalf];
+  for (int i = 0; i < half; ++i) base[i] = 1.0 / std::pow(rs->theta, (2.0 * i) / r);
+  const double kPi = 3.14159265358979323846;
+  switch (rs->kind) {
+    case DA_ROPE_DEFAULT:
+      for (int i = 0; i < half; ++i) f->inv_short[i] = base[i];
+      break;
+    case DA_ROPE_LINEAR:
+      if (!(rs->factor > 0.0)) return fail(DA_ERR_INVALID_ARG, "linear rope scaling needs factor > 0");
+      for (int i = 0; i < half; ++i) f->inv_short[i] = base[i] / rs->factor;
+      break;
+    case DA_ROPE_LLAMA3: {
+      const double old = rs->original_max_position_embeddings, low = rs->low_freq_factor, high = rs->high_freq_factor;
+      if (!(rs->factor > 0.0) || !(old > 0) || !(low > 0.0) || !(high > low))
+        return fail(DA_ERR_INVALID_ARG, "llama3 rope scaling needs factor > 0, original > 0, high > low > 0");
+      for (int i = 0; i < half; ++i) {
+        const double wl = 2.0 * kPi / base[i];
+        double v;
+        if (wl > old / low) {
+          v = base[i] / rs->factor;                           // long wavelengths: interpolated
+        } else if (wl >= old / high) {
+          const double smooth = (old / wl - low) / (high - low);
+          v = (1.0 - smooth) * base[i] / rs->factor + smooth * base[i];
+        } else {
+          v = base[i];                                        // short wavelengths: kept
+        }
+        f->inv_short[i] = v;
+      }
+      break;
+    }
+    case DA_ROPE_LONGROPE: {
+      const int old = rs->original_max_position_embeddings;
+      if (!rs->short_factor || !rs->long_factor) return fail(DA_ERR_INVALID_ARG, "longrope needs short_factor and long_factor");
+      if (old <= 0) return fail(DA_ERR_INVALID_ARG, "longrope needs original_max_position_embeddings > 0");
+      for (int i = 0; i < half; ++i) {
+        if (!(rs->short_factor[i] > 0.0) || !(rs->long_factor[i] > 0.0) || !std::isfinite(rs->short_factor[i]) ||
+            !std::isfinite(rs->long_factor[i]))
+          return fail(DA_ERR_INVALID_ARG, "longrope factors must be finite and > 0 (pair %d)", i);
+        f->inv_short[i] = base[i] / rs->short_factor[i];
+        f->inv_long[i] = base[i] / rs->long_factor[i];
+      }
+      f->switch_len = old;
+      f->use_seq_len = 1;
+      if (rs->attention_factor > 0.0) {
+        f->af = rs->attention_factor;
+      } else {
+        const int mpe = rs->max_position_embeddings > 0 ? rs->max_position_embeddings : old;
+        const double s = static_cast<double>(mpe) / old;
+        f->af = s <= 1.0 ? 1.0 : std::sqrt(1.0 + std::log(s) / std::log(static_cast<double>(old)));
+      }
+      break;
+    }
+    case DA_ROPE_YARN: {
+      const double old = rs->original_max_position_embeddings;
+      if (!(old > 0)) return fail(DA_ERR_INVALID_ARG, "yarn needs original_max_position_embeddings > 0");
+      double factor = rs->factor;
+      if (!(factor > 0.0)) {
+        if (rs->max_position_embeddings <= 0) return fail(DA_ERR_INVALID_ARG, "yarn needs factor or max_position_embeddings");
+        factor = rs->max_position_embeddings / old;
+      }
+      auto mscale = [](double sc, double m) { return sc <= 1.0 ? 1.0 : 0.1 * m * std::log(sc) + 1.0; };
+      if (rs->attention_factor > 0.0)
+        f->af = rs->attention_factor;
+      else if (rs->mscale > 0.0 && rs->mscale_all_dim > 0.0)
+        f->af = mscale(factor, rs->mscale) / mscale(factor, rs->mscale_all_dim);
+      else
+        f->af = mscale(factor, 1.0);
+      // fractional pair index whose wavelength fits `rot` times into the original context
+      auto pair_for = [&](double rot) { return r * std::log(old / (rot * 2.0 * kPi)) / (2.0 * std::log(rs->theta)); };
+      double lo = pair_for(rs->beta_fast > 0.0 ? rs->beta_fast : 32.0);
+      double hi = pair_for(rs->beta_slow > 0.0 ? rs->beta_slow : 1.0);
+      if (rs->truncate) {
+        lo = std::floor(lo);
+        hi = std::ceil(hi);
+      }
+      lo = std::max(lo, 0.0);
+      hi = std::min(hi, static_cast<double>(r - 1));
+      const double span = (hi != lo) ? (hi - lo) : 0.001;
+      for (int i = 0; i < half; ++i) {
+        const double ramp = std::min(1.0, std::max(0.0, (i - lo) / span));   // 0: fast pair, 1: slow pair
+        f->inv_short[i] = base[i] / factor * ramp + base[i] * (1.0 - ramp);
+      }
+      break;
+    }
+    default:
+      return fail(DA_ERR_UNSUPPORTED, "RoPE kind %d is not implemented", rs->kind);
+  }
+  if (!f->use_seq_len)
+    for (int i = 0; i < half; ++i) f->inv_long[i] = f->inv_short[i];
+  return DA_OK;
+}
+
+// ------------------------------------------------------------------------------------------ tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+namespace da {
+
+bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                         uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1, stride2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace da
+
+// ============================================================================================ C ABI
+
+extern "C" {
+
+const char* da_last_error(void) { return g_last_error.c_str(); }
+
+int da_version(void) { return 100; }   // 0.1.0
+
+int da_rope_tables_build(const da_rope_scaling* rs, const int32_t* positions, const int32_t* seq_len, int n,
+                         float* cos, float* sin, cudaStream_t stream) {
+  da::RopeFreqs f;
+  int rc = compute_freqs(rs, &f);
+  if (rc) return rc;
+  if (n < 0) return fail(DA_ERR_INVALID_ARG, "n = %d < 0", n);
+  if (n == 0) return ok();
+  if (!positions || !cos || !sin) return fail(DA_ERR_INVALID_ARG, "positions, cos and sin must be non-NULL");
+  if (f.use_seq_len && !seq_len) return fail(DA_ERR_INVALID_ARG, "longrope needs seq_len per token");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  cudaError_t e = da::launch_rope_tables(f, positions, seq_len, n, cos, sin, err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope_tables launch");
+  return ok();
+}
+
+int da_kv_cache_update(const da_layer* L, const void* q, const void* k, const void* v, int n, const int32_t* rows,
+                       const int32_t* positions, const float* cos, const float* sin, void* q_rot, void* k_cache,
+                       void* v_cache, int num_rows, int max_len, cudaStream_t stream) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n < 0) return fail(DA_ERR_INVALID_ARG, "n = %d < 0", n);
+  if (n == 0) return ok();
+  if (!q || !k || !v || !rows || !positions || !cos || !sin || !q_rot || !k_cache || !v_cache)
+    return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(DA_ERR_INVALID_ARG, "q, k, v, q_rot and the caches must be 16-byte aligned");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  da::KvUpdateArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.n = n;
+  a.hq = L->num_attention_heads;
+  a.hkv = L->num_key_value_heads;
+  a.d = L->head_dim;
+  a.rot = L->rotary_dim;
+  a.rows = rows;
+  a.positions = positions;
+  a.cos = cos;
+  a.sin = sin;
+  a.q_norm_w = L->q_norm_w;
+  a.k_norm_w = L->k_norm_w;
+  a.eps = static_cast<float>(L->eps);
+  a.q_rot = q_rot;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_rows = num_rows;
+  a.max_len = max_len;
+  a.err = err;
+  cudaError_t e = da::launch_kv_update(a, L->dtype == DA_BF16, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_cache_update launch");
+  return ok();
+}
+
+static int attn_common_checks(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache,
+                              int num_rows, int max_len, int n_seqs, const int32_t* rows, void* out) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n_seqs < 0) return fail(DA_ERR_INVALID_ARG, "n_seqs = %d < 0", n_seqs);
+  if (n_seqs > 65535) return fail(DA_ERR_UNSUPPORTED, "n_seqs = %d > 65535 per call", n_seqs);
+  if (n_seqs == 0) return DA_OK;
+  if (!q_rot || !k_cache || !v_cache || !rows || !out) return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
+  if (static_cast<long long>(num_rows) * L->num_key_value_heads * max_len > 0x7fffffffLL)
+    return fail(DA_ERR_UNSUPPORTED, "num_rows * Hkv * max_len exceeds 2^31 key slots");
+  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return fail(DA_ERR_INVALID_ARG, "q_rot, the caches and out must be 16-byte aligned");
+  return DA_OK;
+}
+
+static da::AttnArgs make_args(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache,
+                              int num_rows, int max_len, int n_seqs, const int32_t* rows, const int32_t* key_positions,
+                              void* out, int* err) {
+  da::AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q_rot = q_rot;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.out = out;
+  a.hq = L->num_attention_heads;
+  a.hkv = L->num_key_value_heads;
+  a.d = L->head_dim;
+  a.num_rows = num_rows;
+  a.max_len = max_len;
+  a.n_seqs = n_seqs;
+  a.rows = rows;
+  a.key_positions = key_positions;
+  a.window = L->window;
+  a.softcap = L->softcap;
+  a.scale = layer_scale(L);
+  a.err = err;
+  return a;
+}
+
+int da_attn_prefill(const da_layer* L, const void* q_rot, int n_tokens, const void* k_cache, const void* v_cache,
+                    int num_rows, int max_len, int n_seqs, const int32_t* q_start, const int32_t* rows,
+                    const int32_t* first_pos, int max_q_len, const int32_t* key_positions, void* out, void* workspace,
+                    size_t ws_bytes, cudaStream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out);
+  if (rc) return rc;
+  if (n_tokens < 0 || max_q_len < 0) return fail(DA_ERR_INVALID_ARG, "n_tokens and max_q_len must be >= 0");
+  if (n_seqs == 0 || n_tokens == 0 || max_q_len == 0) return ok();
+  if (!q_start || !first_pos) return fail(DA_ERR_INVALID_ARG, "q_start and first_pos must be non-NULL");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  da::AttnArgs a = make_args(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, key_positions, out, err);
+  a.q_start = q_start;
+  a.first_pos = first_pos;
+  a.max_q_len = max_q_len;
+  a.n_tokens = n_tokens;
+  const bool fast = L->dtype == DA_BF16 && L->head_dim == 128 && key_positions == nullptr;
+  cudaError_t e = fast ? da::launch_prefill_bf16(a, stream) : da::launch_attn_generic(a, L->dtype == DA_BF16, stream);
+  if (e != cudaSuccess) return cuda_fail(e, fast ? "prefill (tcgen05) launch" : "prefill (generic) launch");
+  return ok();
+}
+
+static bool decode_fast(const da_layer* L, const int32_t* key_positions) {
+  return L->dtype == DA_BF16 && L->head_dim == 128 && key_positions == nullptr &&
+         L->num_attention_heads / L->num_key_value_heads <= 8;
+}
+
+size_t da_decode_workspace_bytes(const da_layer* L, int n_seqs, int max_len) {
+  if (check_layer(L) != DA_OK || n_seqs <= 0 || max_len <= 0) return 0;
+  if (!decode_fast(L, nullptr)) return 0;
+  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window);
+  return da::decode_workspace_bytes(L->num_attention_heads, n_seqs, p);
+}
+
+int da_attn_decode(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache, int num_rows,
+                   int max_len, int n_seqs, const int32_t* rows, const int32_t* positions,
+                   const int32_t* key_positions, void* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out);
+  if (rc) return rc;
+  if (n_seqs == 0) return ok();
+  if (!positions) return fail(DA_ERR_INVALID_ARG, "positions must be non-NULL");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  da::AttnArgs a = make_args(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, key_positions, out, err);
+  a.positions = positions;
+  a.max_q_len = 1;
+  a.n_tokens = n_seqs;
+  if (!decode_fast(L, key_positions)) {
+    cudaError_t e = da::launch_attn_generic(a, L->dtype == DA_BF16, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode (generic) launch");
+    return ok();
+  }
+  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window);
+  const size_t need = da::decode_workspace_bytes(L->num_attention_heads, n_seqs, p);
+  if (!workspace || ws_bytes < need)
+    return fail(DA_ERR_INVALID_ARG, "decode workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
+  if (!aligned16(workspace)) return fail(DA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  cudaError_t e = da::launch_decode_bf16(a, p, workspace, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode (split-K) launch");
+  return ok();
+}
+
+int da_check_device_error(cudaStream_t stream) {
+  int flags = 0;
+  if (da::read_and_clear_error_word(stream, &flags) != DA_OK)
+    return fail(DA_ERR_CUDA, "could not read the device error word: %s", cudaGetErrorString(cudaGetLastError()));
+  if (flags & da::kErrTimeout) return fail(DA_ERR_TIMEOUT, "a kernel gave up a bounded wait (timeout)");
+  if (flags & da::kErrIndex) return fail(DA_ERR_DEVICE_INDEX, "a kernel met a row, position or slot out of range");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// Internal interface between the host API (api.cpp) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "decattn.h"
+
+namespace da {
+
+constexpr int kMaxRotHalf = 128;  // r/2 <= 128 (r <= 256)
+
+// Error flags ORed into the device error word (the word itself lives in errors.cu).
+constexpr int kErrIndex = 1;
+constexpr int kErrTimeout = 2;
+
+int* error_word_ptr();
+int read_and_clear_error_word(cudaStream_t stream, int* flags);
+
+// Frequencies of one rope configuration, computed on the host in fp64. Tokens whose sequence length
+// exceeds `switch_len` use the `inv_long` table (LongRoPE); otherwise `inv_short`.
+struct RopeFreqs {
+  int half;                      // r / 2
+  int switch_len;                // long table when seq_len > switch_len; INT32_MAX when unused
+  int use_seq_len;               // 1: read seq_len[] (LongRoPE)
+  double af;                     // attention factor multiplying cos and sin
+  double inv_short[kMaxRotHalf];
+  double inv_long[kMaxRotHalf];
+};
+
+cudaError_t launch_rope_tables(const RopeFreqs& f, const int32_t* positions, const int32_t* seq_len, int n,
+                               float* cos, float* sin, int* err, cudaStream_t stream);
+
+struct KvUpdateArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int n, hq, hkv, d, rot;
+  const int32_t* rows;
+  const int32_t* positions;
+  const float* cos;
+  const float* sin;
+  const float* q_norm_w;
+  const float* k_norm_w;
+  float eps;
+  void* q_rot;
+  void* k_cache;
+  void* v_cache;
+  int num_rows, max_len;
+  int* err;
+};
+cudaError_t launch_kv_update(const KvUpdateArgs& a, bool bf16, cudaStream_t stream);
+
+// Query set of an attention call: prefill chunks (q_start/first_pos) or decode tokens (positions).
+struct AttnArgs {
+  const void* q_rot;
+  const void* k_cache;
+  const void* v_cache;
+  void* out;
+  int hq, hkv, d;
+  int num_rows, max_len;
+  int n_seqs;
+  const int32_t* rows;
+  const int32_t* q_start;         // prefill: [S+1]; NULL for decode (one token per sequence)
+  const int32_t* first_pos;       // prefill: [S]
+  const int32_t* positions;       // decode: [S]
+  int max_q_len;                  // prefill: grid bound; decode: 1
+  int n_tokens;                   // rows of q_rot/out (prefill: q_start[S]; decode: S)
+  const int32_t* key_positions;   // [R, M] or NULL
+  int window;
+  float softcap;
+  float scale;
+  int* err;
+};
+cudaError_t launch_attn_generic(const AttnArgs& a, bool bf16, cudaStream_t stream);
+
+// Split-K decode (bf16, d = 128, Hq/Hkv <= 8, no key_positions).
+struct DecodePlan {
+  int chunk;      // keys per split (multiple of 64)
+  int n_splits;   // splits per (sequence, KV head) at most
+};
+DecodePlan decode_plan(int hkv, int n_seqs, int max_len, int window);
+size_t decode_workspace_bytes(int hq, int n_seqs, const DecodePlan& p);
+cudaError_t launch_decode_bf16(const AttnArgs& a, const DecodePlan& p, void* workspace, cudaStream_t stream);
+
+// tcgen05 prefill (bf16, d = 128, no key_positions).
+cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream);
+
+// Tensor maps (driver entry point resolved at run time; no link-time dependency on libcuda).
+bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_outer);
+bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                         uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2);
+
+}  // namespace da

@@ -1,0 +1,200 @@
+// RoPE tables and the fused q/k RMSNorm + RoPE + KV-cache write.
+//
+// Page "42. More models: a registry, scaled RoPE, sliding windows and latent attention": rope_tables
+// (section "Scaled RoPE") and the part of DecoderAttention.forward from q_norm/k_norm through
+// cache.update; page "MoE, optimisers, decoding -- every line, every shape", §3.2 RMSNorm, §3.3 KVCache
+// and §4 Rotary for the norm, the cache write and the split-half rotation.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace da {
+
+// ---------------------------------------------------------------------------------------------- tables
+
+// One thread per (token, pair). The angle p * inv_i is formed in fp64 and reduced into [-pi, pi] by
+// Cody-Waite reduction with 2 pi split into a head and a tail (both fp64), then cos/sin are taken in
+// fp32: at p ~ 131071 the fp32 product alone would be off by up to 4e-3 rad.
+__global__ void rope_tables_kernel(const __grid_constant__ RopeFreqs f, const int32_t* __restrict__ positions,
+                                   const int32_t* __restrict__ seq_len, int n, float* __restrict__ cos_out,
+                                   float* __restrict__ sin_out, int* err) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(n) * f.half;
+  if (idx >= total) return;
+  const int t = static_cast<int>(idx / f.half);
+  const int i = static_cast<int>(idx - static_cast<long long>(t) * f.half);
+  const int p = positions[t];
+  if (p < 0) {
+    set_error(err, kErrIndex);
+    cos_out[idx] = 0.f;
+    sin_out[idx] = 0.f;
+    return;
+  }
+  const bool use_long = f.use_seq_len && seq_len[t] > f.switch_len;
+  const double inv = use_long ? f.inv_long[i] : f.inv_short[i];
+  const double ang = static_cast<double>(p) * inv;
+  const double kTwoPiHi = 6.283185307179586;        // 2 pi rounded to fp64
+  const double kTwoPiLo = 2.4492935982947064e-16;   // 2 pi - kTwoPiHi
+  const double k = rint(ang * (1.0 / 6.283185307179586));
+  double r = fma(-k, kTwoPiHi, ang);
+  r = fma(-k, kTwoPiLo, r);
+  float s, c;
+  sincosf(static_cast<float>(r), &s, &c);
+  const float af = static_cast<float>(f.af);
+  cos_out[idx] = c * af;
+  sin_out[idx] = s * af;
+}
+
+cudaError_t launch_rope_tables(const RopeFreqs& f, const int32_t* positions, const int32_t* seq_len, int n,
+                               float* cos, float* sin, int* err, cudaStream_t stream) {
+  const long long total = static_cast<long long>(n) * f.half;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (total + threads - 1) / threads;
+  rope_tables_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(f, positions, seq_len, n, cos, sin, err);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------- cache update
+
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const void* p, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f2 = __bfloat1622float2(h[j]);
+      x[2 * j] = f2.x;
+      x[2 * j + 1] = f2.y;
+    }
+  }
+  __device__ static void store(void* p, const float (&x)[8]) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+    *reinterpret_cast<uint4*>(p) = u;
+  }
+};
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const void* p, float (&x)[4]) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+  }
+  __device__ static void store(void* p, const float (&x)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  }
+};
+
+// Each head vector (d elements) is handled by d / VEC threads, each owning 16 bytes (VEC consecutive
+// elements). Items are (token, head) for the Hq query heads followed by the Hkv key heads of each token;
+// a key item also copies the token's value vector for that head into the V cache (bit for bit).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
+  using V = Vec16<T>;
+  constexpr int VEC = V::N;
+  constexpr int TPV = D / VEC;            // threads per vector (8..32)
+  constexpr int VPB = 256 / TPV;          // vectors per block
+  __shared__ float stage[VPB][D];
+
+  const int sub = threadIdx.x % TPV;      // which 16-byte piece of the vector
+  const int slot = threadIdx.x / TPV;
+  const int heads = a.hq + a.hkv;
+  const long long item = static_cast<long long>(blockIdx.x) * VPB + slot;
+  const bool live = item < static_cast<long long>(a.n) * heads;
+  int t = 0, hh = 0;
+  if (live) {
+    t = static_cast<int>(item / heads);
+    hh = static_cast<int>(item - static_cast<long long>(t) * heads);
+  }
+  const bool is_q = hh < a.hq;
+  const int e0 = sub * VEC;
+
+  float x[VEC];
+  if (live) {
+    const T* src = is_q ? static_cast<const T*>(a.q) + (static_cast<long long>(t) * a.hq + hh) * D
+                        : static_cast<const T*>(a.k) + (static_cast<long long>(t) * a.hkv + (hh - a.hq)) * D;
+    V::load(src + e0, x);
+  } else {
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) x[j] = 0.f;
+  }
+
+  // RMSNorm over the head: x / sqrt(mean(x^2) + eps) * w
+  if (a.q_norm_w != nullptr) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) ss = fmaf(x[j], x[j], ss);
+#pragma unroll
+    for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
+    const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
+    const float* w = is_q ? a.q_norm_w : a.k_norm_w;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * w[e0 + j];
+  }
+
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) stage[slot][e0 + j] = x[j];
+  __syncwarp();
+
+  // split-half rotation of the first `rot` dims
+  const int half = a.rot >> 1;
+  float y[VEC];
+  const float* cs = a.cos + static_cast<long long>(t) * half;
+  const float* sn = a.sin + static_cast<long long>(t) * half;
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) {
+    const int e = e0 + j;
+    if (e < half) {
+      y[j] = live ? x[j] * cs[e] - stage[slot][e + half] * sn[e] : 0.f;
+    } else if (e < a.rot) {
+      y[j] = live ? x[j] * cs[e - half] + stage[slot][e - half] * sn[e - half] : 0.f;
+    } else {
+      y[j] = x[j];
+    }
+  }
+  if (!live) return;
+
+  if (is_q) {
+    T* dst = static_cast<T*>(a.q_rot) + (static_cast<long long>(t) * a.hq + hh) * D;
+    V::store(dst + e0, y);
+    return;
+  }
+  const int g = hh - a.hq;
+  const int row = a.rows[t];
+  const int pos = a.positions[t];
+  if (row < 0 || row >= a.num_rows || pos < 0 || pos >= a.max_len) {
+    if (sub == 0) set_error(a.err, kErrIndex);
+    return;
+  }
+  const long long slot_off = ((static_cast<long long>(row) * a.hkv + g) * a.max_len + pos) * D;
+  V::store(static_cast<T*>(a.k_cache) + slot_off + e0, y);
+  const uint4 vv = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.v) +
+                                                   (static_cast<long long>(t) * a.hkv + g) * D + e0);
+  *reinterpret_cast<uint4*>(static_cast<T*>(a.v_cache) + slot_off + e0) = vv;
+}
+
+template <typename T, int D>
+static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
+  constexpr int TPV = D / Vec16<T>::N;
+  constexpr int VPB = 256 / TPV;
+  const long long items = static_cast<long long>(a.n) * (a.hq + a.hkv);
+  if (items == 0) return cudaSuccess;
+  const long long blocks = (items + VPB - 1) / VPB;
+  kv_update_kernel<T, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_update(const KvUpdateArgs& a, bool bf16, cudaStream_t stream) {
+  if (bf16) return a.d == 64 ? launch_kv_t<__nv_bfloat16, 64>(a, stream) : launch_kv_t<__nv_bfloat16, 128>(a, stream);
+  return a.d == 64 ? launch_kv_t<float, 64>(a, stream) : launch_kv_t<float, 128>(a, stream);
+}
+
+}  // namespace da

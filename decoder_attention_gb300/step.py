@@ -1,0 +1,88 @@
+"""One layer's attention step through the C ABI: rope tables -> norm/rope/cache write -> attention.
+
+``AttentionStep`` owns the per-call buffers (cos/sin tables, q_rot, out, decode workspace) that the caller
+must provide to the library, allocated once with torch; ``run()`` only enqueues the library's kernels.
+Prefill chunks and decode tokens of one batch go to da_attn_prefill and da_attn_decode respectively,
+after one da_kv_cache_update for all tokens.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _abi
+
+
+def rotary_dim_of(head_dim, partial_rotary_factor):
+    r = int(round(head_dim * partial_rotary_factor))
+    if r <= 0 or r % 2 or r > head_dim:
+        raise ValueError(f"rotary dim {r} must be even and in (0, {head_dim}]")
+    return r
+
+
+class AttentionStep:
+    """Buffers and C structs for one LayerCall (see decoder_attention_gb300.inputs)."""
+
+    def __init__(self, call, device=None):
+        dev = torch.device(device) if device is not None else call.q.device
+        self.call = c = call
+        self.device = dev
+        self.rot = rotary_dim_of(c.head_dim, c.partial_rotary_factor)
+        self.rs, self._keep = _abi.rope_scaling(c.rope_theta, self.rot, c.rope_scaling, c.max_position_embeddings)
+        self.q_norm_w = c.q_norm_w.to(dev, torch.float32).contiguous() if c.q_norm_w is not None else None
+        self.k_norm_w = c.k_norm_w.to(dev, torch.float32).contiguous() if c.k_norm_w is not None else None
+        self.L = _abi.layer(c.dtype, c.head_dim, c.num_attention_heads, c.num_key_value_heads, self.rot,
+                            self.q_norm_w, self.k_norm_w, c.eps, c.window, c.softcap, 0.0)
+        n = c.n_tokens
+        self.cos = torch.empty((max(n, 1), self.rot // 2), dtype=torch.float32, device=dev)
+        self.sin = torch.empty_like(self.cos)
+        self.q_rot = torch.empty_like(c.q)
+        self.out = torch.empty_like(c.q)
+        self.ws_bytes = 0
+        self.workspace = None
+        if c.n_decode:
+            self.ws_bytes = _abi.decode_workspace_bytes(self.L, c.n_decode, c.max_len)
+            if self.ws_bytes:
+                self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    # -- the three stages, separately callable for timing ------------------------------------------
+    def rope(self, stream=None):
+        c = self.call
+        _abi.rope_tables_build(self.rs, c.tok_pos, c.tok_seq_len, c.n_tokens, self.cos, self.sin, stream)
+
+    def cache_update(self, stream=None):
+        c = self.call
+        _abi.kv_cache_update(self.L, c.q, c.k, c.v, c.n_tokens, c.tok_rows, c.tok_pos, self.cos, self.sin,
+                             self.q_rot, c.k_cache, c.v_cache, c.num_rows, c.max_len, stream)
+
+    def prefill(self, stream=None):
+        c = self.call
+        if c.n_prefill:
+            _abi.attn_prefill(self.L, self.q_rot, c.n_prefill, c.k_cache, c.v_cache, c.num_rows, c.max_len,
+                              len(c.pf_rows), c.q_start, c.pf_rows, c.pf_first_pos, c.max_q_len, None, self.out,
+                              None, 0, stream)
+
+    def decode(self, stream=None):
+        c = self.call
+        if c.n_decode:
+            _abi.attn_decode(self.L, self.q_rot[c.n_prefill:], c.k_cache, c.v_cache, c.num_rows, c.max_len,
+                             c.n_decode, c.dec_rows, c.dec_pos, None, self.out[c.n_prefill:], self.workspace,
+                             self.ws_bytes, stream)
+
+    def run(self, stream=None):
+        self.rope(stream)
+        self.cache_update(stream)
+        self.prefill(stream)
+        self.decode(stream)
+        return self.out
+
+    def kernel_launches(self):
+        """Kernels one run() enqueues (rope tables, cache update, prefill, decode + merge)."""
+        c = self.call
+        n = (1 if c.n_tokens else 0) * 2
+        if c.n_prefill:
+            n += 1
+        if c.n_decode:
+            n += 2 if self.workspace is not None else 1
+        return n

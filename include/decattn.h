@@ -1,0 +1,216 @@
+/*
+ * decattn.h -- C ABI of the GB300 (sm_103a) attention step of a rotary, grouped-query decoder layer.
+ *
+ * The step is the part of DecoderAttention.forward between the q/k/v projections and o_proj, as the page
+ * "42. More models: a registry, scaled RoPE, sliding windows and latent attention" (section "What differs
+ * between model families") writes it:
+ *
+ *     q, k = q_norm(q), k_norm(k)            (optional per-head RMSNorm; Qwen3)
+ *     q, k = apply_rope(q, cos, sin), ...    (RoPE with the model's frequency scaling)
+ *     k, v, key_positions = cache.update(layer, k, v, positions, rows)
+ *     allowed = window_mask(qp, kp, sliding_window)          (only on windowed layers)
+ *     y = causal_attention(q, k, v, positions, key_positions, allowed)
+ *
+ * Four calls carry it: da_rope_tables_build (cos/sin per token), da_kv_cache_update (norm + RoPE + cache
+ * write), da_attn_prefill and da_attn_decode (attention over the cache).
+ *
+ * Conventions shared by every call:
+ *  - Pointers marked "device" are CUDA device (or managed) memory; "host" pointers are read during the call
+ *    only. The caller owns every buffer; the library allocates no memory and frees none.
+ *  - Every call is asynchronous on `stream` and returns after enqueueing. Arguments that can be checked on the
+ *    host are checked before anything is enqueued; a failed check returns a negative code, enqueues nothing
+ *    and leaves a message for da_last_error(). Index violations found on the device (a row, position or
+ *    slot out of range) skip the offending access and set a device error word, which da_check_device_error
+ *    reports.
+ *  - Tensor layouts are dense and row-major (last index fastest):
+ *      q, q_rot, out      [N, Hq, d]      one row per token
+ *      k, v               [N, Hkv, d]
+ *      k_cache, v_cache   [R, Hkv, M, d]  R cache rows (sequences), M positions per row; the slot of a
+ *                                          key is its position (slot index = position)
+ *      cos, sin           [N, r/2] fp32   r = rotary_dim
+ *    Element type: bf16 (DA_BF16) or fp32 (DA_FP32) for q/k/v/caches/out, as da_layer.dtype says.
+ *  - Window: w = da_layer.window; 0 means full attention. A key at position j is visible to a query at
+ *    position p iff j <= p and, when w > 0, p - j <= w - 1 (page 1, "Sliding windows": keys more than w - 1
+ *    positions back are masked).
+ *  - GQA: query head h reads KV head floor(h / (Hq / Hkv)).
+ */
+#ifndef DECATTN_H
+#define DECATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define DA_OK                 0
+#define DA_ERR_INVALID_ARG   (-1)   /* a host-checkable argument is out of range or inconsistent   */
+#define DA_ERR_UNSUPPORTED   (-2)   /* a valid configuration this library does not implement      */
+#define DA_ERR_CUDA          (-3)   /* a CUDA runtime call failed (message names it)              */
+#define DA_ERR_DEVICE_INDEX  (-4)   /* da_check_device_error: a kernel met an out-of-range index   */
+#define DA_ERR_TIMEOUT       (-5)   /* da_check_device_error: a kernel gave up a bounded wait      */
+
+/* RoPE frequency scaling kinds (page 1, "Scaled RoPE", rope_inv_freq; "Model resolution", Overview,
+ * for longrope). */
+typedef enum {
+    DA_ROPE_DEFAULT  = 0,   /* base_i = theta^(-2i/r)                                              */
+    DA_ROPE_LINEAR   = 1,   /* base / factor                                                       */
+    DA_ROPE_LLAMA3   = 2,   /* keep short wavelengths, divide long ones by factor, blend between   */
+    DA_ROPE_LONGROPE = 3,   /* base / short_factor_i, or base / long_factor_i past the original    */
+                            /* context; cos and sin times the attention factor                     */
+    DA_ROPE_YARN     = 4    /* ramp between beta_fast/beta_slow pairs; attention factor (mscale)   */
+} da_rope_kind;
+
+typedef enum { DA_BF16 = 0, DA_FP32 = 1 } da_dtype;
+
+/* The rope_scaling dict of config.json plus rope_theta and the rotated width. */
+typedef struct {
+    int    kind;                              /* da_rope_kind                                        */
+    double theta;                             /* rope_theta (> 1)                                    */
+    int    rotary_dim;                        /* r: even, 2 <= r <= 256 (d * partial_rotary_factor) */
+    double factor;                            /* linear, llama3, yarn (yarn: <= 0 means            */
+                                              /*   max_position_embeddings / original)              */
+    double low_freq_factor, high_freq_factor; /* llama3                                              */
+    int    original_max_position_embeddings;  /* llama3, longrope, yarn                              */
+    int    max_position_embeddings;           /* longrope and yarn: derives the attention factor     */
+    const double* short_factor;               /* longrope: host, r/2 values (per-pair divisors)      */
+    const double* long_factor;                /* longrope: host, r/2 values                          */
+    double attention_factor;                  /* <= 0: derive (1; longrope sqrt(1 + ln s / ln orig)  */
+                                              /*   with s = max / orig; yarn 0.1 ln s + 1)           */
+    double beta_fast, beta_slow;              /* yarn: <= 0 means 32 and 1                           */
+    double mscale, mscale_all_dim;            /* yarn: both > 0 selects the ratio form               */
+    int    truncate;                          /* yarn: nonzero rounds the ramp ends outwards         */
+} da_rope_scaling;
+
+/* The per-layer switches of the attention step (page 1, DecoderConfig / DecoderAttention.__init__). */
+typedef struct {
+    int         dtype;                        /* da_dtype of q, k, v, q_rot, caches and out          */
+    int         head_dim;                     /* d: 64 or 128                                        */
+    int         num_attention_heads;          /* Hq                                                   */
+    int         num_key_value_heads;          /* Hkv, divides Hq                                      */
+    int         rotary_dim;                   /* r: even, 2 <= r <= d                                 */
+    const float* q_norm_w;                    /* device [d] fp32, or NULL for no q/k norm (the pages: */
+    const float* k_norm_w;                    /*   "absent, not identity"); both or neither          */
+    double      eps;                          /* RMSNorm epsilon                                      */
+    int         window;                       /* sliding window w >= 0 (0 = full attention)           */
+    float       softcap;                      /* logit soft-cap c >= 0: z -> c tanh(z / c); 0 = off    */
+    float       scale;                        /* softmax scale; 0 means 1/sqrt(d)                     */
+} da_layer;
+
+/*
+ * da_rope_tables_build -- cos/sin of each token's rotation angles (page 1, "Scaled RoPE": rope_inv_freq
+ * and rope_tables).
+ *
+ * Frequencies inv_i (i < r/2) follow rs->kind; for token t at position p = positions[t]:
+ *     cos[t, i] = cos(p * inv_i) * af,   sin[t, i] = sin(p * inv_i) * af
+ * The angle p * inv_i is formed in fp64 and reduced modulo 2 pi before the fp32 sine/cosine.
+ * LongRoPE picks its long table for a token whose sequence length seq_len[t] (the total length of its
+ * sequence after this step) exceeds original_max_position_embeddings, its short table otherwise.
+ *
+ *   positions  device int32 [n], each >= 0
+ *   seq_len    device int32 [n]; required for DA_ROPE_LONGROPE, ignored (may be NULL) otherwise
+ *   cos, sin   device fp32 [n, r/2], written
+ * Errors: DA_ERR_INVALID_ARG (NULL pointers, n < 0, bad theta/factors/rotary_dim, missing longrope tables),
+ *         DA_ERR_UNSUPPORTED (unknown kind). n == 0 enqueues nothing.
+ */
+int da_rope_tables_build(const da_rope_scaling* rs, const int32_t* positions, const int32_t* seq_len,
+                         int n, float* cos, float* sin, cudaStream_t stream);
+
+/*
+ * da_kv_cache_update -- per-head q/k RMSNorm (when the layer has norm weights), RoPE on q and k, and the
+ * cache write (page 1, DecoderAttention.forward: q_norm/k_norm, apply_rope, cache.update(layer, k, v,
+ * positions, rows); page "MoE, optimisers, decoding", §3.3 KVCache.update and §4 Rotary).
+ *
+ * For each token t and head:  x <- x / sqrt(mean(x^2) + eps) * w      (optional)
+ *                             x'_i       = x_i c_i - x_{i+r/2} s_i     (i < r/2)
+ *                             x'_{i+r/2} = x_{i+r/2} c_i + x_i s_i;    dims >= r pass through
+ * then  q_rot[t] = q', k_cache[rows[t], g, positions[t], :] = k'_g, v_cache[rows[t], g, positions[t], :] = v_g
+ * (v copied bit for bit). Arithmetic in fp32; bf16 outputs are rounded to nearest even.
+ *
+ *   q, k, v       device [N, Hq, d], [N, Hkv, d], [N, Hkv, d]
+ *   rows          device int32 [n], each in [0, num_rows)
+ *   positions     device int32 [n], each in [0, max_len)
+ *   cos, sin      device fp32 [n, r/2] from da_rope_tables_build
+ *   q_rot         device [N, Hq, d], written; may be the same buffer as q
+ *   k_cache, v_cache  device [num_rows, Hkv, max_len, d], written at the (row, position) slots only
+ * Two tokens of one call must not name the same (row, position). A token whose row or position is out of
+ * range is skipped and sets DA_ERR_DEVICE_INDEX on the device.
+ */
+int da_kv_cache_update(const da_layer* layer, const void* q, const void* k, const void* v, int n,
+                       const int32_t* rows, const int32_t* positions, const float* cos, const float* sin,
+                       void* q_rot, void* k_cache, void* v_cache, int num_rows, int max_len,
+                       cudaStream_t stream);
+
+/*
+ * da_attn_prefill -- causal GQA attention of prefill chunks over their cache rows (page 1,
+ * DecoderAttention.forward: window_mask then causal_attention; "Model resolution" for soft-capping).
+ *
+ * Sequence b owns tokens q_start[b] .. q_start[b+1]-1 of q_rot/out, at positions first_pos[b] + i, and
+ * reads cache row rows[b]. Its keys are slots 0 .. first_pos[b] + n_b - 1 of that row (the chunk's own keys
+ * must already be written, e.g. by da_kv_cache_update). For query head h with KV head g:
+ *     z_j = scale * q_rot[t, h] . k_cache[row, g, j];   z_j = c tanh(z_j / c) when softcap c > 0
+ *     out[t, h] = sum_j softmax(z)_j v_cache[row, g, j]   over the visible j; 0 if none is visible
+ * bf16 layers run on the tcgen05 tensor cores (bf16 operands, fp32 accumulation and softmax); fp32 layers
+ * and calls with key_positions run a CUDA-core kernel in fp32.
+ *
+ *   q_rot          device [N, Hq, d];  n_tokens = N (= q_start[S]); rows past N are never read
+ *   n_seqs         number of chunks S >= 0
+ *   q_start        device int32 [S+1], nondecreasing, q_start[0] = 0
+ *   rows           device int32 [S];  first_pos  device int32 [S]
+ *   max_q_len      host int >= every chunk length (sizes the grid; chunks past it are not computed)
+ *   key_positions  device int32 [num_rows, max_len] or NULL. NULL: slot j holds position j. Otherwise slot j
+ *                  of a row holds the key at position key_positions[row, j] (negative = empty slot) and every
+ *                  slot of the row is scanned.
+ *   out            device [N, Hq, d], written for the chunks' tokens
+ *   workspace, ws_bytes  unused by prefill (pass NULL, 0)
+ * Caches must hold finite values in slots that a chunk reads; unwritten slots past a row's length are never
+ * allowed to affect the result.
+ */
+int da_attn_prefill(const da_layer* layer, const void* q_rot, int n_tokens, const void* k_cache, const void* v_cache,
+                    int num_rows, int max_len, int n_seqs, const int32_t* q_start, const int32_t* rows,
+                    const int32_t* first_pos, int max_q_len, const int32_t* key_positions, void* out,
+                    void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * da_attn_decode -- one new token per sequence attends over its cache row (the decode case of
+ * DecoderAttention.forward, page 1; a window bounds the keys read to w, page 1 "Sliding windows").
+ *
+ * Sequence s has one query q_rot[s] at position positions[s] in row rows[s]; it sees slots
+ * 0 .. positions[s] (its own key must already be written). Same arithmetic as da_attn_prefill. The bf16
+ * path splits the keys of each (sequence, KV head) into chunks processed in parallel, each chunk's partial
+ * softmax (max, sum, weighted values) going to `workspace`, then merges them in a fixed order (results
+ * are deterministic run to run).
+ *
+ *   q_rot      device [S, Hq, d];  rows, positions  device int32 [S]
+ *   key_positions  as in da_attn_prefill, or NULL
+ *   out        device [S, Hq, d]
+ *   workspace  device scratch of at least da_decode_workspace_bytes(layer, n_seqs, max_len) bytes,
+ *              16-byte aligned; its contents need no initialisation and are clobbered
+ */
+int da_attn_decode(const da_layer* layer, const void* q_rot, const void* k_cache, const void* v_cache,
+                   int num_rows, int max_len, int n_seqs, const int32_t* rows, const int32_t* positions,
+                   const int32_t* key_positions, void* out, void* workspace, size_t ws_bytes,
+                   cudaStream_t stream);
+
+/* Scratch bytes da_attn_decode needs for n_seqs sequences over a cache of max_len positions per row
+ * (0 when the layer is invalid or decode needs none). Pure host arithmetic. */
+size_t da_decode_workspace_bytes(const da_layer* layer, int n_seqs, int max_len);
+
+/* Waits for `stream`, then reads and clears the device error word that kernels set on an out-of-range
+ * index (DA_ERR_DEVICE_INDEX) or a bounded wait that gave up (DA_ERR_TIMEOUT). Returns DA_OK when clear,
+ * DA_ERR_CUDA if the wait itself failed. */
+int da_check_device_error(cudaStream_t stream);
+
+/* Message for the last nonzero return on the calling thread ("" if none). Owned by the library. */
+const char* da_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int da_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DECATTN_H */

@@ -1,0 +1,76 @@
+"""Run the fp64 oracle on one layer call of the synthetic workloads (TEST INFRASTRUCTURE ONLY).
+
+The call object is read by attribute (q, k, v, tok_rows, ... as the workload generator lays them out);
+nothing of the CUDA library is imported or called here.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import attention as A
+
+
+def _np64(t):
+    return t.detach().to("cpu").double().numpy()
+
+
+def _np_int(t):
+    return t.detach().to("cpu").numpy().astype(np.int64)
+
+
+def layer_of(call) -> A.Layer:
+    rot = A.rotary_dim(call.head_dim, call.partial_rotary_factor)
+    return A.Layer(head_dim=call.head_dim, num_attention_heads=call.num_attention_heads,
+                   num_key_value_heads=call.num_key_value_heads, rotary_dim=rot,
+                   q_norm_w=_np64(call.q_norm_w) if call.q_norm_w is not None else None,
+                   k_norm_w=_np64(call.k_norm_w) if call.k_norm_w is not None else None,
+                   eps=call.eps, window=call.window, softcap=call.softcap, scale=0.0)
+
+
+def spec_of(call) -> A.RopeSpec:
+    return A.RopeSpec(theta=call.rope_theta, scaling=call.rope_scaling,
+                      max_position_embeddings=call.max_position_embeddings)
+
+
+def rope_tables(call, positions=None, seq_len=None):
+    layer = layer_of(call)
+    pos = _np_int(call.tok_pos) if positions is None else np.asarray(positions)
+    lens = _np_int(call.tok_seq_len) if seq_len is None else np.asarray(seq_len)
+    return A.rope_tables_for_tokens(spec_of(call), layer.rotary_dim, pos, lens)
+
+
+def run_layer_call(call, key_positions=None):
+    """All results of one call at a size the oracle handles whole: cos, sin, q_rot, caches after the
+    update, and the attention output of every token (float64)."""
+    layer = layer_of(call)
+    cos, sin = rope_tables(call)
+    kc = _np64(call.k_cache).copy()
+    vc = _np64(call.v_cache).copy()
+    rows, pos = _np_int(call.tok_rows), _np_int(call.tok_pos)
+    q_rot = A.kv_cache_update(layer, _np64(call.q), _np64(call.k), _np64(call.v), rows, pos, cos, sin, kc, vc)
+    out = np.zeros_like(q_rot)
+    npf = call.n_prefill
+    kp = None if key_positions is None else _np_int(key_positions)
+    if npf:
+        out[:npf] = A.attn_prefill(layer, q_rot[:npf], kc, vc, _np_int(call.q_start), _np_int(call.pf_rows),
+                                   _np_int(call.pf_first_pos), key_positions=kp)
+    if call.n_tokens > npf:
+        out[npf:] = A.attn_decode(layer, q_rot[npf:], kc, vc, _np_int(call.dec_rows), _np_int(call.dec_pos),
+                                  key_positions=kp)
+    return {"cos": cos, "sin": sin, "q_rot": q_rot, "k_cache": kc, "v_cache": vc, "out": out}
+
+
+def rotate_tokens(call, token_ids):
+    """q_rot [n, Hq, d] and k_rot [n, Hkv, d] of the given tokens of the call (norm + RoPE), float64."""
+    layer = layer_of(call)
+    idx = np.asarray(token_ids, dtype=np.int64)
+    pos = _np_int(call.tok_pos)[idx]
+    lens = _np_int(call.tok_seq_len)[idx]
+    cos, sin = A.rope_tables_for_tokens(spec_of(call), layer.rotary_dim, pos, lens)
+    q = _np64(call.q[idx])
+    k = _np64(call.k[idx])
+    if layer.q_norm_w is not None:
+        q = A.rms_norm(q, layer.q_norm_w, layer.eps)
+        k = A.rms_norm(k, layer.k_norm_w, layer.eps)
+    c, s = cos[:, None, :], sin[:, None, :]
+    return A.apply_rope(q, c, s), A.apply_rope(k, c, s)
