@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 attention step through its C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
+
+One step = one pass of the whole step over one batch of synthetic input: da_rope_tables_build,
+da_kv_cache_update, then da_attn_prefill for the prefill chunks and da_attn_decode for the decode tokens,
+for every layer of the workload. Default workload: the Qwen3-8B-shaped prefill (4 x 2048 tokens, Hq 32,
+Hkv 8, d 128, q/k RMSNorm). Inputs are resident in HBM when timing starts; L2 (129 MB) is flushed by a
+256 MB write before every timed step, outside the timed events. Prints one JSON line (rank 0).
+
+Multi-GPU: the step does not exchange data between GPUs; N ranks run N independent replicas of the
+workload (weak scaling), and the time is the maximum over ranks.
+
+--impl reference times the fp64 CPU oracle (single-threaded) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn decode HBM GB/s (frac of peak); prefill attn TFLOP/s; tokens/s"
+DEFAULT_WORKLOAD = "qwen3_8b_prefill"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Bounded samples of each workload for the CPU oracle: (prefill chunk indices, decode token indices, KV heads
+# or None for all) per layer. "baseline" is the one-shot figure in the native line (about 5-30 s of one
+# core); "step" is what the reference arm repeats once per step, so that warm-up + steps end in minutes.
+ORACLE_SAMPLES = {
+    "baseline": {
+        "tiny_prefill_fp32": ([0], [], None),
+        "qwen3_8b_prefill": ([0], [], None),
+        "mistral_swa_decode": ([], list(range(16)), None),
+        "llama31_8b_long_decode": ([], [0, 1], None),
+        "phi4_gemma2_mixed": ([0], list(range(16)), None),
+    },
+    "step": {
+        "tiny_prefill_fp32": ([0], [], None),
+        "qwen3_8b_prefill": ([0], [], 1),
+        "mistral_swa_decode": ([], list(range(4)), None),
+        "llama31_8b_long_decode": ([], [0], 1),
+        "phi4_gemma2_mixed": ([0], list(range(4)), 1),
+    },
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)   # internal: child process
+    ap.add_argument("--sample-kind", default="baseline", help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and workload, if the kernel's
+    source is unchanged since the capture (the summary records the source's sha256); else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if line.startswith("<!-- ") and "=" in line:
+            k, v = line[5:].rstrip().rstrip("-> ").split("=", 1)
+            fields[k.strip()] = v.strip()
+    src = fields.get("source")
+    if not src or "dram_bytes_per_launch" not in fields:
+        return None
+    digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()
+    if digest != fields.get("source_sha256"):
+        return None
+    return int(float(fields["dram_bytes_per_launch"]))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "50", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [ln.split(", ") for ln in out.strip().splitlines() if ln.count(",") >= 8]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "window": "warm-up and timed steps"}
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def reduce_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def headline(work, seconds):
+    """(value, unit, tokens/s) of `work` done in `seconds`: TFLOP/s when the step has prefill, else GB/s."""
+    if work["prefill_flops"] > 0:
+        return (work["prefill_flops"] + work["decode_flops"]) / seconds / 1e12, "TFLOP/s", work["tokens"] / seconds
+    return work["decode_bytes"] / seconds / 1e9, "GB/s", work["tokens"] / seconds
+
+
+# ---------------------------------------------------------------------------------------------- oracle leg
+
+def oracle_sample_child(workload, kind, iters):
+    """Runs in a fresh single-threaded process: builds the workload once, times the oracle `iters` times on
+    the bounded sample, prints one JSON line with the per-iteration seconds."""
+    import torch
+
+    from decoder_attention_gb300 import inputs, work as W
+    from oracle import step as ostep
+    torch.set_num_threads(1)
+    chunks, dec, kvh = ORACLE_SAMPLES[kind][workload]
+    num = inputs.NUMBERS[workload]
+    gen_dev = "cuda" if (num in (3, 4, 5) and torch.cuda.is_available()) else "cpu"
+    wl = inputs.make(num, scale="full", device=gen_dev)
+    samples = [inputs.subset(c, chunks, dec, device="cpu", kv_heads=kvh) for c in wl.layers]
+    del wl
+    tot = {}
+    for s in samples:
+        for k, v in W.layer_call_work(s).items():
+            tot[k] = tot.get(k, 0) + v
+    secs = []
+    for _ in range(iters):
+        t0 = time.perf_counter()
+        for s in samples:
+            ostep.run_layer_call(s)
+        secs.append(time.perf_counter() - t0)
+    heads = "all heads" if kvh is None else f"{kvh} KV head(s) and their query heads"
+    desc = (f"{len(chunks)} prefill chunk(s) and {len(dec)} decode token(s), {heads}, per layer x {len(samples)} "
+            f"layer(s); single-threaded fp64 numpy")
+    print(json.dumps({"seconds": secs, "sample": desc, "work": tot}))
+
+
+def run_oracle_sample(workload, kind="baseline", iters=1):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", workload,
+                          "--sample-kind", kind, "--steps", str(iters)],
+                         capture_output=True, text=True, env=env, timeout=1800)
+    if res.returncode != 0:
+        raise RuntimeError(f"oracle sample failed:\n{res.stderr[-2000:]}")
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def main_reference(args):
+    rank, world, _ = dist_init(args)
+    if rank != 0:
+        return 0
+    from decoder_attention_gb300 import inputs
+    r = run_oracle_sample(args.workload, "step", args.warmup + args.steps)
+    sec = statistics.mean(r["seconds"][args.warmup:])
+    value, unit, tps = headline(r["work"], sec)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "number": inputs.NUMBERS[args.workload], "sample": r["sample"]},
+            "tokens_per_s": tps,
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": r["sample"],
+                             "host_cores": os.cpu_count()},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------------------------- native leg
+
+def main_native(args):
+    import torch
+
+    from decoder_attention_gb300 import _abi, inputs, step as S, work as W
+
+    rank, world, local = dist_init(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    num = inputs.NUMBERS[args.workload]
+    wl = inputs.make(num, scale="full", device=dev)
+    steps = [S.AttentionStep(c) for c in wl.layers]
+    work = W.workload_work(wl)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run_step():
+        for st in steps:
+            st.run()
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    clocks.mark_start()
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        run_step()
+    torch.cuda.synchronize()
+    _abi.check_device_error()
+
+    # ------------------------------------------------------------------ timed region
+    n_layers = len(steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(1 + 3 * n_layers)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        e = ev[i]
+        e[0].record(stream)
+        for li, st in enumerate(steps):
+            st.rope()
+            st.cache_update()
+            e[1 + 3 * li].record(stream)
+            st.prefill()
+            e[2 + 3 * li].record(stream)
+            st.decode()
+            e[3 + 3 * li].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks.mark_end()
+    _abi.check_device_error()
+    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
+    pf_ms = [sum(e[1 + 3 * li].elapsed_time(e[2 + 3 * li]) for li in range(n_layers)) for e in ev]
+    dec_ms = [sum(e[2 + 3 * li].elapsed_time(e[3 + 3 * li]) for li in range(n_layers)) for e in ev]
+    pre_ms = [sum((e[0] if li == 0 else e[3 * li]).elapsed_time(e[1 + 3 * li]) for li in range(n_layers)) for e in ev]
+    ms = statistics.mean(step_ms)
+    ms_all = reduce_max(ms, world)
+    clock_info = clocks.stop()
+
+    value_1, unit, _ = headline(work, ms_all / 1e3)
+    value = value_1 * world
+    tokens_per_s = work["tokens"] * world / (ms_all / 1e3)
+
+    peaks, peak_kind = load_peaks()
+    if work["prefill_flops"] > 0:
+        kms = statistics.mean(pf_ms)
+        achieved = work["prefill_flops"] / (kms / 1e3) / 1e12
+        roof = {"kernel": "prefill_kernel (tcgen05)", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "peak_kind": f"bf16 dense burst, of {peak_kind}", "launch_ms": kms,
+                "algorithmic_flops_per_launch": work["prefill_flops"] / n_layers,
+                "traffic": load_traffic("prefill_kernel", args.workload)}
+    else:
+        kms = statistics.mean(dec_ms)
+        achieved = work["decode_bytes"] / (kms / 1e3) / 1e9
+        roof = {"kernel": "decode_kernel + merge_kernel (one da_attn_decode call)", "bound": "hbm",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_kind": f"HBM copy, of {peak_kind}", "launch_ms": kms,
+                "algorithmic_bytes_per_launch": work["decode_bytes"] / n_layers,
+                "traffic": load_traffic("decode_kernel", args.workload)}
+
+    # ------------------------------------------------------------------ end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        names = ["q", "k", "v", "tok_rows", "tok_pos", "tok_seq_len", "q_start", "pf_rows", "pf_first_pos",
+                 "dec_rows", "dec_pos"]
+        host_in = [[getattr(st.call, n).cpu().pin_memory() for n in names] for st in steps]
+        host_out = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for st in steps]
+        h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            for st, hs, ho in zip(steps, host_in, host_out):
+                for n, h in zip(names, hs):
+                    getattr(st.call, n).copy_(h, non_blocking=True)
+                st.run()
+                ho.copy_(st.out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 50))
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            flush.zero_()
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        # the flush is not part of the step: time it alone and take it out
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(n_e2e):
+            flush.zero_()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = (e0.elapsed_time(e1) - f0.elapsed_time(f1)) / n_e2e
+        e2e_ms = reduce_max(e2e_ms, world)
+        v, u, _ = headline(work, e2e_ms / 1e3)
+        e2e = {"value": v * world, "unit": u, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms, "via": "AttentionStep.run (C ABI) with pinned host inputs/outputs"}
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            r = run_oracle_sample(args.workload, "baseline", 1)
+            v, u, _ = headline(r["work"], r["seconds"][0])
+            cpu_base = {"value": v, "unit": u, "cores": 1, "kind": "oracle", "sample": r["sample"],
+                        "seconds": r["seconds"][0], "host_cores": os.cpu_count()}
+        except Exception as exc:  # reported, not fatal
+            cpu_base = {"value": None, "unit": unit, "cores": 1, "kind": "oracle", "error": str(exc)[-300:]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if wl.layers[0].dtype == torch.bfloat16 else "fp32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "number": num, "description": wl.description,
+                       "l2": "flushed (256 MB write) before every timed step, outside the step's events",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tokens_per_s": tokens_per_s,
+            "breakdown_ms": {"rope_and_cache_update": statistics.mean(pre_ms), "prefill": statistics.mean(pf_ms),
+                             "decode": statistics.mean(dec_ms), "wall_ms_per_step_incl_flush": wall * 1e3 / args.steps},
+            "work": {k: v for k, v in work.items() if v},
+            "roofline": roof,
+            "e2e": e2e,
+            "gpu_launches": sum(st.kernel_launches() for st in steps) * args.steps,
+            "clocks": clock_info,
+            "cpu_baseline": cpu_base,
+            "peaks": dict(peaks, kind=peak_kind),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_sample:
+        oracle_sample_child(args.workload, args.sample_kind, args.steps)
+        return 0
+    if args.impl == "reference":
+        return main_reference(args)
+    return main_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

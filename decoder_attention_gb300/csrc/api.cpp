@@ -253,8 +253,9 @@ int da_kv_cache_update(const da_layer* L, const void* q, const void* k, const vo
   if (!q || !k || !v || !rows || !positions || !cos || !sin || !q_rot || !k_cache || !v_cache)
     return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache))
-    return fail(DA_ERR_INVALID_ARG, "q, k, v, q_rot and the caches must be 16-byte aligned");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(cos) || !aligned16(sin) || !aligned16(L->q_norm_w) || !aligned16(L->k_norm_w))
+    return fail(DA_ERR_INVALID_ARG, "q, k, v, q_rot, the caches, cos/sin and the norm weights must be 16-byte aligned");
   int* err = da::error_word_ptr();
   if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
   da::KvUpdateArgs a;

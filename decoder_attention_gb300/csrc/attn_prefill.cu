@@ -6,13 +6,17 @@
 // query row, softmax over its visible keys of scale * q.k (optionally c * tanh(. / c)), times V.
 //
 // CTA = 256 query rows (two 128-row tiles Q0, Q1) of one (sequence, query head). Key tiles of 128 keys
-// stream through a 2-stage shared-memory ring by TMA (128-byte swizzle). Roles:
-//   warp 8      TMA producer (Q once, then K and V tiles)
-//   warp 9      MMA issuer: S_w = Q_w K^T into TMEM, then O_w += P_w V with P_w read from TMEM
-//   warps 10-11 idle (they complete the third warpgroup, which setmaxnreg works on)
+// stream by TMA (128-byte swizzle) through a 3-stage K ring and a 2-stage V ring. Roles:
+//   warp 8      TMA producer of Q (once) and K tiles
+//   warp 10     TMA producer of V tiles
+//   warp 9      MMA issuer (one thread): S_w = Q_w K^T into TMEM; O_w += P_w V with P_w read from TMEM
+//   warp 11     idle (completes the third warpgroup, which setmaxnreg works on)
 //   warps 0-3   softmax of Q0 rows, warps 4-7 softmax of Q1 rows: one thread per row; S row from TMEM,
-//               mask (only on tiles that need it), online softmax in fp32 (log2 domain, rescale of O
-//               only when the running max grows by more than 2^8), P written back into TMEM as bf16
+//               mask only on tiles that need it, online softmax in fp32 (log2 domain; O is rescaled only
+//               when the running max grows by more than 2^8), P written back into TMEM as bf16
+// MMA order per key tile j:  PV0(j), S0(j+1), PV1(j), S1(j+1)  -- so the softmax of one Q tile runs while
+// the tensor core works on the other tile's PV and next S. S0(j+1) overwrites the TMEM columns of P0(j);
+// tcgen05.mma instructions of one thread execute in issue order, so PV0(j) has read P0(j) by then.
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512). Key tiles outside every query's
 // causal window are never loaded (the loop starts at the first tile inside the oldest query's window),
 // so a windowed layer costs O(w) per query. Every mbarrier wait is bounded; a wait that gives up sets
@@ -30,20 +34,30 @@ constexpr int BM = 128;             // rows per Q tile
 constexpr int BN = 128;             // keys per K/V tile
 constexpr int D = 128;
 constexpr int NQT = 2;              // Q tiles per CTA
-constexpr int NST = 2;              // K/V ring stages
-constexpr int THREADS = 384;     // 3 warpgroups: softmax Q0, softmax Q1, producer/MMA
-// setmaxnreg split: launched at 168 per thread (384 x 168 = 64512); softmax warpgroups rise to 224 and
-// the producer/MMA warpgroup drops to 56: 256 x 224 + 128 x 56 = 64512, the launch total.
-constexpr int REGS_SOFTMAX = 224;
-constexpr int REGS_CTRL = 56;
+constexpr int NK = 3;               // K ring stages
+constexpr int NV = 2;               // V ring stages
+constexpr int THREADS = 384;        // 3 warpgroups: softmax Q0, softmax Q1, producers/MMA
+// setmaxnreg split: launched at 168 per thread (384 x 168 = 64512); softmax warpgroups rise to 216 and
+// the producer/MMA warpgroup drops to 72: 256 x 216 + 128 x 72 = 64512, the launch total (per SMSP, one
+// warp of each warpgroup: 216 + 216 + 72 = 504 of 512 registers per lane).
+#ifndef DA_PF_REGS_SOFTMAX
+#define DA_PF_REGS_SOFTMAX 216
+#define DA_PF_REGS_CTRL 72
+#endif
+constexpr int REGS_SOFTMAX = DA_PF_REGS_SOFTMAX;
+constexpr int REGS_CTRL = DA_PF_REGS_CTRL;
+static_assert(256 * REGS_SOFTMAX + 128 * REGS_CTRL == 384 * 168, "register split must match the launch total");
 constexpr int HALF = 128 * 128;     // bytes of a 64-wide half of a 128-row tile (16 KB)
 constexpr int TILE = 2 * HALF;      // 32 KB
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + NQT * TILE;
-constexpr int OFF_V = OFF_K + NST * TILE;
-constexpr int OFF_BAR = OFF_V + NST * TILE;
-constexpr int N_BARS = 1 + 3 * NST + 2 * NQT + 1;
+constexpr int OFF_V = OFF_K + NK * TILE;
+constexpr int OFF_BAR = OFF_V + NV * TILE;
+// barriers: q, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[NQT], p_full[NQT], o_done
+constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NK, B_VF = B_KE + NK, B_VE = B_VF + NV, B_SF = B_VE + NV,
+              B_PF = B_SF + NQT, B_OD = B_PF + NQT, N_BARS = B_OD + 1;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + TMEM address slot + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: stale max allowed to lag by up to x256
@@ -72,19 +86,46 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
-struct TileInfo {
-  int valid[NQT];      // Q tile has at least one real row
-  int pmin[NQT], pmax[NQT];
-  int tb[NQT], te[NQT];
-  int tbeg, tend;
-  __device__ bool active(int w, int t) const { return valid[w] && t >= tb[w] && t <= te[w]; }
-};
+// One pass over a row's 128 scores: soft-cap (CAP), mask to the visible column range [lo_c, hi_c] (MASK),
+// and the row max with 8 independent partial maxima (one running max would be a 128-long dependency chain).
+template <bool CAP, bool MASK>
+__device__ __forceinline__ float row_pass(uint32_t (&zr)[BN], float cap_in, float cap_l2, int lo_c, int hi_c) {
+  float mx[8];
+#pragma unroll
+  for (int c = 0; c < BN; ++c) {
+    float v = __uint_as_float(zr[c]);
+    if (CAP) v = cap_l2 * tanh_fast(v * cap_in);
+    if (MASK) v = (c >= lo_c && c <= hi_c) ? v : -CUDART_INF_F;
+    zr[c] = __float_as_uint(v);
+    mx[c & 7] = c < 8 ? v : fmaxf(mx[c & 7], v);
+  }
+  return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+}
+
+// The 8 MMAs (K = 16 each) of S = Q K^T for one 128 x 128 tile; both operands K-major, 128-byte swizzled
+// in two 64-wide halves.
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+    mma_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// The 8 MMAs (K = 16 keys each) of O (+)= P V; P from TMEM (bf16, 2 per column), V MN-major in smem.
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(BM, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk)
+    mma_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 2048, HALF, 1024), idesc, (accumulate || kk > 0) ? 1u : 0u);
+}
 
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmq,
                                                              const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
                                                              const Params prm) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ int abort_flag;
 
@@ -110,46 +151,51 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   const int g = h / (prm.hq / prm.hkv);
   const int window = prm.window;
 
-  TileInfo ti;
-#pragma unroll
-  for (int w = 0; w < NQT; ++w) {
-    const int r0 = q0 + w * BM;
-    ti.valid[w] = r0 < n_b;
-    const int nr = ti.valid[w] ? min(BM, n_b - r0) : 1;
-    ti.pmin[w] = fp + r0;
-    ti.pmax[w] = fp + r0 + nr - 1;
-    const int lo = window > 0 ? max(0, ti.pmin[w] - window + 1) : 0;
-    ti.tb[w] = lo / BN;
-    ti.te[w] = ti.pmax[w] / BN;
+  // Key-tile range of each Q tile: from the tile holding the oldest query's first visible key to the tile
+  // holding the newest query's own key. Q0's range starts no later and ends no later than Q1's.
+  bool valid0, valid1;
+  int pmin0, pmax0, pmin1, pmax1, tb0, te0, tb1, te1;
+  {
+    auto range = [&](int w, bool& valid, int& pmin, int& pmax, int& tb, int& te) {
+      const int r0 = q0 + w * BM;
+      valid = r0 < n_b;
+      const int nr = valid ? min(BM, n_b - r0) : 1;
+      pmin = fp + r0;
+      pmax = fp + r0 + nr - 1;
+      const int lo = window > 0 ? max(0, pmin - window + 1) : 0;
+      tb = lo / BN;
+      te = pmax / BN;
+    };
+    range(0, valid0, pmin0, pmax0, tb0, te0);
+    range(1, valid1, pmin1, pmax1, tb1, te1);
   }
-  ti.tbeg = ti.tb[0];
-  ti.tend = ti.valid[1] ? ti.te[1] : ti.te[0];
-  const int n_tiles = ti.tend - ti.tbeg + 1;
+  const int tbeg = tb0;
+  const int tend = valid1 ? te1 : te0;
+  const int n_tiles = tend - tbeg + 1;
+  auto act0 = [&](int t) { return t >= tb0 && t <= te0; };
+  auto act1 = [&](int t) { return valid1 && t >= tb1 && t <= te1; };
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar = sbase + OFF_BAR;
-  const uint32_t bar_q = bar;
-  auto bar_kfull = [&](int st) { return bar + 8u * (1 + st); };
-  auto bar_vfull = [&](int st) { return bar + 8u * (1 + NST + st); };
-  auto bar_empty = [&](int st) { return bar + 8u * (1 + 2 * NST + st); };
-  auto bar_sfull = [&](int w) { return bar + 8u * (1 + 3 * NST + w); };
-  auto bar_pfull = [&](int w) { return bar + 8u * (1 + 3 * NST + NQT + w); };
-  const uint32_t bar_odone = bar + 8u * (1 + 3 * NST + 2 * NQT);
+  auto B = [&](int i) { return bar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + N_BARS * 8);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(bar_q, 1);
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(bar_kfull(i), 1);
-      mbar_init(bar_vfull(i), 1);
-      mbar_init(bar_empty(i), 1);
+    mbar_init(B(B_Q), 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(B(B_KF + i), 1);
+      mbar_init(B(B_KE + i), 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(B(B_VF + i), 1);
+      mbar_init(B(B_VE + i), 1);
     }
     for (int w = 0; w < NQT; ++w) {
-      mbar_init(bar_sfull(w), 1);
-      mbar_init(bar_pfull(w), BM);
+      mbar_init(B(B_SF + w), 1);
+      mbar_init(B(B_PF + w), BM);
     }
-    mbar_init(bar_odone, 1);
+    mbar_init(B(B_OD), 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -161,95 +207,115 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const volatile int* vabort = &abort_flag;
+  const int plane = (row * prm.hkv + g) * prm.max_len;
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
     if (warp == 8 && lane == 0) {
-    // ---------------------------------------------------------------- TMA producer
+      // ---------------------------------------------------------------- TMA producer: Q, then K tiles
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
-      prefetch_tmap(&tmv);
-      const int nq = ti.valid[1] ? 2 : 1;
-      mbar_arrive_expect_tx(bar_q, nq * TILE);
+      const int nq = valid1 ? 2 : 1;
+      mbar_arrive_expect_tx(B(B_Q), nq * TILE);
       for (int w = 0; w < nq; ++w) {
         const int tok = t0 + q0 + w * BM;
-        tma_load_3d(sbase + OFF_Q + w * TILE, &tmq, bar_q, 0, h, tok);
-        tma_load_3d(sbase + OFF_Q + w * TILE + HALF, &tmq, bar_q, 64, h, tok);
+        tma_load_3d(sbase + OFF_Q + w * TILE, &tmq, B(B_Q), 0, h, tok);
+        tma_load_3d(sbase + OFF_Q + w * TILE + HALF, &tmq, B(B_Q), 64, h, tok);
       }
-      const int plane = (row * prm.hkv + g) * prm.max_len;
       int issued = 0;
       for (int i = 0; i < n_tiles && !*vabort; ++i) {
-        const int st = i % NST;
-        if (i >= NST && !mbar_wait(bar_empty(st), ((i / NST) + 1) & 1, prm.err)) {
+        const int st = i % NK;
+        if (i >= NK && !mbar_wait(B(B_KE + st), ((i / NK) + 1) & 1, prm.err)) {
           abort_flag = 1;
           break;
         }
-        const int key = plane + (ti.tbeg + i) * BN;
-        mbar_arrive_expect_tx(bar_kfull(st), TILE);
-        tma_load_2d(sbase + OFF_K + st * TILE, &tmk, bar_kfull(st), 0, key);
-        tma_load_2d(sbase + OFF_K + st * TILE + HALF, &tmk, bar_kfull(st), 64, key);
-        mbar_arrive_expect_tx(bar_vfull(st), TILE);
-        tma_load_2d(sbase + OFF_V + st * TILE, &tmv, bar_vfull(st), 0, key);
-        tma_load_2d(sbase + OFF_V + st * TILE + HALF, &tmv, bar_vfull(st), 64, key);
+        const int key = plane + (tbeg + i) * BN;
+        mbar_arrive_expect_tx(B(B_KF + st), TILE);
+        tma_load_2d(sbase + OFF_K + st * TILE, &tmk, B(B_KF + st), 0, key);
+        tma_load_2d(sbase + OFF_K + st * TILE + HALF, &tmk, B(B_KF + st), 64, key);
         ++issued;
       }
       // every issued copy must land before the CTA's shared memory is released
-      mbar_wait(bar_q, 0, prm.err);
-      for (int i = max(0, issued - NST); i < issued; ++i) {
-        mbar_wait(bar_kfull(i % NST), (i / NST) & 1, prm.err);
-        mbar_wait(bar_vfull(i % NST), (i / NST) & 1, prm.err);
+      mbar_wait(B(B_Q), 0, prm.err);
+      for (int i = max(0, issued - NK); i < issued; ++i) mbar_wait(B(B_KF + i % NK), (i / NK) & 1, prm.err);
+    } else if (warp == 10 && lane == 0) {
+      // ---------------------------------------------------------------- TMA producer: V tiles
+      prefetch_tmap(&tmv);
+      int issued = 0;
+      for (int i = 0; i < n_tiles && !*vabort; ++i) {
+        const int st = i % NV;
+        if (i >= NV && !mbar_wait(B(B_VE + st), ((i / NV) + 1) & 1, prm.err)) {
+          abort_flag = 1;
+          break;
+        }
+        const int key = plane + (tbeg + i) * BN;
+        mbar_arrive_expect_tx(B(B_VF + st), TILE);
+        tma_load_2d(sbase + OFF_V + st * TILE, &tmv, B(B_VF + st), 0, key);
+        tma_load_2d(sbase + OFF_V + st * TILE + HALF, &tmv, B(B_VF + st), 64, key);
+        ++issued;
       }
+      for (int i = max(0, issued - NV); i < issued; ++i) mbar_wait(B(B_VF + i % NV), (i / NV) & 1, prm.err);
     } else if (warp == 9 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issuer (one thread)
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);   // Q, K both K-major
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);     // P (TMEM), V MN-major
-      int nact[NQT] = {0, 0};
-      bool ok = mbar_wait(bar_q, 0, prm.err);
+      // ---------------------------------------------------------------- MMA issuer (one thread)
+      const uint32_t q0s = sbase + OFF_Q, q1s = sbase + OFF_Q + TILE;
+      const uint32_t s0t = tmem, s1t = tmem + BN, o0t = tmem + 256, o1t = tmem + 256 + D;
+      int npv0 = 0, npv1 = 0;
+      bool ok = mbar_wait(B(B_Q), 0, prm.err) && mbar_wait(B(B_KF), 0, prm.err);
       tc_fence_after();
+      if (ok) {
+        // prologue: scores of the first key tile
+        if (act0(tbeg)) {
+          issue_s(s0t, q0s, sbase + OFF_K);
+          tc_commit(B(B_SF + 0));
+        }
+        if (act1(tbeg)) {
+          issue_s(s1t, q1s, sbase + OFF_K);
+          tc_commit(B(B_SF + 1));
+        }
+        tc_commit(B(B_KE + 0));
+      }
       for (int i = 0; ok && i < n_tiles; ++i) {
         if (*vabort) break;
-        const int t = ti.tbeg + i;
-        const int st = i % NST;
-        const uint32_t ph = (i / NST) & 1;
-        if (!mbar_wait(bar_kfull(st), ph, prm.err)) { ok = false; break; }
+        const int t = tbeg + i;
+        const bool nxt = i + 1 < n_tiles;
+        const int kst1 = (i + 1) % NK;
+        const uint32_t k1s = sbase + OFF_K + kst1 * TILE;
+        const int vst = i % NV;
+        const uint32_t vs = sbase + OFF_V + vst * TILE;
+        if (!mbar_wait(B(B_VF + vst), (i / NV) & 1, prm.err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kb = sbase + OFF_K + st * TILE;
-        const bool act[NQT] = {ti.active(0, t), ti.active(1, t)};
-#pragma unroll
-        for (int w = 0; w < NQT; ++w) {
-          if (!act[w]) continue;
-          const uint32_t qb = sbase + OFF_Q + w * TILE;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-            mma_ss(tmem + w * BN, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_qk,
-                   kk > 0 ? 1u : 0u);
-          }
-          tc_commit(bar_sfull(w));
-        }
-        if (!mbar_wait(bar_vfull(st), ph, prm.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t vb = sbase + OFF_V + st * TILE;
-#pragma unroll
-        for (int w = 0; w < NQT; ++w) {
-          if (!act[w] || !ok) continue;
-          if (!mbar_wait(bar_pfull(w), nact[w] & 1, prm.err)) {
-            ok = false;
-            continue;
-          }
+        if (act0(t)) {
+          if (!mbar_wait(B(B_PF + 0), npv0 & 1, prm.err)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            mma_ts(tmem + 256 + w * D, tmem + w * BN + kk * 8, sdesc_sw128(vb + kk * 2048, HALF, 1024), idesc_pv,
-                   (nact[w] > 0 || kk > 0) ? 1u : 0u);
-          }
-          ++nact[w];
+          issue_pv(o0t, s0t, vs, npv0 > 0);
+          ++npv0;
         }
-        tc_commit(bar_empty(st));
+        if (nxt) {
+          if (!mbar_wait(B(B_KF + kst1), ((i + 1) / NK) & 1, prm.err)) { ok = false; break; }
+          tc_fence_after();
+          if (act0(t + 1)) {
+            issue_s(s0t, q0s, k1s);
+            tc_commit(B(B_SF + 0));
+          }
+        }
+        if (act1(t)) {
+          if (!mbar_wait(B(B_PF + 1), npv1 & 1, prm.err)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(o1t, s1t, vs, npv1 > 0);
+          ++npv1;
+        }
+        tc_commit(B(B_VE + vst));
+        if (nxt) {
+          if (act1(t + 1)) {
+            issue_s(s1t, q1s, k1s);
+            tc_commit(B(B_SF + 1));
+          }
+          tc_commit(B(B_KE + kst1));
+        }
       }
       if (!ok) abort_flag = 1;
-      tc_commit(bar_odone);
-      mbar_wait(bar_odone, 0, prm.err);   // all MMAs done before TMEM may be released
+      tc_commit(B(B_OD));
+      mbar_wait(B(B_OD), 0, prm.err);   // all MMAs done before TMEM may be released
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
@@ -264,22 +330,23 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const uint32_t t_s = tmem + lane_addr + w * BN;
     const uint32_t t_o = tmem + lane_addr + 256 + w * D;
     const float cap = prm.softcap;
-    const float zmul = cap > 0.f ? prm.scale / cap : prm.scale * kLog2e;
+    const float cap_in = cap > 0.f ? prm.scale / cap : 0.f;
     const float cap_l2 = cap * kLog2e;
-    const bool my_valid = w == 0 ? ti.valid[0] : ti.valid[1];
-    const int my_tb = w == 0 ? ti.tb[0] : ti.tb[1];
-    const int my_te = w == 0 ? ti.te[0] : ti.te[1];
-    const int my_pmin = w == 0 ? ti.pmin[0] : ti.pmin[1];
-    const int my_pmax = w == 0 ? ti.pmax[0] : ti.pmax[1];
+    const float zmul = cap > 0.f ? 1.f : prm.scale * kLog2e;   // z * zmul is the logit in log2 units
+    const bool my_valid = w == 0 ? true : valid1;
+    const int my_tb = w == 0 ? tb0 : tb1;
+    const int my_te = w == 0 ? te0 : te1;
+    const int my_pmin = w == 0 ? pmin0 : pmin1;
+    const int my_pmax = w == 0 ? pmax0 : pmax1;
     float m = -CUDART_INF_F, l = 0.f;
     int nact = 0;
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
-      const int t = ti.tbeg + i;
+      const int t = tbeg + i;
       if (!my_valid || t < my_tb || t > my_te) continue;
       // outcomes are made warp-uniform: the TMEM loads and stores below are warp-collective
       if (__any_sync(0xffffffffu, *vabort != 0)) { ok = false; break; }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sfull(w), nact & 1, prm.err))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(B(B_SF + w), nact & 1, prm.err))) {
         abort_flag = 1;
         ok = false;
         break;
@@ -292,19 +359,19 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       const int kstart = t * BN;
       const bool need_mask = !(kstart + BN - 1 <= my_pmin &&
                                (window == 0 || my_pmax - kstart <= window - 1) && kstart + BN <= kv_len);
-      float tmax = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        float v = __uint_as_float(zr[c]) * zmul;
-        if (cap > 0.f) v = cap_l2 * tanh_fast(v);
-        if (need_mask) {
-          const int j = kstart + c;
-          const bool vis = j <= p && (window == 0 || p - j <= window - 1) && j < kv_len;
-          v = vis ? v : -CUDART_INF_F;
-        }
-        zr[c] = __float_as_uint(v);
-        tmax = fmaxf(tmax, v);
+      // zr: the raw score q.k (scaled into log2 units inside the exponent), or for capped layers the
+      // capped logit already in log2 units. Visible keys of this row in the tile: columns [lo_c, hi_c].
+      const int hi_c = min(p, kv_len - 1) - kstart;
+      const int lo_c = window > 0 ? p - window + 1 - kstart : -BN;
+      float tmax;
+      if (cap > 0.f) {
+        tmax = need_mask ? row_pass<true, true>(zr, cap_in, cap_l2, lo_c, hi_c)
+                         : row_pass<true, false>(zr, cap_in, cap_l2, lo_c, hi_c);
+      } else {
+        tmax = need_mask ? row_pass<false, true>(zr, cap_in, cap_l2, lo_c, hi_c)
+                         : row_pass<false, false>(zr, cap_in, cap_l2, lo_c, hi_c);
       }
+      tmax *= zmul;
       const float m_new = fmaxf(m, tmax);
       const bool grow = m_new > m + kRescaleThreshold;
       float alpha = 1.f;
@@ -326,32 +393,35 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           tmem_st32(t_o + j * 32, ov);
         }
       }
-      const float mu = (m == -CUDART_INF_F) ? 0.f : m;
+      const float nmu = (m == -CUDART_INF_F) ? 0.f : -m;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < BN / 32; ++j) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float pa = ex2(__uint_as_float(zr[j * 32 + 2 * e]) - mu);
-          const float pb = ex2(__uint_as_float(zr[j * 32 + 2 * e + 1]) - mu);
-          l += pa + pb;
+          const float pa = ex2(fmaf(__uint_as_float(zr[j * 32 + 2 * e]), zmul, nmu));
+          const float pb = ex2(fmaf(__uint_as_float(zr[j * 32 + 2 * e + 1]), zmul, nmu));
+          ls[(2 * e) & 7] += pa;
+          ls[(2 * e + 1) & 7] += pb;
           pk[e] = pack_bf16(pa, pb);
         }
         tmem_st16(t_s + j * 16, pk);     // P (bf16, 2 per column) over the first half of the S columns
       }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tmem_wait_st();
       if (kstart + BN > kv_len) {
         // V rows past the row's last key hold whatever the cache holds there (maybe NaN); P is 0 there,
         // but 0 * NaN is NaN, so zero those rows before the tensor core reads them (after the V copy has
         // landed; the stage cannot be refilled before this tile's PV, which waits for us).
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_vfull(i % NST), (i / NST) & 1, prm.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(B(B_VF + i % NV), (i / NV) & 1, prm.err))) {
           abort_flag = 1;
           ok = false;
           break;
         }
         if (kstart + r >= kv_len) {
-          uint4* vrow0 = reinterpret_cast<uint4*>(smem + OFF_V + (i % NST) * TILE + r * 128);
-          uint4* vrow1 = reinterpret_cast<uint4*>(smem + OFF_V + (i % NST) * TILE + HALF + r * 128);
+          uint4* vrow0 = reinterpret_cast<uint4*>(smem + OFF_V + (i % NV) * TILE + r * 128);
+          uint4* vrow1 = reinterpret_cast<uint4*>(smem + OFF_V + (i % NV) * TILE + HALF + r * 128);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             vrow0[e] = make_uint4(0, 0, 0, 0);
@@ -361,11 +431,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(bar_pfull(w));
+      mbar_arrive(B(B_PF + w));
       ++nact;
     }
     // ------------------------------------------------------------ epilogue: O / l -> out
-    if (ok && __all_sync(0xffffffffu, mbar_wait(bar_odone, 0, prm.err))) {
+    if (ok && __all_sync(0xffffffffu, mbar_wait(B(B_OD), 0, prm.err))) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       uint4* orow = reinterpret_cast<uint4*>(prm.out + (static_cast<long long>(t0 + qrow) * prm.hq + h) * D);

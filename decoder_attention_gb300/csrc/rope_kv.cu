@@ -96,13 +96,16 @@ struct Vec16<float> {
 // Each head vector (d elements) is handled by d / VEC threads, each owning 16 bytes (VEC consecutive
 // elements). Items are (token, head) for the Hq query heads followed by the Hkv key heads of each token;
 // a key item also copies the token's value vector for that head into the V cache (bit for bit).
-template <typename T, int D>
+// SHFL: r/2 is a multiple of VEC, so a thread's rotation partner (element i +- r/2) is another thread's
+// whole 16-byte piece: it comes by warp shuffle and the thread's cos/sin are VEC consecutive table
+// entries (vector loads). Otherwise the normalised vector is staged in shared memory.
+template <typename T, int D, bool SHFL>
 __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
   using V = Vec16<T>;
   constexpr int VEC = V::N;
   constexpr int TPV = D / VEC;            // threads per vector (8..32)
   constexpr int VPB = 256 / TPV;          // vectors per block
-  __shared__ float stage[VPB][D];
+  __shared__ float stage[SHFL ? 1 : VPB][SHFL ? 1 : D];
 
   const int sub = threadIdx.x % TPV;      // which 16-byte piece of the vector
   const int slot = threadIdx.x / TPV;
@@ -136,28 +139,62 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
     for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
     const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
     const float* w = is_q ? a.q_norm_w : a.k_norm_w;
+    float wv[VEC];
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * w[e0 + j];
+    for (int j = 0; j < VEC; j += 4) {
+      const float4 w4 = *reinterpret_cast<const float4*>(w + e0 + j);
+      wv[j] = w4.x; wv[j + 1] = w4.y; wv[j + 2] = w4.z; wv[j + 3] = w4.w;
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * wv[j];
   }
 
-#pragma unroll
-  for (int j = 0; j < VEC; ++j) stage[slot][e0 + j] = x[j];
-  __syncwarp();
-
-  // split-half rotation of the first `rot` dims
+  // split-half rotation of the first `rot` dims: x'_i = x_i c - x_{i+h} s, x'_{i+h} = x_{i+h} c + x_i s
   const int half = a.rot >> 1;
   float y[VEC];
-  const float* cs = a.cos + static_cast<long long>(t) * half;
-  const float* sn = a.sin + static_cast<long long>(t) * half;
+  if (SHFL) {
+    const int hc = half / VEC;                       // pieces per half
+    const bool lower = sub < hc, upper = sub >= hc && sub < 2 * hc;
+    const int psub = lower ? sub + hc : (upper ? sub - hc : sub);
+    const int src_lane = (threadIdx.x & 31 & ~(TPV - 1)) | psub;
+    float px[VEC];
 #pragma unroll
-  for (int j = 0; j < VEC; ++j) {
-    const int e = e0 + j;
-    if (e < half) {
-      y[j] = live ? x[j] * cs[e] - stage[slot][e + half] * sn[e] : 0.f;
-    } else if (e < a.rot) {
-      y[j] = live ? x[j] * cs[e - half] + stage[slot][e - half] * sn[e - half] : 0.f;
+    for (int j = 0; j < VEC; ++j) px[j] = __shfl_sync(0xffffffffu, x[j], src_lane);
+    if (lower || upper) {
+      const int ci = (lower ? sub : sub - hc) * VEC;
+      const float* cs = a.cos + static_cast<long long>(t) * half + ci;
+      const float* sn = a.sin + static_cast<long long>(t) * half + ci;
+      float c[VEC], sv[VEC];
+#pragma unroll
+      for (int j = 0; j < VEC; j += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(cs + j);
+        const float4 s4 = *reinterpret_cast<const float4*>(sn + j);
+        c[j] = c4.x; c[j + 1] = c4.y; c[j + 2] = c4.z; c[j + 3] = c4.w;
+        sv[j] = s4.x; sv[j + 1] = s4.y; sv[j + 2] = s4.z; sv[j + 3] = s4.w;
+      }
+      const float sgn = lower ? -1.f : 1.f;
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) y[j] = fmaf(sgn * px[j], sv[j], x[j] * c[j]);
     } else {
-      y[j] = x[j];
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) y[j] = x[j];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) stage[slot][e0 + j] = x[j];
+    __syncwarp();
+    const float* cs = a.cos + static_cast<long long>(t) * half;
+    const float* sn = a.sin + static_cast<long long>(t) * half;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const int e = e0 + j;
+      if (e < half) {
+        y[j] = live ? x[j] * cs[e] - stage[slot][e + half] * sn[e] : 0.f;
+      } else if (e < a.rot) {
+        y[j] = live ? x[j] * cs[e - half] + stage[slot][e - half] * sn[e - half] : 0.f;
+      } else {
+        y[j] = x[j];
+      }
     }
   }
   if (!live) return;
@@ -188,7 +225,10 @@ static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
   const long long items = static_cast<long long>(a.n) * (a.hq + a.hkv);
   if (items == 0) return cudaSuccess;
   const long long blocks = (items + VPB - 1) / VPB;
-  kv_update_kernel<T, D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  if ((a.rot / 2) % Vec16<T>::N == 0)
+    kv_update_kernel<T, D, true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  else
+    kv_update_kernel<T, D, false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -336,3 +336,48 @@ def make(workload, scale="full", device="cpu", **kw):
     """Build workload `workload` (number or name)."""
     num = workload if isinstance(workload, int) else NUMBERS[workload]
     return BUILDERS[num](scale=scale, device=device, **kw)
+
+
+def subset(call: LayerCall, chunks, decode_idx, device="cpu", kv_heads=None) -> LayerCall:
+    """A LayerCall holding only prefill chunks `chunks` and decode tokens `decode_idx` of `call`, with the
+    cache rows they use (renumbered 0..k-1) copied to `device`; with `kv_heads`, only the first kv_heads
+    KV heads and their query-head groups. Bookkeeping only: used to size bounded samples of a full
+    workload for the CPU oracle."""
+    chunks = list(chunks)
+    hkv = call.num_key_value_heads if kv_heads is None else int(kv_heads)
+    hq = hkv * (call.num_attention_heads // call.num_key_value_heads)
+    decode_idx = list(decode_idx)
+    qs = call.q_start.cpu().tolist()
+    pf_rows = call.pf_rows.cpu().tolist()
+    pf_fp = call.pf_first_pos.cpu().tolist()
+    dec_rows = call.dec_rows.cpu().tolist()
+    dec_pos = call.dec_pos.cpu().tolist()
+    rows_used = [pf_rows[b] for b in chunks] + [dec_rows[i] for i in decode_idx]
+    remap = {r: j for j, r in enumerate(dict.fromkeys(rows_used))}
+    tok = []
+    lens = []
+    for b in chunks:
+        tok += list(range(qs[b], qs[b + 1]))
+        lens.append(qs[b + 1] - qs[b])
+    n_pf = len(tok)
+    tok += [call.n_prefill + i for i in decode_idx]
+    idx = torch.as_tensor(tok, dtype=torch.long)
+    q_start, tr, tp, tl = _prefill_meta(lens, [pf_fp[b] for b in chunks], [remap[pf_rows[b]] for b in chunks])
+    d_rows = [remap[dec_rows[i]] for i in decode_idx]
+    d_pos = [dec_pos[i] for i in decode_idx]
+    d_len = [p + 1 for p in d_pos]
+    ridx = torch.as_tensor(list(remap.keys()), dtype=torch.long, device=call.k_cache.device)
+    fields = {k: getattr(call, k) for k in call.__dataclass_fields__}
+    fields.update(
+        num_attention_heads=hq, num_key_value_heads=hkv,
+        q=call.q[idx.to(call.q.device), :hq].to(device), k=call.k[idx.to(call.k.device), :hkv].to(device),
+        v=call.v[idx.to(call.v.device), :hkv].to(device),
+        tok_rows=_i32(tr + d_rows, device), tok_pos=_i32(tp + d_pos, device), tok_seq_len=_i32(tl + d_len, device),
+        n_prefill=n_pf, q_start=_i32(q_start, device), pf_rows=_i32([remap[pf_rows[b]] for b in chunks], device),
+        pf_first_pos=_i32([pf_fp[b] for b in chunks], device), max_q_len=max(lens) if lens else 0,
+        dec_rows=_i32(d_rows, device), dec_pos=_i32(d_pos, device),
+        k_cache=call.k_cache[ridx, :hkv].to(device), v_cache=call.v_cache[ridx, :hkv].to(device),
+        q_norm_w=call.q_norm_w.to(device) if call.q_norm_w is not None else None,
+        k_norm_w=call.k_norm_w.to(device) if call.k_norm_w is not None else None,
+        meta=dict(call.meta))
+    return LayerCall(**fields)

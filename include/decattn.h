@@ -136,6 +136,7 @@ int da_rope_tables_build(const da_rope_scaling* rs, const int32_t* positions, co
  *   cos, sin      device fp32 [n, r/2] from da_rope_tables_build
  *   q_rot         device [N, Hq, d], written; may be the same buffer as q
  *   k_cache, v_cache  device [num_rows, Hkv, max_len, d], written at the (row, position) slots only
+ * Every pointer, cos/sin and the norm weights included, must be 16-byte aligned (16-byte vector accesses).
  * Two tokens of one call must not name the same (row, position). A token whose row or position is out of
  * range is skipped and sets DA_ERR_DEVICE_INDEX on the device.
  */

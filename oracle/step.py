@@ -39,15 +39,30 @@ def rope_tables(call, positions=None, seq_len=None):
     return A.rope_tables_for_tokens(spec_of(call), layer.rotary_dim, pos, lens)
 
 
-def run_layer_call(call, key_positions=None):
+def round_to_storage(x, dtype):
+    """x rounded once to the storage type `dtype` (torch dtype; round to nearest even), back in float64.
+
+    The pages' engine keeps rotated queries and cached keys in the activation dtype (page "42. More models",
+    section "Scaled RoPE": rope_tables casts cos/sin to that dtype, and the cache holds that dtype); a bf16
+    cache therefore carries each rotated key rounded to bf16. Oracle values only pass through here."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).to(dtype).double().numpy()
+
+
+def run_layer_call(call, key_positions=None, storage_rounding=False):
     """All results of one call at a size the oracle handles whole: cos, sin, q_rot, caches after the
-    update, and the attention output of every token (float64)."""
+    update, and the attention output of every token (float64). With storage_rounding, the oracle's own
+    rotated q and k are rounded to the call's dtype before attention, as a cache of that dtype stores them."""
     layer = layer_of(call)
     cos, sin = rope_tables(call)
     kc = _np64(call.k_cache).copy()
     vc = _np64(call.v_cache).copy()
     rows, pos = _np_int(call.tok_rows), _np_int(call.tok_pos)
     q_rot = A.kv_cache_update(layer, _np64(call.q), _np64(call.k), _np64(call.v), rows, pos, cos, sin, kc, vc)
+    if storage_rounding:
+        q_rot = round_to_storage(q_rot, call.dtype)
+        for t in range(len(rows)):
+            kc[rows[t], :, pos[t]] = round_to_storage(kc[rows[t], :, pos[t]], call.dtype)
     out = np.zeros_like(q_rot)
     npf = call.n_prefill
     kp = None if key_positions is None else _np_int(key_positions)

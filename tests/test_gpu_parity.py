@@ -80,13 +80,23 @@ def test_small_workload_parity(cuda, number):
 
 
 def test_softcap_binds(cuda):
-    """Workload 5 with q x 16: logits reach the cap of 50, so the soft-cap shapes the result."""
+    """Workload 5 with q x 8: logits reach ~30 against the cap of 50, so the soft-cap shapes the result. At
+    such logits the bf16 rounding of the stored rotated q and k alone moves a logit by ~0.1, which a peaked
+    softmax turns into output changes above 2e-2; the attention kernels are therefore checked against the
+    oracle with its rotated q/k rounded to bf16 as the cache stores them (the rotation itself is checked
+    against the unrounded oracle in the other tests)."""
     from decoder_attention_gb300 import inputs
-    wl = inputs.make(5, scale="small", q_mult=16.0)
+    wl = inputs.make(5, scale="small", q_mult=8.0)
     for call in wl.layers:
         st, _ = _run(call, cuda)
-        ref = ostep.run_layer_call(call)
+        ref = ostep.run_layer_call(call, storage_rounding=True)
         _check_out(st.out, ref["out"], False)
+        # the cap binds: the uncapped result differs grossly
+        import copy
+        nocap = copy.copy(call)
+        nocap.softcap = 0.0
+        ref_nocap = ostep.run_layer_call(nocap, storage_rounding=True)
+        assert np.abs(ref_nocap["out"] - ref["out"]).max() > 0.1
 
 
 def test_repeat_is_deterministic(cuda):
