@@ -63,6 +63,8 @@ def _load():
         "da_attn_prefill": (I, [ctypes.POINTER(DaLayer), P, I, P, P, I, I, I, P, P, P, I, P, P, P, Z, P]),
         "da_attn_decode": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, I, P, P, P, P, P, Z, P]),
         "da_decode_workspace_bytes": (Z, [ctypes.POINTER(DaLayer), I, I]),
+        "da_attn_decode_noalloc": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, I, P, P, P, P, P]),
+        "da_decode_noalloc_max_scratch_bytes": (Z, []),
         "da_check_device_error": (I, [P]),
         "da_last_error": (ctypes.c_char_p, []),
         "da_version": (I, []),
@@ -203,6 +205,18 @@ def attn_decode(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, pos
     _check(LIB.da_attn_decode(ctypes.byref(L), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), int(num_rows),
                               int(max_len), int(n_seqs), _ptr(rows), _ptr(positions), _ptr(key_positions), _ptr(out),
                               _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def attn_decode_noalloc(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, positions, key_positions, out,
+                        stream=None):
+    """da_attn_decode without a workspace argument: the library's fixed scratch is used (see decattn.h)."""
+    _check(LIB.da_attn_decode_noalloc(ctypes.byref(L), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), int(num_rows),
+                                      int(max_len), int(n_seqs), _ptr(rows), _ptr(positions), _ptr(key_positions),
+                                      _ptr(out), _stream(stream)))
+
+
+def decode_noalloc_max_scratch_bytes() -> int:
+    return int(LIB.da_decode_noalloc_max_scratch_bytes())
 
 
 def decode_workspace_bytes(L, n_seqs, max_len) -> int:

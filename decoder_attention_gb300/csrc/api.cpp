@@ -389,6 +389,40 @@ int da_attn_decode(const da_layer* L, const void* q_rot, const void* k_cache, co
   return ok();
 }
 
+int da_attn_decode_noalloc(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache,
+                           int num_rows, int max_len, int n_seqs, const int32_t* rows, const int32_t* positions,
+                           const int32_t* key_positions, void* out, cudaStream_t stream) {
+  int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out);
+  if (rc) return rc;
+  if (n_seqs == 0) return ok();
+  if (!positions) return fail(DA_ERR_INVALID_ARG, "positions must be non-NULL");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  da::AttnArgs a = make_args(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, key_positions, out, err);
+  a.positions = positions;
+  a.max_q_len = 1;
+  a.n_tokens = n_seqs;
+  if (!decode_fast(L, key_positions)) {   // the CUDA-core kernel needs no scratch
+    cudaError_t e = da::launch_attn_generic(a, L->dtype == DA_BF16, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode (generic) launch");
+    return ok();
+  }
+  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window);
+  const size_t need = da::decode_workspace_bytes(L->num_attention_heads, n_seqs, p);
+  if (need > da::kDecodeStaticScratchBytes)
+    return fail(DA_ERR_INVALID_ARG,
+                "decode needs %zu bytes of scratch, more than the %zu bytes of the library's fixed scratch; "
+                "use da_attn_decode with a caller-provided workspace or split the batch",
+                need, da::kDecodeStaticScratchBytes);
+  void* scratch = da::static_scratch();
+  if (!scratch) return fail(DA_ERR_CUDA, "cannot locate the fixed decode scratch on this device");
+  cudaError_t e = da::launch_decode_bf16(a, p, scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode (split-K, fixed scratch) launch");
+  return ok();
+}
+
+size_t da_decode_noalloc_max_scratch_bytes(void) { return da::kDecodeStaticScratchBytes; }
+
 int da_check_device_error(cudaStream_t stream) {
   int flags = 0;
   if (da::read_and_clear_error_word(stream, &flags) != DA_OK)

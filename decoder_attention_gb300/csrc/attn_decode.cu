@@ -18,6 +18,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -331,6 +332,26 @@ __global__ void __launch_bounds__(D) merge_kernel(const Params prm) {
 }
 
 }  // namespace dec
+
+// Scratch of da_attn_decode_noalloc: a fixed array in the module's global memory, so that callers who
+// may not allocate device memory can still run the split-K decode. Every GPU that loads the library holds
+// these bytes until the process exits. Host code must not pass the symbol itself to a kernel (on the host
+// it names a stand-in, not device memory): static_scratch() looks up its device address once per device.
+static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeStaticScratchBytes];
+
+void* static_scratch() {
+  static std::mutex mu;
+  static void* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
 
 DecodePlan decode_plan(int hkv, int n_seqs, int max_len, int window) {
   DecodePlan p;

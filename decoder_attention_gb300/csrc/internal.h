@@ -85,6 +85,10 @@ DecodePlan decode_plan(int hkv, int n_seqs, int max_len, int window);
 size_t decode_workspace_bytes(int hq, int n_seqs, const DecodePlan& p);
 cudaError_t launch_decode_bf16(const AttnArgs& a, const DecodePlan& p, void* workspace, cudaStream_t stream);
 
+// Fixed scratch for da_attn_decode_noalloc (file-scope device array in attn_decode.cu).
+constexpr size_t kDecodeStaticScratchBytes = size_t(32) << 20;
+void* static_scratch();   // its device address on the current device; NULL if the lookup fails
+
 // tcgen05 prefill (bf16, d = 128, no key_positions).
 cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream);
 

@@ -200,6 +200,33 @@ int da_attn_decode(const da_layer* layer, const void* q_rot, const void* k_cache
  * (0 when the layer is invalid or decode needs none). Pure host arithmetic. */
 size_t da_decode_workspace_bytes(const da_layer* layer, int n_seqs, int max_len);
 
+/*
+ * da_attn_decode_noalloc -- da_attn_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers of this library that may not call
+ * cudaMalloc or any allocating routine -- for example a host process whose device memory is owned by
+ * another component's pool, or a path where an allocation's implicit synchronisation is not acceptable.
+ * It computes exactly what da_attn_decode computes (same arguments, minus the workspace) and allocates
+ * nothing: the split-K partials go to a fixed scratch array of da_decode_noalloc_max_scratch_bytes()
+ * bytes (32 MiB) in the library's own device memory, which every GPU that loads the library holds until
+ * the process exits.
+ *  - A call whose split plan needs more scratch than that (da_decode_workspace_bytes(layer, n_seqs,
+ *    max_len) > 32 MiB) returns DA_ERR_INVALID_ARG and enqueues nothing; split the batch or use
+ *    da_attn_decode.
+ *  - Every call shares the one array: calls whose kernels overlap on the GPU (different streams, or
+ *    different threads without ordering) race on it and may return wrong results. Calls on one stream are
+ *    ordered and safe. The scratch needs no clearing between calls: each call writes every partial before
+ *    reading it.
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress) with that
+ *    device current; make that first call before any stream capture.
+ */
+int da_attn_decode_noalloc(const da_layer* layer, const void* q_rot, const void* k_cache, const void* v_cache,
+                           int num_rows, int max_len, int n_seqs, const int32_t* rows, const int32_t* positions,
+                           const int32_t* key_positions, void* out, cudaStream_t stream);
+
+/* Size in bytes of the fixed scratch behind da_attn_decode_noalloc. */
+size_t da_decode_noalloc_max_scratch_bytes(void);
+
 /* Waits for `stream`, then reads and clears the device error word that kernels set on an out-of-range
  * index (DA_ERR_DEVICE_INDEX) or a bounded wait that gave up (DA_ERR_TIMEOUT). Returns DA_OK when clear,
  * DA_ERR_CUDA if the wait itself failed. */
