@@ -90,16 +90,23 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 // and the row max with 8 independent partial maxima (one running max would be a 128-long dependency chain).
 template <bool CAP, bool MASK>
 __device__ __forceinline__ float row_pass(uint32_t (&zr)[BN], float cap_in, float cap_l2, int lo_c, int hi_c) {
+  if (CAP || MASK) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c) {
+      float v = __uint_as_float(zr[c]);
+      if (CAP) v = cap_l2 * tanh_fast(v * cap_in);
+      if (MASK) v = (c >= lo_c && c <= hi_c) ? v : -CUDART_INF_F;
+      zr[c] = __float_as_uint(v);
+    }
+  }
+  // 8 independent partial maxima, two new scores per 3-input max
   float mx[8];
 #pragma unroll
-  for (int c = 0; c < BN; ++c) {
-    float v = __uint_as_float(zr[c]);
-    if (CAP) v = cap_l2 * tanh_fast(v * cap_in);
-    if (MASK) v = (c >= lo_c && c <= hi_c) ? v : -CUDART_INF_F;
-    zr[c] = __float_as_uint(v);
-    mx[c & 7] = c < 8 ? v : fmaxf(mx[c & 7], v);
-  }
-  return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(zr[2 * e]), __uint_as_float(zr[2 * e + 1]));
+#pragma unroll
+  for (int c = 16; c < BN; c += 2)
+    mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], __uint_as_float(zr[c]), __uint_as_float(zr[c + 1]));
+  return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
 }
 
 // The 8 MMAs (K = 16 each) of S = Q K^T for one 128 x 128 tile; both operands K-major, 128-byte swizzled
@@ -273,17 +280,18 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           tc_commit(B(B_SF + 1));
         }
         tc_commit(B(B_KE + 0));
+        ok = mbar_wait(B(B_VF + 0), 0, prm.err);
       }
+      // The waits that are normally already satisfied (K and V copies) sit where the tensor core still has
+      // queued work; the gap between issuing S1(t+1) and PV0(t+1) -- the tensor core's idle window when
+      // P0(t+1) is late -- holds only the P0 wait.
       for (int i = 0; ok && i < n_tiles; ++i) {
-        if (*vabort) break;
         const int t = tbeg + i;
         const bool nxt = i + 1 < n_tiles;
         const int kst1 = (i + 1) % NK;
         const uint32_t k1s = sbase + OFF_K + kst1 * TILE;
         const int vst = i % NV;
         const uint32_t vs = sbase + OFF_V + vst * TILE;
-        if (!mbar_wait(B(B_VF + vst), (i / NV) & 1, prm.err)) { ok = false; break; }
-        tc_fence_after();
         if (act0(t)) {
           if (!mbar_wait(B(B_PF + 0), npv0 & 1, prm.err)) { ok = false; break; }
           tc_fence_after();
@@ -297,6 +305,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             issue_s(s0t, q0s, k1s);
             tc_commit(B(B_SF + 0));
           }
+          // V of the next tile, for the next iteration's PVs
+          if (!mbar_wait(B(B_VF + (i + 1) % NV), ((i + 1) / NV) & 1, prm.err)) { ok = false; break; }
         }
         if (act1(t)) {
           if (!mbar_wait(B(B_PF + 1), npv1 & 1, prm.err)) { ok = false; break; }
@@ -394,21 +404,30 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         }
       }
       const float nmu = (m == -CUDART_INF_F) ? 0.f : -m;
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // p = 2^(z * zmul - m) two scores at a time (packed fp32 pairs), row sum in 4 packed accumulators
+      const uint64_t zmul2 = f2_pack(zmul, zmul), nmu2 = f2_pack(nmu, nmu);
+      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int j = 0; j < BN / 32; ++j) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float pa = ex2(fmaf(__uint_as_float(zr[j * 32 + 2 * e]), zmul, nmu));
-          const float pb = ex2(fmaf(__uint_as_float(zr[j * 32 + 2 * e + 1]), zmul, nmu));
-          ls[(2 * e) & 7] += pa;
-          ls[(2 * e + 1) & 7] += pb;
+          float xa, xb;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(zr[j * 32 + 2 * e]), __uint_as_float(zr[j * 32 + 2 * e + 1])),
+                           zmul2, nmu2), xa, xb);
+          const float pa = ex2(xa), pb = ex2(xb);
+          ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(pa, pb));
           pk[e] = pack_bf16(pa, pb);
         }
         tmem_st16(t_s + j * 16, pk);     // P (bf16, 2 per column) over the first half of the S columns
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      {
+        float a0, a1, b0, b1, c0, c1, d0, d1;
+        f2_unpack(f2_add(ls2[0], ls2[1]), a0, a1);
+        f2_unpack(f2_add(ls2[2], ls2[3]), b0, b1);
+        (void)c0; (void)c1; (void)d0; (void)d1;
+        l += (a0 + a1) + (b0 + b1);
+      }
       tmem_wait_st();
       if (kstart + BN > kv_len) {
         // V rows past the row's last key hold whatever the cache holds there (maybe NaN); P is 0 there,
