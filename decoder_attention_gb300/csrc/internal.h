@@ -20,7 +20,10 @@ int* error_word_ptr();
 int read_and_clear_error_word(cudaStream_t stream, int* flags);
 
 // Frequencies of one rope configuration, computed on the host in fp64. Tokens whose sequence length
-// exceeds `switch_len` use the `inv_long` table (LongRoPE); otherwise `inv_short`.
+// exceeds `switch_len` use the long table (LongRoPE); otherwise the short one. inv_* are the angular
+// frequencies (radians per position); turn_* are the same frequencies in turns per position as 64-bit
+// fixed-point fractions (value * 2^64), which the device multiplies by the integer position modulo 2^64:
+// the wrap-around is the exact reduction of the angle modulo 2 pi.
 struct RopeFreqs {
   int half;                      // r / 2
   int switch_len;                // long table when seq_len > switch_len; INT32_MAX when unused
@@ -29,6 +32,13 @@ struct RopeFreqs {
   double inv_short[kMaxRotHalf];
   double inv_long[kMaxRotHalf];
 };
+struct RopeTurns {
+  int half, switch_len, use_seq_len;
+  float af;
+  unsigned long long turn_short[kMaxRotHalf];
+  unsigned long long turn_long[kMaxRotHalf];
+};
+RopeTurns rope_turns(const RopeFreqs& f);
 
 cudaError_t launch_rope_tables(const RopeFreqs& f, const int32_t* positions, const int32_t* seq_len, int n,
                                float* cos, float* sin, int* err, cudaStream_t stream);

@@ -6,6 +6,8 @@
 // and §4 Rotary for the norm, the cache write and the split-half rotation.
 #include <cuda_bf16.h>
 
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -13,10 +15,33 @@ namespace da {
 
 // ---------------------------------------------------------------------------------------------- tables
 
-// One thread per (token, pair). The angle p * inv_i is formed in fp64 and reduced into [-pi, pi] by
-// Cody-Waite reduction with 2 pi split into a head and a tail (both fp64), then cos/sin are taken in
-// fp32: at p ~ 131071 the fp32 product alone would be off by up to 4e-3 rad.
-__global__ void rope_tables_kernel(const __grid_constant__ RopeFreqs f, const int32_t* __restrict__ positions,
+// inv / (2 pi) as a fixed-point fraction of 2^64 (inv < 2 pi for every RoPE pair, so the value is < 1).
+// fp64 carries 53 bits of it, the same precision an fp64 angle product would have.
+static unsigned long long turn_fixed(double inv) {
+  const double f = inv / 6.283185307179586476925286766559;   // turns per position
+  const double hi = std::floor(std::ldexp(f, 32));
+  const double lo = std::floor(std::ldexp(std::ldexp(f, 32) - hi, 32));
+  return (static_cast<unsigned long long>(hi) << 32) | static_cast<unsigned long long>(lo);
+}
+
+RopeTurns rope_turns(const RopeFreqs& f) {
+  RopeTurns t;
+  t.half = f.half;
+  t.switch_len = f.switch_len;
+  t.use_seq_len = f.use_seq_len;
+  t.af = static_cast<float>(f.af);
+  for (int i = 0; i < kMaxRotHalf; ++i) {
+    t.turn_short[i] = i < f.half ? turn_fixed(f.inv_short[i]) : 0ull;
+    t.turn_long[i] = i < f.half ? turn_fixed(f.inv_long[i]) : 0ull;
+  }
+  return t;
+}
+
+// One thread per (token, pair). p * turns (mod 2^64) is the angle's fraction of a full turn, exactly up to
+// the table's 53 significant bits; its top 32 bits, read as a signed fraction x in [-1, 1), give the angle
+// pi * x in [-pi, pi), whose sine and cosine sincospif takes in fp32. At p ~ 131071 an fp32 product
+// p * inv would be off by up to 4e-3 rad; this stays within ~2e-7.
+__global__ void rope_tables_kernel(const __grid_constant__ RopeTurns f, const int32_t* __restrict__ positions,
                                    const int32_t* __restrict__ seq_len, int n, float* __restrict__ cos_out,
                                    float* __restrict__ sin_out, int* err) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -32,27 +57,24 @@ __global__ void rope_tables_kernel(const __grid_constant__ RopeFreqs f, const in
     return;
   }
   const bool use_long = f.use_seq_len && seq_len[t] > f.switch_len;
-  const double inv = use_long ? f.inv_long[i] : f.inv_short[i];
-  const double ang = static_cast<double>(p) * inv;
-  const double kTwoPiHi = 6.283185307179586;        // 2 pi rounded to fp64
-  const double kTwoPiLo = 2.4492935982947064e-16;   // 2 pi - kTwoPiHi
-  const double k = rint(ang * (1.0 / 6.283185307179586));
-  double r = fma(-k, kTwoPiHi, ang);
-  r = fma(-k, kTwoPiLo, r);
+  const unsigned long long turn = use_long ? f.turn_long[i] : f.turn_short[i];
+  const unsigned long long frac = static_cast<unsigned long long>(p) * turn;     // mod 2^64
+  const int top = static_cast<int>(static_cast<unsigned int>(frac >> 32));      // signed fraction of 2^31
+  const float x = static_cast<float>(top) * 4.656612873077393e-10f;             // top / 2^31
   float s, c;
-  sincosf(static_cast<float>(r), &s, &c);
-  const float af = static_cast<float>(f.af);
-  cos_out[idx] = c * af;
-  sin_out[idx] = s * af;
+  sincospif(x, &s, &c);
+  cos_out[idx] = c * f.af;
+  sin_out[idx] = s * f.af;
 }
 
 cudaError_t launch_rope_tables(const RopeFreqs& f, const int32_t* positions, const int32_t* seq_len, int n,
                                float* cos, float* sin, int* err, cudaStream_t stream) {
   const long long total = static_cast<long long>(n) * f.half;
   if (total == 0) return cudaSuccess;
+  const RopeTurns turns = rope_turns(f);
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
-  rope_tables_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(f, positions, seq_len, n, cos, sin, err);
+  rope_tables_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(turns, positions, seq_len, n, cos, sin, err);
   return cudaGetLastError();
 }
 
@@ -120,51 +142,36 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
   const bool is_q = hh < a.hq;
   const int e0 = sub * VEC;
 
+  // every global load of the item is issued here, before any of them is used, so that one memory
+  // round trip covers the vector, the value, the slot and the table/weight reads
   float x[VEC];
+  uint4 vv = make_uint4(0, 0, 0, 0);
+  int row = 0, pos = 0;
   if (live) {
     const T* src = is_q ? static_cast<const T*>(a.q) + (static_cast<long long>(t) * a.hq + hh) * D
                         : static_cast<const T*>(a.k) + (static_cast<long long>(t) * a.hkv + (hh - a.hq)) * D;
     V::load(src + e0, x);
+    if (!is_q) {
+      vv = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.v) +
+                                           (static_cast<long long>(t) * a.hkv + (hh - a.hq)) * D + e0);
+      row = a.rows[t];
+      pos = a.positions[t];
+    }
   } else {
 #pragma unroll
     for (int j = 0; j < VEC; ++j) x[j] = 0.f;
   }
-
-  // RMSNorm over the head: x / sqrt(mean(x^2) + eps) * w
-  if (a.q_norm_w != nullptr) {
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) ss = fmaf(x[j], x[j], ss);
-#pragma unroll
-    for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
-    const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
-    const float* w = is_q ? a.q_norm_w : a.k_norm_w;
-    float wv[VEC];
-#pragma unroll
-    for (int j = 0; j < VEC; j += 4) {
-      const float4 w4 = *reinterpret_cast<const float4*>(w + e0 + j);
-      wv[j] = w4.x; wv[j + 1] = w4.y; wv[j + 2] = w4.z; wv[j + 3] = w4.w;
-    }
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * wv[j];
-  }
-
-  // split-half rotation of the first `rot` dims: x'_i = x_i c - x_{i+h} s, x'_{i+h} = x_{i+h} c + x_i s
   const int half = a.rot >> 1;
-  float y[VEC];
+  float c[VEC], sv[VEC];
+  bool lower = false, upper = false;
   if (SHFL) {
     const int hc = half / VEC;                       // pieces per half
-    const bool lower = sub < hc, upper = sub >= hc && sub < 2 * hc;
-    const int psub = lower ? sub + hc : (upper ? sub - hc : sub);
-    const int src_lane = (threadIdx.x & 31 & ~(TPV - 1)) | psub;
-    float px[VEC];
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) px[j] = __shfl_sync(0xffffffffu, x[j], src_lane);
-    if (lower || upper) {
+    lower = sub < hc;
+    upper = sub >= hc && sub < 2 * hc;
+    if (live && (lower || upper)) {
       const int ci = (lower ? sub : sub - hc) * VEC;
       const float* cs = a.cos + static_cast<long long>(t) * half + ci;
       const float* sn = a.sin + static_cast<long long>(t) * half + ci;
-      float c[VEC], sv[VEC];
 #pragma unroll
       for (int j = 0; j < VEC; j += 4) {
         const float4 c4 = *reinterpret_cast<const float4*>(cs + j);
@@ -172,6 +179,38 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
         c[j] = c4.x; c[j + 1] = c4.y; c[j + 2] = c4.z; c[j + 3] = c4.w;
         sv[j] = s4.x; sv[j + 1] = s4.y; sv[j + 2] = s4.z; sv[j + 3] = s4.w;
       }
+    }
+  }
+
+  // RMSNorm over the head: x / sqrt(mean(x^2) + eps) * w
+  if (a.q_norm_w != nullptr) {
+    const float* w = is_q ? a.q_norm_w : a.k_norm_w;
+    float wv[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; j += 4) {
+      const float4 w4 = *reinterpret_cast<const float4*>(w + e0 + j);
+      wv[j] = w4.x; wv[j + 1] = w4.y; wv[j + 2] = w4.z; wv[j + 3] = w4.w;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) ss = fmaf(x[j], x[j], ss);
+#pragma unroll
+    for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
+    const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * wv[j];
+  }
+
+  // split-half rotation of the first `rot` dims: x'_i = x_i c - x_{i+h} s, x'_{i+h} = x_{i+h} c + x_i s
+  float y[VEC];
+  if (SHFL) {
+    const int hc = half / VEC;
+    const int psub = lower ? sub + hc : (upper ? sub - hc : sub);
+    const int src_lane = (threadIdx.x & 31 & ~(TPV - 1)) | psub;
+    float px[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) px[j] = __shfl_sync(0xffffffffu, x[j], src_lane);
+    if (lower || upper) {
       const float sgn = lower ? -1.f : 1.f;
 #pragma unroll
       for (int j = 0; j < VEC; ++j) y[j] = fmaf(sgn * px[j], sv[j], x[j] * c[j]);
@@ -205,16 +244,12 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
     return;
   }
   const int g = hh - a.hq;
-  const int row = a.rows[t];
-  const int pos = a.positions[t];
   if (row < 0 || row >= a.num_rows || pos < 0 || pos >= a.max_len) {
     if (sub == 0) set_error(a.err, kErrIndex);
     return;
   }
   const long long slot_off = ((static_cast<long long>(row) * a.hkv + g) * a.max_len + pos) * D;
   V::store(static_cast<T*>(a.k_cache) + slot_off + e0, y);
-  const uint4 vv = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.v) +
-                                                   (static_cast<long long>(t) * a.hkv + g) * D + e0);
   *reinterpret_cast<uint4*>(static_cast<T*>(a.v_cache) + slot_off + e0) = vv;
 }
 

@@ -1,0 +1,232 @@
+"""Edge cases of the CUDA path against the fp64 oracle (through the C ABI).
+
+Covers: calls with nothing to do; a window of one key; a window at least as long as the context, which must
+reproduce full attention bit for bit; cache slots past a row's length filled with NaN (they must never
+reach a result); explicit key positions (slots permuted); fp32 decode; layers the fast kernels leave to the
+CUDA-core kernel (d = 64 in bf16, a GQA group of 16); and out-of-range rows, which the kernels skip and
+report through the device error word instead of faulting.
+"""
+import copy
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from oracle import step as ostep
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN, FP32_MAX = 2e-2, 2e-3, 1e-4
+
+
+def _abi():
+    from decoder_attention_gb300 import _abi
+    return _abi
+
+
+def _run(call, dev):
+    from decoder_attention_gb300 import step
+    g = call.to(dev)
+    st = step.AttentionStep(g)
+    st.run()
+    torch.cuda.synchronize()
+    _abi().check_device_error()
+    return st, g
+
+
+def _close(got, ref, fp32=False):
+    d = np.abs(got.double().cpu().numpy() - ref)
+    assert np.isfinite(d).all()
+    if fp32:
+        assert d.max() <= FP32_MAX, d.max()
+    else:
+        assert d.max() <= BF16_MAX and d.mean() <= BF16_MEAN, (d.max(), d.mean())
+
+
+def _prefill_call(lens, first_pos, hq=8, hkv=2, d=128, window=0, softcap=0.0, dtype=torch.bfloat16, seed=5,
+                  M=None, rot=None):
+    """A prefill-only call with random caches for the positions before each chunk."""
+    from decoder_attention_gb300 import inputs
+    g = torch.Generator().manual_seed(seed)
+    n = sum(lens)
+    q = (torch.randn((n, hq, d), generator=g) / math.sqrt(d) * 4).to(dtype)
+    k = torch.randn((n, hkv, d), generator=g).to(dtype)
+    v = torch.randn((n, hkv, d), generator=g).to(dtype)
+    R = len(lens)
+    M = M or max(p + L for p, L in zip(first_pos, lens))
+    kc = torch.randn((R, hkv, M, d), generator=g).to(dtype)
+    vc = torch.randn((R, hkv, M, d), generator=g).to(dtype)
+    qs, tr, tp, tl = inputs._prefill_meta(lens, first_pos, list(range(R)))
+    return inputs.LayerCall(head_dim=d, num_attention_heads=hq, num_key_value_heads=hkv,
+                            partial_rotary_factor=(rot or d) / d, rope_theta=1e4, rope_scaling=None,
+                            max_position_embeddings=M, dtype=dtype, window=window, softcap=softcap,
+                            q=q, k=k, v=v, tok_rows=inputs._i32(tr), tok_pos=inputs._i32(tp),
+                            tok_seq_len=inputs._i32(tl), n_prefill=n, q_start=inputs._i32(qs),
+                            pf_rows=inputs._i32(list(range(R))), pf_first_pos=inputs._i32(first_pos),
+                            max_q_len=max(lens), dec_rows=inputs._i32([]), dec_pos=inputs._i32([]),
+                            k_cache=kc, v_cache=vc)
+
+
+def _decode_call(lens, hq=8, hkv=2, d=128, window=0, dtype=torch.bfloat16, seed=6):
+    from decoder_attention_gb300 import inputs
+    g = torch.Generator().manual_seed(seed)
+    S = len(lens)
+    M = max(lens)
+    q = (torch.randn((S, hq, d), generator=g) / math.sqrt(d) * 4).to(dtype)
+    k = torch.randn((S, hkv, d), generator=g).to(dtype)
+    v = torch.randn((S, hkv, d), generator=g).to(dtype)
+    kc = torch.randn((S, hkv, M, d), generator=g).to(dtype)
+    vc = torch.randn((S, hkv, M, d), generator=g).to(dtype)
+    pos = [L - 1 for L in lens]
+    rows = list(range(S))
+    return inputs.LayerCall(head_dim=d, num_attention_heads=hq, num_key_value_heads=hkv, partial_rotary_factor=1.0,
+                            rope_theta=1e4, rope_scaling=None, max_position_embeddings=M, dtype=dtype,
+                            window=window, q=q, k=k, v=v, tok_rows=inputs._i32(rows), tok_pos=inputs._i32(pos),
+                            tok_seq_len=inputs._i32(lens), n_prefill=0, q_start=inputs._i32([0]),
+                            pf_rows=inputs._i32([]), pf_first_pos=inputs._i32([]), max_q_len=0,
+                            dec_rows=inputs._i32(rows), dec_pos=inputs._i32(pos), k_cache=kc, v_cache=vc)
+
+
+def test_empty_calls_do_nothing(cuda):
+    ab = _abi()
+    L = ab.layer(torch.bfloat16, 128, 8, 2, 128)
+    x = torch.zeros(16, dtype=torch.bfloat16, device=cuda)
+    i = torch.zeros(4, dtype=torch.int32, device=cuda)
+    f = torch.zeros(16, dtype=torch.float32, device=cuda)
+    rs, keep = ab.rope_scaling(1e4, 128)
+    ab.rope_tables_build(rs, i, None, 0, f, f)
+    ab.kv_cache_update(L, x, x, x, 0, i, i, f, f, x, x, x, 1, 1)
+    ab.attn_prefill(L, x, 0, x, x, 1, 1, 0, i, i, i, 0, None, x)
+    ab.attn_decode(L, x, x, x, 1, 1, 0, i, i, None, x, None, 0)
+    torch.cuda.synchronize()
+    ab.check_device_error()
+    assert torch.count_nonzero(x) == 0
+
+
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_window_one_and_window_covering_context(cuda, kind):
+    base = (_prefill_call([300, 129], [0, 170]) if kind == "prefill" else _decode_call([700, 1, 129, 4096]))
+    one = copy.copy(base)
+    one.window = 1
+    st, _ = _run(one, cuda)
+    _close(st.out, ostep.run_layer_call(one)["out"])
+    full, _ = _run(base, cuda)
+    wide = copy.copy(base)
+    wide.window = 1 << 20
+    st_w, _ = _run(wide, cuda)
+    assert torch.equal(st_w.out, full.out)
+
+
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_nan_in_unwritten_slots_never_reaches_the_result(cuda, kind):
+    call = _prefill_call([77, 200], [0, 333]) if kind == "prefill" else _decode_call([65, 1000, 3, 130])
+    ref = ostep.run_layer_call(call)["out"]
+    poisoned = copy.copy(call)
+    kc, vc = call.k_cache.clone(), call.v_cache.clone()
+    if kind == "prefill":
+        ends = [p + L for p, L in zip(call.pf_first_pos.tolist(), np.diff(call.q_start.numpy()).tolist())]
+        rows = call.pf_rows.tolist()
+    else:
+        ends = [p + 1 for p in call.dec_pos.tolist()]
+        rows = call.dec_rows.tolist()
+    for r, e in zip(rows, ends):
+        kc[r, :, e:] = float("nan")
+        vc[r, :, e:] = float("nan")
+    poisoned.k_cache, poisoned.v_cache = kc, vc
+    st, _ = _run(poisoned, cuda)
+    _close(st.out, ref)
+
+
+def test_explicit_key_positions(cuda):
+    """With key_positions the mask compares positions: a row whose slots are permuted (positions alike)
+    gives the oracle's result; -1 marks empty slots (filled with NaN here)."""
+    ab = _abi()
+    from decoder_attention_gb300 import step
+    call = _prefill_call([150], [90], window=64)
+    ref = ostep.run_layer_call(call)["out"]
+    st = step.AttentionStep(call.to(cuda))
+    st.rope()
+    st.cache_update()
+    torch.cuda.synchronize()
+    M = call.k_cache.shape[2]
+    kv_len = 90 + 150
+    perm = torch.randperm(kv_len, generator=torch.Generator().manual_seed(3))
+    kp = torch.full((1, M + 8), -1, dtype=torch.int32)
+    kp[0, :kv_len] = perm.to(torch.int32)
+    kc = torch.full((1, 2, M + 8, 128), float("nan"), dtype=torch.bfloat16, device=cuda)
+    vc = torch.full_like(kc, float("nan"))
+    kc[0, :, :kv_len] = st.call.k_cache[0, :, perm.to(cuda)]
+    vc[0, :, :kv_len] = st.call.v_cache[0, :, perm.to(cuda)]
+    out = torch.empty_like(st.q_rot)
+    c = st.call
+    ab.attn_prefill(st.L, st.q_rot, c.n_prefill, kc, vc, 1, M + 8, 1, c.q_start, c.pf_rows, c.pf_first_pos,
+                    c.max_q_len, kp.to(cuda), out)
+    torch.cuda.synchronize()
+    ab.check_device_error()
+    _close(out, ref)
+
+
+def test_fp32_decode_and_generic_fallbacks(cuda):
+    """fp32 decode (CUDA-core kernel at 1e-4), bf16 d = 64 and a GQA group of 16 (also the CUDA-core kernel)."""
+    c32 = _decode_call([40, 1, 513], dtype=torch.float32)
+    st, _ = _run(c32, cuda)
+    _close(st.out, ostep.run_layer_call(c32)["out"], fp32=True)
+    c64 = _prefill_call([100, 33], [0, 50], hq=4, hkv=2, d=64)
+    st, _ = _run(c64, cuda)
+    _close(st.out, ostep.run_layer_call(c64)["out"])
+    g16 = _decode_call([300, 2], hq=16, hkv=1)
+    st, _ = _run(g16, cuda)
+    _close(st.out, ostep.run_layer_call(g16)["out"])
+
+
+def test_out_of_range_rows_are_reported_not_faulted(cuda):
+    ab = _abi()
+    from decoder_attention_gb300 import step
+    for call in (_decode_call([50, 60]), _prefill_call([40, 30], [0, 10])):
+        g = call.to(cuda)
+        st = step.AttentionStep(g)
+        st.rope()
+        st.cache_update()
+        torch.cuda.synchronize()
+        ab.check_device_error()
+        bad = g.dec_rows.clone() if call.n_decode else g.pf_rows.clone()
+        bad[1] = 9999
+        if call.n_decode:
+            g.dec_rows = bad
+            st.decode()
+            rows_out = st.out[1]
+        else:
+            g.pf_rows = bad
+            st.prefill()
+            qs = g.q_start.tolist()
+            rows_out = st.out[qs[1]:qs[2]]
+        torch.cuda.synchronize()
+        with pytest.raises(ab.DecAttnError) as ei:
+            ab.check_device_error()
+        assert ei.value.code == ab.DA_ERR_DEVICE_INDEX
+        assert torch.count_nonzero(rows_out) == 0          # the bad sequence's outputs are zero
+        ab.check_device_error()                             # the word was cleared
+
+
+def test_rope_tables_at_long_positions(cuda):
+    """cos/sin at positions up to 2^17 against fp64 (llama3 scaling and LongRoPE's long table)."""
+    ab = _abi()
+    pos = torch.tensor([0, 1, 4095, 4096, 8191, 65535, 100003, 131071], dtype=torch.int32)
+    for theta, sc, r, mpe in ((5e5, {"rope_type": "llama3", "factor": 8.0, "low_freq_factor": 1.0,
+                                     "high_freq_factor": 4.0, "original_max_position_embeddings": 8192}, 128, 131072),
+                              (1e4, {"rope_type": "longrope", "short_factor": list(np.linspace(1, 1.2, 48)),
+                                     "long_factor": list(np.linspace(1, 40, 48)),
+                                     "original_max_position_embeddings": 4096}, 96, 131072)):
+        rs, keep = ab.rope_scaling(theta, r, sc, mpe)
+        lens = pos + 1
+        cos = torch.empty((len(pos), r // 2), dtype=torch.float32, device=cuda)
+        sin = torch.empty_like(cos)
+        ab.rope_tables_build(rs, pos.to(cuda), lens.to(cuda), len(pos), cos, sin)
+        torch.cuda.synchronize()
+        ab.check_device_error()
+        spec = A.RopeSpec(theta=theta, scaling=sc, max_position_embeddings=mpe)
+        rc, rsn = A.rope_tables_for_tokens(spec, r, pos.numpy(), lens.numpy())
+        np.testing.assert_allclose(cos.cpu().double().numpy(), rc, atol=5e-7, rtol=0)
+        np.testing.assert_allclose(sin.cpu().double().numpy(), rsn, atol=5e-7, rtol=0)
