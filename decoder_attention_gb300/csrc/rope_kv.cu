@@ -115,155 +115,159 @@ struct Vec16<float> {
   }
 };
 
-// Each head vector (d elements) is handled by d / VEC threads, each owning 16 bytes (VEC consecutive
-// elements). Items are (token, head) for the Hq query heads followed by the Hkv key heads of each token;
-// a key item also copies the token's value vector for that head into the V cache (bit for bit).
-// SHFL: r/2 is a multiple of VEC, so a thread's rotation partner (element i +- r/2) is another thread's
-// whole 16-byte piece: it comes by warp shuffle and the thread's cos/sin are VEC consecutive table
-// entries (vector loads). Otherwise the normalised vector is staged in shared memory.
+// One warp per token. Lane l owns the 16-byte piece sub = l % TPV (VEC consecutive elements) of a head
+// vector, TPV = d / VEC lanes per vector, HPW = 32 / TPV vectors per warp at a time; the warp walks the
+// token's Hq query heads then its Hkv key heads. A key head also copies the token's value vector into the
+// V cache (bit for bit). A lane's cos/sin entries and norm weights depend only on its piece, so they are
+// loaded once per token.
+// SHFL: r/2 is a multiple of VEC, so the rotation partner of a lane's piece (elements i +- r/2) is another
+// lane's whole piece: it comes by warp shuffle. Otherwise the normalised vector is staged in shared memory.
 template <typename T, int D, bool SHFL>
 __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
   using V = Vec16<T>;
   constexpr int VEC = V::N;
-  constexpr int TPV = D / VEC;            // threads per vector (8..32)
-  constexpr int VPB = 256 / TPV;          // vectors per block
-  __shared__ float stage[SHFL ? 1 : VPB][SHFL ? 1 : D];
+  constexpr int TPV = D / VEC;            // lanes per vector (8..32)
+  constexpr int HPW = 32 / TPV;           // vectors per warp per step
+  constexpr int WPB = 8;                  // warps per block
+  __shared__ float stage[SHFL ? 1 : WPB][SHFL ? 1 : HPW][SHFL ? 1 : D];
 
-  const int sub = threadIdx.x % TPV;      // which 16-byte piece of the vector
-  const int slot = threadIdx.x / TPV;
-  const int heads = a.hq + a.hkv;
-  const long long item = static_cast<long long>(blockIdx.x) * VPB + slot;
-  const bool live = item < static_cast<long long>(a.n) * heads;
-  int t = 0, hh = 0;
-  if (live) {
-    t = static_cast<int>(item / heads);
-    hh = static_cast<int>(item - static_cast<long long>(t) * heads);
-  }
-  const bool is_q = hh < a.hq;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int t = blockIdx.x * WPB + wib;
+  if (t >= a.n) return;                   // whole warps leave together
+  const int sub = lane % TPV;
+  const int slot = lane / TPV;
   const int e0 = sub * VEC;
-
-  // every global load of the item is issued here, before any of them is used, so that one memory
-  // round trip covers the vector, the value, the slot and the table/weight reads
-  float x[VEC];
-  uint4 vv = make_uint4(0, 0, 0, 0);
-  int row = 0, pos = 0;
-  if (live) {
-    const T* src = is_q ? static_cast<const T*>(a.q) + (static_cast<long long>(t) * a.hq + hh) * D
-                        : static_cast<const T*>(a.k) + (static_cast<long long>(t) * a.hkv + (hh - a.hq)) * D;
-    V::load(src + e0, x);
-    if (!is_q) {
-      vv = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.v) +
-                                           (static_cast<long long>(t) * a.hkv + (hh - a.hq)) * D + e0);
-      row = a.rows[t];
-      pos = a.positions[t];
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) x[j] = 0.f;
-  }
   const int half = a.rot >> 1;
-  float c[VEC], sv[VEC];
-  bool lower = false, upper = false;
-  if (SHFL) {
-    const int hc = half / VEC;                       // pieces per half
-    lower = sub < hc;
-    upper = sub >= hc && sub < 2 * hc;
-    if (live && (lower || upper)) {
-      const int ci = (lower ? sub : sub - hc) * VEC;
-      const float* cs = a.cos + static_cast<long long>(t) * half + ci;
-      const float* sn = a.sin + static_cast<long long>(t) * half + ci;
-#pragma unroll
-      for (int j = 0; j < VEC; j += 4) {
-        const float4 c4 = *reinterpret_cast<const float4*>(cs + j);
-        const float4 s4 = *reinterpret_cast<const float4*>(sn + j);
-        c[j] = c4.x; c[j + 1] = c4.y; c[j + 2] = c4.z; c[j + 3] = c4.w;
-        sv[j] = s4.x; sv[j + 1] = s4.y; sv[j + 2] = s4.z; sv[j + 3] = s4.w;
-      }
-    }
-  }
+  const int heads = a.hq + a.hkv;
 
-  // RMSNorm over the head: x / sqrt(mean(x^2) + eps) * w
-  if (a.q_norm_w != nullptr) {
-    const float* w = is_q ? a.q_norm_w : a.k_norm_w;
-    float wv[VEC];
+  // per-token, per-piece data: cos/sin of the piece's pairs, norm weights, the token's cache slot
+  float c[VEC], sv[VEC], wq[VEC], wk[VEC];
+  const int hc = half / VEC;               // pieces per half (SHFL path)
+  const bool lower = SHFL && sub < hc, upper = SHFL && sub >= hc && sub < 2 * hc;
+  if (SHFL && (lower || upper)) {
+    const int ci = (lower ? sub : sub - hc) * VEC;
+    const float* cs = a.cos + static_cast<long long>(t) * half + ci;
+    const float* sn = a.sin + static_cast<long long>(t) * half + ci;
 #pragma unroll
     for (int j = 0; j < VEC; j += 4) {
-      const float4 w4 = *reinterpret_cast<const float4*>(w + e0 + j);
-      wv[j] = w4.x; wv[j + 1] = w4.y; wv[j + 2] = w4.z; wv[j + 3] = w4.w;
+      const float4 c4 = *reinterpret_cast<const float4*>(cs + j);
+      const float4 s4 = *reinterpret_cast<const float4*>(sn + j);
+      c[j] = c4.x; c[j + 1] = c4.y; c[j + 2] = c4.z; c[j + 3] = c4.w;
+      sv[j] = s4.x; sv[j + 1] = s4.y; sv[j + 2] = s4.z; sv[j + 3] = s4.w;
     }
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) ss = fmaf(x[j], x[j], ss);
-#pragma unroll
-    for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
-    const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * wv[j];
   }
-
-  // split-half rotation of the first `rot` dims: x'_i = x_i c - x_{i+h} s, x'_{i+h} = x_{i+h} c + x_i s
-  float y[VEC];
-  if (SHFL) {
-    const int hc = half / VEC;
-    const int psub = lower ? sub + hc : (upper ? sub - hc : sub);
-    const int src_lane = (threadIdx.x & 31 & ~(TPV - 1)) | psub;
-    float px[VEC];
+  const bool norm = a.q_norm_w != nullptr;
+  if (norm) {
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) px[j] = __shfl_sync(0xffffffffu, x[j], src_lane);
-    if (lower || upper) {
-      const float sgn = lower ? -1.f : 1.f;
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) y[j] = fmaf(sgn * px[j], sv[j], x[j] * c[j]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) y[j] = x[j];
+    for (int j = 0; j < VEC; j += 4) {
+      const float4 q4 = *reinterpret_cast<const float4*>(a.q_norm_w + e0 + j);
+      const float4 k4 = *reinterpret_cast<const float4*>(a.k_norm_w + e0 + j);
+      wq[j] = q4.x; wq[j + 1] = q4.y; wq[j + 2] = q4.z; wq[j + 3] = q4.w;
+      wk[j] = k4.x; wk[j + 1] = k4.y; wk[j + 2] = k4.z; wk[j + 3] = k4.w;
     }
-  } else {
+  }
+  const int row = a.rows[t];
+  const int pos = a.positions[t];
+  const bool slot_ok = row >= 0 && row < a.num_rows && pos >= 0 && pos < a.max_len;
+  if (!slot_ok && lane == 0) set_error(a.err, kErrIndex);
+  const long long slot_base = slot_ok ? (static_cast<long long>(row) * a.hkv * a.max_len + pos) * D : 0;
+
+  // U heads per lane are loaded before any is processed: enough loads in flight to cover HBM latency
+  constexpr int U = 4;
+  const int steps = (heads + HPW - 1) / HPW;
+  for (int it0 = 0; it0 < steps; it0 += U) {
+    uint4 xr[U], vr[U];
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) stage[slot][e0 + j] = x[j];
-    __syncwarp();
-    const float* cs = a.cos + static_cast<long long>(t) * half;
-    const float* sn = a.sin + static_cast<long long>(t) * half;
+    for (int u = 0; u < U; ++u) {
+      const int hh = (it0 + u) * HPW + slot;
+      xr[u] = make_uint4(0, 0, 0, 0);
+      vr[u] = make_uint4(0, 0, 0, 0);
+      if (hh < heads) {
+        const bool q_head = hh < a.hq;
+        const T* src = q_head ? static_cast<const T*>(a.q) + (static_cast<long long>(t) * a.hq + hh) * D
+                              : static_cast<const T*>(a.k) + (static_cast<long long>(t) * a.hkv + (hh - a.hq)) * D;
+        xr[u] = *reinterpret_cast<const uint4*>(src + e0);
+        if (!q_head)
+          vr[u] = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.v) +
+                                                  (static_cast<long long>(t) * a.hkv + (hh - a.hq)) * D + e0);
+      }
+    }
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-      const int e = e0 + j;
-      if (e < half) {
-        y[j] = live ? x[j] * cs[e] - stage[slot][e + half] * sn[e] : 0.f;
-      } else if (e < a.rot) {
-        y[j] = live ? x[j] * cs[e - half] + stage[slot][e - half] * sn[e - half] : 0.f;
+    for (int u = 0; u < U; ++u) {
+      const int it = it0 + u;
+      const int hh = it * HPW + slot;
+      const bool live = hh < heads;
+      const bool is_q = hh < a.hq;
+      const int g = hh - a.hq;
+      float x[VEC];
+      V::load(&xr[u], x);
+      const uint4 vv = vr[u];
+      // RMSNorm over the head: x / sqrt(mean(x^2) + eps) * w
+      if (norm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) ss = fmaf(x[j], x[j], ss);
+#pragma unroll
+        for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
+        const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * (is_q ? wq[j] : wk[j]);
+      }
+      // split-half rotation of the first `rot` dims: x'_i = x_i c - x_{i+h} s, x'_{i+h} = x_{i+h} c + x_i s
+      float y[VEC];
+      if (SHFL) {
+        const int psub = lower ? sub + hc : (upper ? sub - hc : sub);
+        const int src_lane = slot * TPV + psub;
+        float px[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) px[j] = __shfl_sync(0xffffffffu, x[j], src_lane);
+        if (lower || upper) {
+          const float sgn = lower ? -1.f : 1.f;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) y[j] = fmaf(sgn * px[j], sv[j], x[j] * c[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) y[j] = x[j];
+        }
       } else {
-        y[j] = x[j];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) stage[wib][slot][e0 + j] = x[j];
+        __syncwarp();
+        const float* cs = a.cos + static_cast<long long>(t) * half;
+        const float* sn = a.sin + static_cast<long long>(t) * half;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          const int e = e0 + j;
+          if (e < half) {
+            y[j] = x[j] * cs[e] - stage[wib][slot][e + half] * sn[e];
+          } else if (e < a.rot) {
+            y[j] = x[j] * cs[e - half] + stage[wib][slot][e - half] * sn[e - half];
+          } else {
+            y[j] = x[j];
+          }
+        }
+        __syncwarp();
+      }
+      if (!live) continue;
+      if (is_q) {
+        V::store(static_cast<T*>(a.q_rot) + (static_cast<long long>(t) * a.hq + hh) * D + e0, y);
+      } else if (slot_ok) {
+        const long long off = slot_base + static_cast<long long>(g) * a.max_len * D + e0;
+        V::store(static_cast<T*>(a.k_cache) + off, y);
+        *reinterpret_cast<uint4*>(static_cast<T*>(a.v_cache) + off) = vv;
       }
     }
   }
-  if (!live) return;
-
-  if (is_q) {
-    T* dst = static_cast<T*>(a.q_rot) + (static_cast<long long>(t) * a.hq + hh) * D;
-    V::store(dst + e0, y);
-    return;
-  }
-  const int g = hh - a.hq;
-  if (row < 0 || row >= a.num_rows || pos < 0 || pos >= a.max_len) {
-    if (sub == 0) set_error(a.err, kErrIndex);
-    return;
-  }
-  const long long slot_off = ((static_cast<long long>(row) * a.hkv + g) * a.max_len + pos) * D;
-  V::store(static_cast<T*>(a.k_cache) + slot_off + e0, y);
-  *reinterpret_cast<uint4*>(static_cast<T*>(a.v_cache) + slot_off + e0) = vv;
 }
 
 template <typename T, int D>
 static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
-  constexpr int TPV = D / Vec16<T>::N;
-  constexpr int VPB = 256 / TPV;
-  const long long items = static_cast<long long>(a.n) * (a.hq + a.hkv);
-  if (items == 0) return cudaSuccess;
-  const long long blocks = (items + VPB - 1) / VPB;
+  if (a.n == 0) return cudaSuccess;
+  const int blocks = (a.n + 7) / 8;   // 8 warps (tokens) per block
   if ((a.rot / 2) % Vec16<T>::N == 0)
-    kv_update_kernel<T, D, true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    kv_update_kernel<T, D, true><<<blocks, 256, 0, stream>>>(a);
   else
-    kv_update_kernel<T, D, false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    kv_update_kernel<T, D, false><<<blocks, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,8 @@ soft-capping):
 
 Each builder takes ``scale``: "full" is the workload itself; "small" keeps its structure (several tiles,
 ragged tails, windows that bind, longrope on both sides of its switch) at sizes the fp64 oracle finishes
-in seconds. Tensor draws come from a ``torch.Generator`` seeded with 1000 + workload number, in a fixed
+in seconds; "profile" (decode and mixed workloads) keeps the full head shapes with fewer sequences or
+shorter contexts, so that the caches stay within a few GB for profiler captures. Tensor draws come from a ``torch.Generator`` seeded with 1000 + workload number, in a fixed
 order (q, k, v, norm weights, cache K, cache V); context lengths, chunk starts and row permutations come
 from a second CPU generator seeded with 2000 + workload number. Full-size caches are drawn on the device
 from a generator of their own, so that no multi-GB tensor is staged on the host.
@@ -234,6 +235,8 @@ def mistral_swa_decode(scale="full", device="cpu"):
     g = _gen(1003)
     if scale == "full":
         S, lo, hi, w, hq, hkv, M = 64, 1024, 32768, 4096, 32, 8, 32768
+    elif scale == "profile":
+        S, lo, hi, w, hq, hkv, M = 16, 1024, 32768, 4096, 32, 8, 32768
     else:
         S, lo, hi, w, hq, hkv, M = 12, 40, 2000, 300, 8, 2, 2000
     d = 128
@@ -254,6 +257,8 @@ def llama31_8b_long_decode(scale="full", device="cpu"):
     d = 128
     if scale == "full":
         lens, hq, hkv, M = [131072] * 16, 32, 8, 131072
+    elif scale == "profile":
+        lens, hq, hkv, M = [16384] * 16, 32, 8, 16384
     else:
         lens, hq, hkv, M = [3000, 2500, 700, 1], 8, 2, 3000
     S = len(lens)
@@ -286,6 +291,9 @@ def phi4_gemma2_mixed(scale="full", device="cpu", q_mult=1.0):
     if scale == "full":
         n_chunks, chunk, n_dec, dlo, dhi, pmax, w, hq, hkv = 8, 1024, 120, 512, 65536, 64512, 4096, 24, 8
         M = 65536
+    elif scale == "profile":
+        n_chunks, chunk, n_dec, dlo, dhi, pmax, w, hq, hkv = 2, 1024, 16, 512, 16384, 15360, 4096, 24, 8
+        M = 16384
     else:
         n_chunks, chunk, n_dec, dlo, dhi, pmax, w, hq, hkv = 3, 100, 9, 50, 6000, 5800, 512, 6, 2
         M = 6000
