@@ -60,6 +60,7 @@ struct KvUpdateArgs {
   void* v_cache;
   int num_rows, max_len;
   int* err;
+  int wpt;                        // warps per token (set by the launcher)
 };
 cudaError_t launch_kv_update(const KvUpdateArgs& a, bool bf16, cudaStream_t stream);
 

@@ -6,6 +6,7 @@
 // and §4 Rotary for the norm, the cache write and the split-half rotation.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -132,7 +133,10 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
   __shared__ float stage[SHFL ? 1 : WPB][SHFL ? 1 : HPW][SHFL ? 1 : D];
 
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int t = blockIdx.x * WPB + wib;
+  // a.wpt warps share a token when tokens are few (decode), each taking every wpt-th group of heads
+  const long long gw = static_cast<long long>(blockIdx.x) * WPB + wib;
+  const int t = static_cast<int>(gw / a.wpt);
+  const int part = static_cast<int>(gw - static_cast<long long>(t) * a.wpt);
   if (t >= a.n) return;                   // whole warps leave together
   const int sub = lane % TPV;
   const int slot = lane / TPV;
@@ -175,11 +179,11 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
   // U heads per lane are loaded before any is processed: enough loads in flight to cover HBM latency
   constexpr int U = 4;
   const int steps = (heads + HPW - 1) / HPW;
-  for (int it0 = 0; it0 < steps; it0 += U) {
+  for (int it0 = part; it0 < steps; it0 += U * a.wpt) {
     uint4 xr[U], vr[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int hh = (it0 + u) * HPW + slot;
+      const int hh = (it0 + u * a.wpt) * HPW + slot;
       xr[u] = make_uint4(0, 0, 0, 0);
       vr[u] = make_uint4(0, 0, 0, 0);
       if (hh < heads) {
@@ -194,7 +198,7 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int it = it0 + u;
+      const int it = it0 + u * a.wpt;
       const int hh = it * HPW + slot;
       const bool live = hh < heads;
       const bool is_q = hh < a.hq;
@@ -263,11 +267,17 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
 template <typename T, int D>
 static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
   if (a.n == 0) return cudaSuccess;
-  const int blocks = (a.n + 7) / 8;   // 8 warps (tokens) per block
+  // warps per token: enough warps in the grid (~2048) to cover memory latency, at most one per head group
+  constexpr int HPW = 32 / (D / Vec16<T>::N);
+  const int groups = (a.hq + a.hkv + HPW - 1) / HPW;
+  KvUpdateArgs b = a;
+  b.wpt = std::max(1, std::min(groups, (2048 + a.n - 1) / a.n));
+  const long long warps = static_cast<long long>(a.n) * b.wpt;
+  const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);   // 8 warps per block
   if ((a.rot / 2) % Vec16<T>::N == 0)
-    kv_update_kernel<T, D, true><<<blocks, 256, 0, stream>>>(a);
+    kv_update_kernel<T, D, true><<<blocks, 256, 0, stream>>>(b);
   else
-    kv_update_kernel<T, D, false><<<blocks, 256, 0, stream>>>(a);
+    kv_update_kernel<T, D, false><<<blocks, 256, 0, stream>>>(b);
   return cudaGetLastError();
 }
 
