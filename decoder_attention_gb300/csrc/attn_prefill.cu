@@ -53,9 +53,9 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + NQT * TILE;
 constexpr int OFF_V = OFF_K + NK * TILE;
 constexpr int OFF_BAR = OFF_V + NV * TILE;
-// barriers: q, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[NQT], p_full[NQT], o_done
-constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + NK, B_VF = B_KE + NK, B_VE = B_VF + NV, B_SF = B_VE + NV,
-              B_PF = B_SF + NQT, B_OD = B_PF + NQT, N_BARS = B_OD + 1;
+// barriers: q[NQT], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[NQT], p_full[NQT], o_done[NQT]
+constexpr int B_Q = 0, B_KF = B_Q + NQT, B_KE = B_KF + NK, B_VF = B_KE + NK, B_VE = B_VF + NV, B_SF = B_VE + NV,
+              B_PF = B_SF + NQT, B_OD = B_PF + NQT, N_BARS = B_OD + NQT;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + TMEM address slot + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TMEM_COLS = 512;
@@ -131,6 +131,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmq,
                                                              const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
+                                                             const __grid_constant__ CUtensorMap tmo,
                                                              const Params prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -189,7 +190,6 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(B(B_Q), 1);
     for (int i = 0; i < NK; ++i) {
       mbar_init(B(B_KF + i), 1);
       mbar_init(B(B_KE + i), 1);
@@ -201,8 +201,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     for (int w = 0; w < NQT; ++w) {
       mbar_init(B(B_SF + w), 1);
       mbar_init(B(B_PF + w), BM);
+      mbar_init(B(B_OD + w), 1);
+      mbar_init(B(B_Q + w), 1);
     }
-    mbar_init(B(B_OD), 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -219,18 +220,24 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
     if (warp == 8 && lane == 0) {
-      // ---------------------------------------------------------------- TMA producer: Q, then K tiles
+      // ---------------------------------------------------------------- TMA producer: Q0, K0, Q1, K1, ...
+      // (the first scores need only Q0 and the first K tile, so Q1 queues behind them)
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
-      const int nq = valid1 ? 2 : 1;
-      mbar_arrive_expect_tx(B(B_Q), nq * TILE);
-      for (int w = 0; w < nq; ++w) {
+      auto load_q = [&](int w) {
         const int tok = t0 + q0 + w * BM;
-        tma_load_3d(sbase + OFF_Q + w * TILE, &tmq, B(B_Q), 0, h, tok);
-        tma_load_3d(sbase + OFF_Q + w * TILE + HALF, &tmq, B(B_Q), 64, h, tok);
-      }
+        mbar_arrive_expect_tx(B(B_Q + w), TILE);
+        tma_load_3d(sbase + OFF_Q + w * TILE, &tmq, B(B_Q + w), 0, h, tok);
+        tma_load_3d(sbase + OFF_Q + w * TILE + HALF, &tmq, B(B_Q + w), 64, h, tok);
+      };
+      load_q(0);
+      bool q1_loaded = false;
       int issued = 0;
       for (int i = 0; i < n_tiles && !*vabort; ++i) {
+        if (i == 1 && valid1) {
+          load_q(1);
+          q1_loaded = true;
+        }
         const int st = i % NK;
         if (i >= NK && !mbar_wait(B(B_KE + st), ((i / NK) + 1) & 1, prm.err)) {
           abort_flag = 1;
@@ -242,8 +249,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         tma_load_2d(sbase + OFF_K + st * TILE + HALF, &tmk, B(B_KF + st), 64, key);
         ++issued;
       }
+      if (valid1 && !q1_loaded && !*vabort) {
+        load_q(1);
+        q1_loaded = true;
+      }
       // every issued copy must land before the CTA's shared memory is released
-      mbar_wait(B(B_Q), 0, prm.err);
+      mbar_wait(B(B_Q + 0), 0, prm.err);
+      if (q1_loaded) mbar_wait(B(B_Q + 1), 0, prm.err);
       for (int i = max(0, issued - NK); i < issued; ++i) mbar_wait(B(B_KF + i % NK), (i / NK) & 1, prm.err);
     } else if (warp == 10 && lane == 0) {
       // ---------------------------------------------------------------- TMA producer: V tiles
@@ -267,7 +279,16 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       const uint32_t q0s = sbase + OFF_Q, q1s = sbase + OFF_Q + TILE;
       const uint32_t s0t = tmem, s1t = tmem + BN, o0t = tmem + 256, o1t = tmem + 256 + D;
       int npv0 = 0, npv1 = 0;
-      bool ok = mbar_wait(B(B_Q), 0, prm.err) && mbar_wait(B(B_KF), 0, prm.err);
+      bool od0 = false;
+      bool q1_ready = false;
+      auto wait_q1 = [&]() {          // Q1 lands after the first K tile; waited on before its first scores
+        if (!q1_ready) {
+          q1_ready = mbar_wait(B(B_Q + 1), 0, prm.err);
+          tc_fence_after();
+        }
+        return q1_ready;
+      };
+      bool ok = mbar_wait(B(B_Q + 0), 0, prm.err) && mbar_wait(B(B_KF), 0, prm.err);
       tc_fence_after();
       if (ok) {
         // prologue: scores of the first key tile
@@ -276,8 +297,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           tc_commit(B(B_SF + 0));
         }
         if (act1(tbeg)) {
-          issue_s(s1t, q1s, sbase + OFF_K);
-          tc_commit(B(B_SF + 1));
+          ok = wait_q1();
+          if (ok) {
+            issue_s(s1t, q1s, sbase + OFF_K);
+            tc_commit(B(B_SF + 1));
+          }
         }
         tc_commit(B(B_KE + 0));
         ok = mbar_wait(B(B_VF + 0), 0, prm.err);
@@ -297,6 +321,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           tc_fence_after();
           issue_pv(o0t, s0t, vs, npv0 > 0);
           ++npv0;
+          if (t == te0) {
+            tc_commit(B(B_OD + 0));     // Q0's output is final: its epilogue overlaps Q1's last tiles
+            od0 = true;
+          }
         }
         if (nxt) {
           if (!mbar_wait(B(B_KF + kst1), ((i + 1) / NK) & 1, prm.err)) { ok = false; break; }
@@ -317,6 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         tc_commit(B(B_VE + vst));
         if (nxt) {
           if (act1(t + 1)) {
+            if (!wait_q1()) { ok = false; break; }
             issue_s(s1t, q1s, k1s);
             tc_commit(B(B_SF + 1));
           }
@@ -324,8 +353,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         }
       }
       if (!ok) abort_flag = 1;
-      tc_commit(B(B_OD));
-      mbar_wait(B(B_OD), 0, prm.err);   // all MMAs done before TMEM may be released
+      if (!od0) tc_commit(B(B_OD + 0));
+      tc_commit(B(B_OD + 1));
+      mbar_wait(B(B_OD + 1), 0, prm.err);   // all MMAs done before TMEM may be released
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
@@ -454,25 +484,45 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       ++nact;
     }
     // ------------------------------------------------------------ epilogue: O / l -> out
-    if (ok && __all_sync(0xffffffffu, mbar_wait(B(B_OD), 0, prm.err))) {
+    // Each warp normalises its 32 rows into the Q tile's shared memory (free once every MMA is done) in the
+    // 128-byte-swizzled layout and writes them with two TMA tensor stores; a warp whose rows run past the
+    // chunk stores row by row instead (a whole box would overwrite the next sequence's rows).
+    if (ok && __all_sync(0xffffffffu, mbar_wait(B(B_OD + w), 0, prm.err))) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const bool full_tile = q0 + w * BM + wi * 32 + 32 <= n_b;   // warp-uniform
       uint4* orow = reinterpret_cast<uint4*>(prm.out + (static_cast<long long>(t0 + qrow) * prm.hq + h) * D);
+      uint8_t* srow = smem + OFF_Q + w * TILE + r * 128;
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         uint32_t ov[32];
         tmem_ld32(t_o + j * 32, ov);
         tmem_wait_ld();
-        if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 u;
-            u.x = pack_bf16(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
-            u.y = pack_bf16(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
-            u.z = pack_bf16(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
-            u.w = pack_bf16(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
-            orow[j * 4 + e] = u;
+        for (int e = 0; e < 4; ++e) {
+          uint4 u;
+          u.x = pack_bf16(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
+          u.y = pack_bf16(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
+          u.z = pack_bf16(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
+          u.w = pack_bf16(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
+          const int c16 = j * 4 + e;                 // 16-byte chunk of the row, 0..15
+          if (full_tile) {
+            *reinterpret_cast<uint4*>(srow + (c16 >> 3) * HALF + (((c16 & 7) ^ (r & 7)) << 4)) = u;
+          } else if (row_ok) {
+            orow[c16] = u;
           }
+        }
+      }
+      if (full_tile) {
+        fence_proxy_async_smem();                    // generic-proxy writes -> visible to the copy engine
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t src = sbase + OFF_Q + w * TILE + wi * 32 * 128;   // 4 KB aligned: swizzle phase 0
+          const int tok = t0 + q0 + w * BM + wi * 32;
+          tma_store_3d(&tmo, src, 0, h, tok);
+          tma_store_3d(&tmo, src + HALF, 64, h, tok);
+          bulk_commit();
+          bulk_wait_read();                          // shared memory stays valid until the copies read it
         }
       }
     } else {
@@ -491,11 +541,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   using namespace pf;
   if (a.n_seqs == 0 || a.max_q_len == 0 || a.n_tokens == 0) return cudaSuccess;
-  CUtensorMap tmq, tmk, tmv;
+  CUtensorMap tmq, tmk, tmv, tmo;
   const uint64_t rows_total = static_cast<uint64_t>(a.num_rows) * a.hkv * a.max_len;
-  // q_rot [N, Hq, D]: rows past N are zero-filled by the copy engine, never read from memory
+  // q_rot and out [N, Hq, D]: q rows past N are zero-filled by the copy engine, never read from memory; out
+  // boxes are only stored whole when all their rows belong to the chunk
   const uint64_t n_tok = static_cast<uint64_t>(a.n_tokens);
   if (!encode_tmap_3d_bf16(&tmq, a.q_rot, D, a.hq, n_tok, D * 2, static_cast<uint64_t>(a.hq) * D * 2, 64, 1, BM) ||
+      !encode_tmap_3d_bf16(&tmo, a.out, D, a.hq, n_tok, D * 2, static_cast<uint64_t>(a.hq) * D * 2, 64, 1, 32) ||
       !encode_tmap_2d_bf16(&tmk, a.k_cache, D, rows_total, D * 2, 64, BN) ||
       !encode_tmap_2d_bf16(&tmv, a.v_cache, D, rows_total, D * 2, 64, BN))
     return cudaErrorInvalidValue;
@@ -516,7 +568,7 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int n_qt = (a.max_q_len + NQT * BM - 1) / (NQT * BM);
   dim3 grid(a.hq * a.n_seqs, n_qt);
-  prefill_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, prm);
+  prefill_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
   return cudaGetLastError();
 }
 
