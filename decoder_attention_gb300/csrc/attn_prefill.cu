@@ -110,22 +110,57 @@ __device__ __forceinline__ float row_pass(uint32_t (&zr)[BN], float cap_in, floa
 }
 
 // The 8 MMAs (K = 16 each) of S = Q K^T for one 128 x 128 tile; both operands K-major, 128-byte swizzled
-// in two 64-wide halves.
+// in two 64-wide halves. One asm block with the descriptors stepped by immediate adds: the issuing thread
+// shares its SM sub-partition with two softmax warps, and every instruction between MMAs delays the next.
+// The start-address field of a descriptor holds address >> 4 in bits [0, 14); shared addresses stay below
+// 2^18, so adding to the low word never carries out of the field. Steps per K = 16 slice (16-byte units):
+// 32 bytes within a 128-byte row, then the second 64-wide half 16 KB on.
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, false);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
-  }
+  const uint64_t a = sdesc_sw128(q_smem, 16, 1024), b = sdesc_sw128(k_smem, 16, 1024);
+  asm volatile(
+      "{\n\t"
+      ".reg .b32 alo, ahi, blo, bhi, x, y;\n\t"
+      ".reg .b64 da, db;\n\t"
+      ".reg .pred pf, pt;\n\t"
+      "setp.ne.b32 pf, %3, %3;\n\t"
+      "setp.eq.b32 pt, %3, %3;\n\t"
+      "mov.b64 {alo, ahi}, %1;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+#define DA_S_STEP(o)                                                        \
+      "add.u32 x, alo, " #o "; add.u32 y, blo, " #o ";\n\t"                 \
+      "mov.b64 da, {x, ahi}; mov.b64 db, {y, bhi};\n\t"                     \
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"
+      DA_S_STEP(2) DA_S_STEP(4) DA_S_STEP(6) DA_S_STEP(1024) DA_S_STEP(1026) DA_S_STEP(1028) DA_S_STEP(1030)
+#undef DA_S_STEP
+      "}" ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc)
+      : "memory");
 }
 
-// The 8 MMAs (K = 16 keys each) of O (+)= P V; P from TMEM (bf16, 2 per column), V MN-major in smem.
+// The 8 MMAs (K = 16 keys each) of O (+)= P V; P from TMEM (bf16, 2 per column: 8 columns per slice), V
+// MN-major in smem (16 key rows = 2048 bytes per slice). One asm block, as for issue_s.
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(BM, D, false, true);
-#pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk)
-    mma_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 2048, HALF, 1024), idesc, (accumulate || kk > 0) ? 1u : 0u);
+  const uint64_t b = sdesc_sw128(v_smem, HALF, 1024);
+  asm volatile(
+      "{\n\t"
+      ".reg .b32 blo, bhi, x, y;\n\t"
+      ".reg .b64 db;\n\t"
+      ".reg .pred p0, pt;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\t"
+      "setp.eq.b32 pt, %3, %3;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+#define DA_PV_STEP(ta, o)                                                   \
+      "add.u32 x, %1, " #ta "; add.u32 y, blo, " #o ";\n\t"                 \
+      "mov.b64 db, {y, bhi};\n\t"                                           \
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x], db, %3, pt;\n\t"
+      DA_PV_STEP(8, 128) DA_PV_STEP(16, 256) DA_PV_STEP(24, 384) DA_PV_STEP(32, 512) DA_PV_STEP(40, 640)
+      DA_PV_STEP(48, 768) DA_PV_STEP(56, 896)
+#undef DA_PV_STEP
+      "}" ::"r"(o_tmem), "r"(p_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
 }
 
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmq,
