@@ -86,6 +86,34 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// 32 lanes x 128 consecutive 32-bit columns in one tcgen05.ld (one tensor-memory request per warp instead
+// of four; the MMA issuer's tcgen05 operations queue behind the softmax warps' loads and stores).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
+      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,"
+      "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+      "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127"
+      "}, [%128];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr));
+}
+
+// 32 lanes x 64 consecutive 32-bit columns in one tcgen05.st.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {"
+      "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
+      "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+      "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64"
+      "};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63]) : "memory");
+}
+
 // One pass over a row's 128 scores: soft-cap (CAP), mask to the visible column range [lo_c, hi_c] (MASK),
 // and the row max with 8 independent partial maxima (one running max would be a 128-long dependency chain).
 template <bool CAP, bool MASK>
@@ -339,18 +367,24 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           }
         }
         tc_commit(B(B_KE + 0));
-        ok = mbar_wait(B(B_VF + 0), 0, prm.err);
       }
-      // The waits that are normally already satisfied (K and V copies) sit where the tensor core still has
-      // queued work; the gap between issuing S1(t+1) and PV0(t+1) -- the tensor core's idle window when
-      // P0(t+1) is late -- holds only the P0 wait.
+      // Per round (key tile t): PV0(t), S0(t+1), PV1(t), S1(t+1). Each tcgen05.mma blocks the issuing
+      // thread until the tensor core takes it (the queue is short), so any wait between two MMA groups
+      // idles the tensor core. The operand waits (V(t), K(t+1), Q1), normally satisfied long before,
+      // therefore sit at the top of the round, while the previous round's last group still runs; between
+      // groups there are only the P waits. Ring stages and phases advance by counting, not dividing.
+      int kst1 = 1 % NK, kph1 = (1 / NK) & 1;   // K(t+1)
+      int vst = 0, vph = 0;                      // V(t)
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int t = tbeg + i;
         const bool nxt = i + 1 < n_tiles;
-        const int kst1 = (i + 1) % NK;
         const uint32_t k1s = sbase + OFF_K + kst1 * TILE;
-        const int vst = i % NV;
         const uint32_t vs = sbase + OFF_V + vst * TILE;
+        if (!mbar_wait(B(B_VF + vst), vph, prm.err) || (nxt && !mbar_wait(B(B_KF + kst1), kph1, prm.err)) ||
+            (nxt && act1(t + 1) && !wait_q1())) {
+          ok = false;
+          break;
+        }
         if (act0(t)) {
           if (!mbar_wait(B(B_PF + 0), npv0 & 1, prm.err)) { ok = false; break; }
           tc_fence_after();
@@ -361,15 +395,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             od0 = true;
           }
         }
-        if (nxt) {
-          if (!mbar_wait(B(B_KF + kst1), ((i + 1) / NK) & 1, prm.err)) { ok = false; break; }
-          tc_fence_after();
-          if (act0(t + 1)) {
-            issue_s(s0t, q0s, k1s);
-            tc_commit(B(B_SF + 0));
-          }
-          // V of the next tile, for the next iteration's PVs
-          if (!mbar_wait(B(B_VF + (i + 1) % NV), ((i + 1) / NV) & 1, prm.err)) { ok = false; break; }
+        if (nxt && act0(t + 1)) {
+          issue_s(s0t, q0s, k1s);
+          tc_commit(B(B_SF + 0));
         }
         if (act1(t)) {
           if (!mbar_wait(B(B_PF + 1), npv1 & 1, prm.err)) { ok = false; break; }
@@ -380,11 +408,18 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         tc_commit(B(B_VE + vst));
         if (nxt) {
           if (act1(t + 1)) {
-            if (!wait_q1()) { ok = false; break; }
             issue_s(s1t, q1s, k1s);
             tc_commit(B(B_SF + 1));
           }
           tc_commit(B(B_KE + kst1));
+        }
+        if (++kst1 == NK) {
+          kst1 = 0;
+          kph1 ^= 1;
+        }
+        if (++vst == NV) {
+          vst = 0;
+          vph ^= 1;
         }
       }
       if (!ok) abort_flag = 1;
@@ -429,7 +464,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       tc_fence_after();
       uint32_t zr[BN];
 #pragma unroll
-      for (int j = 0; j < BN / 32; ++j) tmem_ld32(t_s + j * 32, *reinterpret_cast<uint32_t(*)[32]>(&zr[j * 32]));
+      tmem_ld128(t_s, zr);
       tmem_wait_ld();
       const int kstart = t * BN;
       const bool need_mask = !(kstart + BN - 1 <= my_pmin &&
@@ -472,20 +507,16 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       // p = 2^(z * zmul - m) two scores at a time (packed fp32 pairs), row sum in 4 packed accumulators
       const uint64_t zmul2 = f2_pack(zmul, zmul), nmu2 = f2_pack(nmu, nmu);
       uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[BN / 2];
 #pragma unroll
-      for (int j = 0; j < BN / 32; ++j) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float xa, xb;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(zr[j * 32 + 2 * e]), __uint_as_float(zr[j * 32 + 2 * e + 1])),
-                           zmul2, nmu2), xa, xb);
-          const float pa = ex2(xa), pb = ex2(xb);
-          ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(pa, pb));
-          pk[e] = pack_bf16(pa, pb);
-        }
-        tmem_st16(t_s + j * 16, pk);     // P (bf16, 2 per column) over the first half of the S columns
+      for (int e = 0; e < BN / 2; ++e) {
+        float xa, xb;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(zr[2 * e]), __uint_as_float(zr[2 * e + 1])), zmul2, nmu2), xa, xb);
+        const float pa = ex2(xa), pb = ex2(xb);
+        ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(pa, pb));
+        pk[e] = pack_bf16(pa, pb);
       }
+      tmem_st64(t_s, pk);     // P (bf16, 2 per column) over the first half of the S columns
       {
         float a0, a1, b0, b1, c0, c1, d0, d1;
         f2_unpack(f2_add(ls2[0], ls2[1]), a0, a1);
