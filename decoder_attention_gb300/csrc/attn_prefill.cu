@@ -6,7 +6,8 @@
 // query row, softmax over its visible keys of scale * q.k (optionally c * tanh(. / c)), times V.
 //
 // CTA = 256 query rows (two 128-row tiles Q0, Q1) of one (sequence, query head). Key tiles of 128 keys
-// stream by TMA (128-byte swizzle) through a 3-stage K ring and a 2-stage V ring. Roles:
+// stream by TMA (128-byte swizzle) through a 2-stage ring whose stage holds one round's K and V tiles.
+// Roles:
 //   warp 8      TMA producer of Q (once) and K tiles
 //   warp 10     TMA producer of V tiles
 //   warp 9      MMA issuer (one thread): S_w = Q_w K^T into TMEM; O_w += P_w V with P_w read from TMEM
@@ -34,8 +35,7 @@ constexpr int BM = 128;             // rows per Q tile
 constexpr int BN = 128;             // keys per K/V tile
 constexpr int D = 128;
 constexpr int NQT = 2;              // Q tiles per CTA
-constexpr int NK = 3;               // K ring stages
-constexpr int NV = 2;               // V ring stages
+constexpr int NS = 2;               // ring stages; stage of round slot j holds K(tbeg + j) and V(tbeg + j - 1)
 constexpr int THREADS = 384;        // 3 warpgroups: softmax Q0, softmax Q1, producers/MMA
 // setmaxnreg split: launched at 168 per thread (384 x 168 = 64512); softmax warpgroups rise to 216 and
 // the producer/MMA warpgroup drops to 72: 256 x 216 + 128 x 72 = 64512, the launch total (per SMSP, one
@@ -50,11 +50,11 @@ static_assert(256 * REGS_SOFTMAX + 128 * REGS_CTRL == 384 * 168, "register split
 constexpr int HALF = 128 * 128;     // bytes of a 64-wide half of a 128-row tile (16 KB)
 constexpr int TILE = 2 * HALF;      // 32 KB
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + NQT * TILE;
-constexpr int OFF_V = OFF_K + NK * TILE;
-constexpr int OFF_BAR = OFF_V + NV * TILE;
-// barriers: q[NQT], k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[NQT], p_full[NQT], o_done[NQT]
-constexpr int B_Q = 0, B_KF = B_Q + NQT, B_KE = B_KF + NK, B_VF = B_KE + NK, B_VE = B_VF + NV, B_SF = B_VE + NV,
+constexpr int OFF_R = OFF_Q + NQT * TILE;   // ring: stage s = K tile at OFF_R + 2s TILE, V tile after it
+constexpr int OFF_BAR = OFF_R + NS * 2 * TILE;
+// barriers: q[NQT], full[NS] (two arrivals: K producer, V producer), empty[NS], s_full[NQT], p_full[NQT],
+// o_done[NQT]
+constexpr int B_Q = 0, B_FU = B_Q + NQT, B_EM = B_FU + NS, B_SF = B_EM + NS,
               B_PF = B_SF + NQT, B_OD = B_PF + NQT, N_BARS = B_OD + NQT;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + TMEM address slot + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -253,13 +253,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < NK; ++i) {
-      mbar_init(B(B_KF + i), 1);
-      mbar_init(B(B_KE + i), 1);
-    }
-    for (int i = 0; i < NV; ++i) {
-      mbar_init(B(B_VF + i), 1);
-      mbar_init(B(B_VE + i), 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(B(B_FU + i), 2);
+      mbar_init(B(B_EM + i), 1);
     }
     for (int w = 0; w < NQT; ++w) {
       mbar_init(B(B_SF + w), 1);
@@ -283,8 +279,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
     if (warp == 8 && lane == 0) {
-      // ---------------------------------------------------------------- TMA producer: Q0, K0, Q1, K1, ...
-      // (the first scores need only Q0 and the first K tile, so Q1 queues behind them)
+      // ---------------------------------------------------------------- TMA producer: Q and K tiles
+      // Round slot j (one ring stage) holds K(tbeg + j) and V(tbeg + j - 1): the K tile the round's scores
+      // need and the V tile its PVs need. This producer fills the K halves (slot n_tiles has none: a bare
+      // arrival). Q0 and the first K tile go first; Q1 queues behind them.
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
       auto load_q = [&](int w) {
@@ -296,20 +294,25 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       load_q(0);
       bool q1_loaded = false;
       int issued = 0;
-      for (int i = 0; i < n_tiles && !*vabort; ++i) {
-        if (i == 1 && valid1) {
+      for (int j = 0; j <= n_tiles && !*vabort; ++j) {
+        if (j == 1 && valid1) {
           load_q(1);
           q1_loaded = true;
         }
-        const int st = i % NK;
-        if (i >= NK && !mbar_wait(B(B_KE + st), ((i / NK) + 1) & 1, prm.err)) {
+        const int st = j % NS;
+        if (j >= NS && !mbar_wait(B(B_EM + st), ((j / NS) + 1) & 1, prm.err)) {
           abort_flag = 1;
           break;
         }
-        const int key = plane + (tbeg + i) * BN;
-        mbar_arrive_expect_tx(B(B_KF + st), TILE);
-        tma_load_2d(sbase + OFF_K + st * TILE, &tmk, B(B_KF + st), 0, key);
-        tma_load_2d(sbase + OFF_K + st * TILE + HALF, &tmk, B(B_KF + st), 64, key);
+        if (j < n_tiles) {
+          const int key = plane + (tbeg + j) * BN;
+          const uint32_t dst = sbase + OFF_R + st * 2 * TILE;
+          mbar_arrive_expect_tx(B(B_FU + st), TILE);
+          tma_load_2d(dst, &tmk, B(B_FU + st), 0, key);
+          tma_load_2d(dst + HALF, &tmk, B(B_FU + st), 64, key);
+        } else {
+          mbar_arrive(B(B_FU + st));
+        }
         ++issued;
       }
       if (valid1 && !q1_loaded && !*vabort) {
@@ -319,24 +322,30 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       // every issued copy must land before the CTA's shared memory is released
       mbar_wait(B(B_Q + 0), 0, prm.err);
       if (q1_loaded) mbar_wait(B(B_Q + 1), 0, prm.err);
-      for (int i = max(0, issued - NK); i < issued; ++i) mbar_wait(B(B_KF + i % NK), (i / NK) & 1, prm.err);
+      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(B(B_FU + j % NS), (j / NS) & 1, prm.err);
     } else if (warp == 10 && lane == 0) {
       // ---------------------------------------------------------------- TMA producer: V tiles
+      // the V halves of the round slots (slot 0 has none: a bare arrival)
       prefetch_tmap(&tmv);
       int issued = 0;
-      for (int i = 0; i < n_tiles && !*vabort; ++i) {
-        const int st = i % NV;
-        if (i >= NV && !mbar_wait(B(B_VE + st), ((i / NV) + 1) & 1, prm.err)) {
+      for (int j = 0; j <= n_tiles && !*vabort; ++j) {
+        const int st = j % NS;
+        if (j >= NS && !mbar_wait(B(B_EM + st), ((j / NS) + 1) & 1, prm.err)) {
           abort_flag = 1;
           break;
         }
-        const int key = plane + (tbeg + i) * BN;
-        mbar_arrive_expect_tx(B(B_VF + st), TILE);
-        tma_load_2d(sbase + OFF_V + st * TILE, &tmv, B(B_VF + st), 0, key);
-        tma_load_2d(sbase + OFF_V + st * TILE + HALF, &tmv, B(B_VF + st), 64, key);
+        if (j > 0) {
+          const int key = plane + (tbeg + j - 1) * BN;
+          const uint32_t dst = sbase + OFF_R + st * 2 * TILE + TILE;
+          mbar_arrive_expect_tx(B(B_FU + st), TILE);
+          tma_load_2d(dst, &tmv, B(B_FU + st), 0, key);
+          tma_load_2d(dst + HALF, &tmv, B(B_FU + st), 64, key);
+        } else {
+          mbar_arrive(B(B_FU + st));
+        }
         ++issued;
       }
-      for (int i = max(0, issued - NV); i < issued; ++i) mbar_wait(B(B_VF + i % NV), (i / NV) & 1, prm.err);
+      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(B(B_FU + j % NS), (j / NS) & 1, prm.err);
     } else if (warp == 9 && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer (one thread)
       const uint32_t q0s = sbase + OFF_Q, q1s = sbase + OFF_Q + TILE;
@@ -351,37 +360,36 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         }
         return q1_ready;
       };
-      bool ok = mbar_wait(B(B_Q + 0), 0, prm.err) && mbar_wait(B(B_KF), 0, prm.err);
+      bool ok = mbar_wait(B(B_Q + 0), 0, prm.err) && mbar_wait(B(B_FU), 0, prm.err);
       tc_fence_after();
       if (ok) {
         // prologue: scores of the first key tile
         if (act0(tbeg)) {
-          issue_s(s0t, q0s, sbase + OFF_K);
+          issue_s(s0t, q0s, sbase + OFF_R);
           tc_commit(B(B_SF + 0));
         }
         if (act1(tbeg)) {
           ok = wait_q1();
           if (ok) {
-            issue_s(s1t, q1s, sbase + OFF_K);
+            issue_s(s1t, q1s, sbase + OFF_R);
             tc_commit(B(B_SF + 1));
           }
         }
-        tc_commit(B(B_KE + 0));
+        tc_commit(B(B_EM + 0));
       }
-      // Per round (key tile t): PV0(t), S0(t+1), PV1(t), S1(t+1). Each tcgen05.mma blocks the issuing
-      // thread until the tensor core takes it (the queue is short), so any wait between two MMA groups
-      // idles the tensor core. The operand waits (V(t), K(t+1), Q1), normally satisfied long before,
-      // therefore sit at the top of the round, while the previous round's last group still runs; between
-      // groups there are only the P waits. Ring stages and phases advance by counting, not dividing.
-      int kst1 = 1 % NK, kph1 = (1 / NK) & 1;   // K(t+1)
-      int vst = 0, vph = 0;                      // V(t)
+      // Per round (key tile t): PV0(t), S0(t+1), PV1(t), S1(t+1), all reading round slot i + 1 (V(t) and
+      // K(t+1)), which one commit releases at the end. Each tcgen05.mma blocks the issuing thread until the
+      // tensor core takes it (the queue is short), so any wait between two MMA groups idles the tensor
+      // core: the operand waits (the slot, Q1), normally satisfied long before, sit at the top of the
+      // round while the previous round's last group still runs, and between groups there are only the P
+      // waits. The slot's stage and phase advance by counting, not dividing.
+      int st = 1 % NS, ph = (1 / NS) & 1;
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int t = tbeg + i;
         const bool nxt = i + 1 < n_tiles;
-        const uint32_t k1s = sbase + OFF_K + kst1 * TILE;
-        const uint32_t vs = sbase + OFF_V + vst * TILE;
-        if (!mbar_wait(B(B_VF + vst), vph, prm.err) || (nxt && !mbar_wait(B(B_KF + kst1), kph1, prm.err)) ||
-            (nxt && act1(t + 1) && !wait_q1())) {
+        const uint32_t k1s = sbase + OFF_R + st * 2 * TILE;
+        const uint32_t vs = k1s + TILE;
+        if (!mbar_wait(B(B_FU + st), ph, prm.err) || (nxt && act1(t + 1) && !wait_q1())) {
           ok = false;
           break;
         }
@@ -405,21 +413,14 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           issue_pv(o1t, s1t, vs, npv1 > 0);
           ++npv1;
         }
-        tc_commit(B(B_VE + vst));
-        if (nxt) {
-          if (act1(t + 1)) {
-            issue_s(s1t, q1s, k1s);
-            tc_commit(B(B_SF + 1));
-          }
-          tc_commit(B(B_KE + kst1));
+        if (nxt && act1(t + 1)) {
+          issue_s(s1t, q1s, k1s);
+          tc_commit(B(B_SF + 1));
         }
-        if (++kst1 == NK) {
-          kst1 = 0;
-          kph1 ^= 1;
-        }
-        if (++vst == NV) {
-          vst = 0;
-          vph ^= 1;
+        tc_commit(B(B_EM + st));
+        if (++st == NS) {
+          st = 0;
+          ph ^= 1;
         }
       }
       if (!ok) abort_flag = 1;
@@ -529,14 +530,15 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         // V rows past the row's last key hold whatever the cache holds there (maybe NaN); P is 0 there,
         // but 0 * NaN is NaN, so zero those rows before the tensor core reads them (after the V copy has
         // landed; the stage cannot be refilled before this tile's PV, which waits for us).
-        if (!__all_sync(0xffffffffu, mbar_wait(B(B_VF + i % NV), (i / NV) & 1, prm.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(B(B_FU + (i + 1) % NS), ((i + 1) / NS) & 1, prm.err))) {
           abort_flag = 1;
           ok = false;
           break;
         }
         if (kstart + r >= kv_len) {
-          uint4* vrow0 = reinterpret_cast<uint4*>(smem + OFF_V + (i % NV) * TILE + r * 128);
-          uint4* vrow1 = reinterpret_cast<uint4*>(smem + OFF_V + (i % NV) * TILE + HALF + r * 128);
+          uint8_t* vtile = smem + OFF_R + ((i + 1) % NS) * 2 * TILE + TILE;   // V(t), in round slot i + 1
+          uint4* vrow0 = reinterpret_cast<uint4*>(vtile + r * 128);
+          uint4* vrow1 = reinterpret_cast<uint4*>(vtile + HALF + r * 128);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             vrow0[e] = make_uint4(0, 0, 0, 0);
