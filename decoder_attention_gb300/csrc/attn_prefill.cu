@@ -5,25 +5,34 @@
 // families" and "Sliding windows"; soft-capping as "Model resolution" lists it for Gemma 2): for every
 // query row, softmax over its visible keys of scale * q.k (optionally c * tanh(. / c)), times V.
 //
-// CTA = 256 query rows (two 128-row tiles Q0, Q1) of one (sequence, query head). Key tiles of 128 keys
-// stream by TMA (128-byte swizzle) through a 2-stage ring whose stage holds one round's K and V tiles.
-// Roles:
-//   warp 8      TMA producer of Q (once) and K tiles
-//   warp 10     TMA producer of V tiles
+// Persistent: one CTA per SM walks a fixed list of work items. An item is 256 query rows (two 128-row
+// tiles Q0, Q1) of one (sequence, query head); items are numbered with the latest query tiles (the most
+// keys) first and dealt to the CTAs in snake order. The items' key tiles form one sequence that streams
+// by TMA (128-byte swizzle) through a 2-stage ring; a stage holds one round's K and V tiles. Each Q tile's
+// buffer is freed as soon as its last scores are done, so the next item's Q tiles load while the current
+// item finishes; the output leaves through a per-warp staging slot by TMA tensor stores. Roles:
+//   warp 11     item decoder: reads the chunk tables into a small ring of decoded items in shared memory
+//               that every other role walks in the same order
+//   warp 8      TMA producer of Q tiles and of the K halves of the ring
+//   warp 10     TMA producer of the V halves of the ring
 //   warp 9      MMA issuer (one thread): S_w = Q_w K^T into TMEM; O_w += P_w V with P_w read from TMEM
-//   warp 11     idle (completes the third warpgroup, which setmaxnreg works on)
 //   warps 0-3   softmax of Q0 rows, warps 4-7 softmax of Q1 rows: one thread per row; S row from TMEM,
 //               mask only on tiles that need it, online softmax in fp32 (log2 domain; O is rescaled only
-//               when the running max grows by more than 2^8), P written back into TMEM as bf16
-// MMA order per key tile j:  PV0(j), S0(j+1), PV1(j), S1(j+1)  -- so the softmax of one Q tile runs while
-// the tensor core works on the other tile's PV and next S. S0(j+1) overwrites the TMEM columns of P0(j);
-// tcgen05.mma instructions of one thread execute in issue order, so PV0(j) has read P0(j) by then.
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512). Key tiles outside every query's
-// causal window are never loaded (the loop starts at the first tile inside the oldest query's window),
-// so a windowed layer costs O(w) per query. Every mbarrier wait is bounded; a wait that gives up sets
-// the device error word and the CTA drains and exits.
+//               when the running max grows by more than 2^8), P written back into TMEM as bf16. An item's
+//               output O / l leaves during the warpgroup's next item (read from TMEM before its first P
+//               arrival), through the warp's staging slot, so that it is off the MMA chain's critical path
+// MMA order per round (key tile t, next tile u -- the first tile of the next item after an item's last):
+//   PV0(t), S0(u), PV1(t), S1(u)
+// so the softmax of one Q tile runs while the tensor core works on the other tile's PV and next S, and at
+// an item boundary the next item's scores start while the current item's last softmax runs. S_w(u)
+// overwrites the TMEM columns of P_w(t); tcgen05.mma instructions of one thread execute in issue order, so
+// PV_w(t) has read P_w(t) by then. TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512). Key
+// tiles outside every query's causal window are never loaded, so a windowed layer costs O(w) per query.
+// Every wait is bounded; a wait that gives up sets the device error word and the CTA drains and exits.
 #include <cuda_bf16.h>
 #include <math_constants.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -34,11 +43,13 @@ namespace pf {
 constexpr int BM = 128;             // rows per Q tile
 constexpr int BN = 128;             // keys per K/V tile
 constexpr int D = 128;
-constexpr int NQT = 2;              // Q tiles per CTA
-constexpr int NS = 2;               // ring stages; stage of round slot j holds K(tbeg + j) and V(tbeg + j - 1)
-constexpr int THREADS = 384;        // 3 warpgroups: softmax Q0, softmax Q1, producers/MMA
+constexpr int NQT = 2;              // Q tiles per item
+constexpr int NQB = 2;              // Q buffers (each freed by its last scores)
+constexpr int NS = 2;               // ring stages
+constexpr int NI = 8;               // decoded-item ring entries
+constexpr int THREADS = 384;        // 3 warpgroups: softmax Q0, softmax Q1, decoder/producers/MMA
 // setmaxnreg split: launched at 168 per thread (384 x 168 = 64512); softmax warpgroups rise to 216 and
-// the producer/MMA warpgroup drops to 72: 256 x 216 + 128 x 72 = 64512, the launch total (per SMSP, one
+// the control warpgroup drops to 72: 256 x 216 + 128 x 72 = 64512, the launch total (per SMSP, one
 // warp of each warpgroup: 216 + 216 + 72 = 504 of 512 registers per lane).
 #ifndef DA_PF_REGS_SOFTMAX
 #define DA_PF_REGS_SOFTMAX 216
@@ -50,17 +61,24 @@ static_assert(256 * REGS_SOFTMAX + 128 * REGS_CTRL == 384 * 168, "register split
 constexpr int HALF = 128 * 128;     // bytes of a 64-wide half of a 128-row tile (16 KB)
 constexpr int TILE = 2 * HALF;      // 32 KB
 constexpr int OFF_Q = 0;
-constexpr int OFF_R = OFF_Q + NQT * TILE;   // ring: stage s = K tile at OFF_R + 2s TILE, V tile after it
-constexpr int OFF_BAR = OFF_R + NS * 2 * TILE;
-// barriers: q[NQT], full[NS] (two arrivals: K producer, V producer), empty[NS], s_full[NQT], p_full[NQT],
-// o_done[NQT]
-constexpr int B_Q = 0, B_FU = B_Q + NQT, B_EM = B_FU + NS, B_SF = B_EM + NS,
-              B_PF = B_SF + NQT, B_OD = B_PF + NQT, N_BARS = B_OD + NQT;
-constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + TMEM address slot + alignment slack
+constexpr int OFF_R = OFF_Q + NQB * TILE;   // ring: stage s = K tile at OFF_R + 2s TILE, V tile after it
+constexpr int OFF_E = OFF_R + NS * 2 * TILE;  // output staging: 4 KB (16 rows) per softmax warp
+constexpr int STG = 16 * 2 * 128;
+constexpr int OFF_BAR = OFF_E + 8 * STG;
+// barriers: q_full[NQB], q_empty[NQB], full[NS] (two arrivals: K producer, V producer), empty[NS],
+// s_full[NQT], p_full[NQT], o_done[NQT], item_full[NI], item_empty[NI], drain
+constexpr int B_QF = 0, B_QE = B_QF + NQB, B_FU = B_QE + NQB, B_EM = B_FU + NS, B_SF = B_EM + NS,
+              B_PF = B_SF + NQT, B_OD = B_PF + NQT, B_IF = B_OD + NQT, B_IE = B_IF + NI, B_DR = B_IE + NI,
+              N_BARS = B_DR + 1;
+constexpr int OFF_ITEMS = (OFF_BAR + N_BARS * 8 + 15) / 16 * 16;
+constexpr int OFF_SLOT = OFF_ITEMS + NI * 32;
+constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;   // + TMEM address slot + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: stale max allowed to lag by up to x256
+// readers of every item-ring entry: the two producers, the MMA issuer, the 256 softmax threads
+constexpr int kItemReaders = 3 + 256;
 
 struct Params {
   const int32_t* q_start;
@@ -68,9 +86,51 @@ struct Params {
   const int32_t* first_pos;
   __nv_bfloat16* out;
   int hq, hkv, max_len, num_rows, window;
+  int n_seqs, n_qt, n_items;
   float softcap, scale;
   int* err;
 };
+
+// A decoded work item as the ring holds it.
+struct Item {
+  int t0;      // first token of the chunk
+  int n_b;     // chunk length
+  int q0;      // first chunk row of the item
+  int fp;      // position of the chunk's first token
+  int plane;   // cache row index of (row, kv head, position 0)
+  int h;       // query head
+  int kind;    // kEnd, kLive, kBad
+  int round0;  // global round of the item's first key tile (rounds count the CTA's key tiles in order)
+};
+constexpr int kEnd = 0, kLive = 1, kBad = 2;
+
+// Key-tile ranges of an item's two Q tiles: each from the tile holding its oldest query's first visible
+// key to the tile holding its newest query's own key. Q0's range starts and ends no later than Q1's, and
+// together they cover tb0 .. max(te0, te1) without a gap.
+struct Tiles {
+  bool valid1;             // Q1 has rows
+  int pmin0, pmax0, pmin1, pmax1;
+  int tb0, te0, tb1, te1;  // tile ranges (te1 < tb1 when Q1 has no rows)
+  int n;                   // tiles tb0 .. max(te0, te1)
+};
+__device__ __forceinline__ Tiles tiles_of(const Item& it, int window) {
+  Tiles T;
+  T.valid1 = it.q0 + BM < it.n_b;
+  const int nr0 = min(BM, it.n_b - it.q0);
+  T.pmin0 = it.fp + it.q0;
+  T.pmax0 = T.pmin0 + nr0 - 1;
+  T.pmin1 = T.pmin0 + BM;
+  T.pmax1 = T.valid1 ? it.fp + min(it.q0 + 2 * BM, it.n_b) - 1 : T.pmin1;
+  T.tb0 = (window > 0 ? max(0, T.pmin0 - window + 1) : 0) / BN;
+  T.te0 = T.pmax0 / BN;
+  T.tb1 = (window > 0 ? max(0, T.pmin1 - window + 1) : 0) / BN;
+  T.te1 = T.valid1 ? T.pmax1 / BN : T.tb1 - 1;
+  T.n = (T.valid1 ? T.te1 : T.te0) - T.tb0 + 1;
+  return T;
+}
+
+// Item of round r for CTA c of G: snake order over the heaviest-first numbering.
+__device__ __forceinline__ int item_of(int r, int c, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -191,6 +251,14 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
       : "memory");
 }
 
+
+// What the MMA issuer keeps of an item: tile ranges and the Q sequence numbers of its tiles.
+struct IssItem {
+  bool live;
+  int tb0, te0, tb1, te1, tend;
+  int q0, q1;   // Q tile sequence numbers (buffer = q % NQB)
+};
+
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmq,
                                                              const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
@@ -201,68 +269,20 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x % prm.hq;
-  const int s = blockIdx.x / prm.hq;
-  const int qt = gridDim.y - 1 - blockIdx.y;      // the longest (latest) query tiles are scheduled first
-  const int t0 = prm.q_start[s];
-  const int n_b = prm.q_start[s + 1] - t0;
-  const int q0 = qt * (NQT * BM);
-  if (q0 >= n_b) return;
-  const int row = prm.rows[s];
-  const int fp = prm.first_pos[s];
-  const int kv_len = fp + n_b;
-  if (row < 0 || row >= prm.num_rows || fp < 0 || kv_len > prm.max_len) {
-    if (threadIdx.x == 0) set_error(prm.err, kErrIndex);
-    for (int r = threadIdx.x; r < min(NQT * BM, n_b - q0); r += blockDim.x) {
-      uint4* o = reinterpret_cast<uint4*>(prm.out + (static_cast<long long>(t0 + q0 + r) * prm.hq + h) * D);
-      for (int j = 0; j < D / 8; ++j) o[j] = make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
-  const int g = h / (prm.hq / prm.hkv);
+  const int cta = blockIdx.x, G = gridDim.x;
   const int window = prm.window;
-
-  // Key-tile range of each Q tile: from the tile holding the oldest query's first visible key to the tile
-  // holding the newest query's own key. Q0's range starts no later and ends no later than Q1's.
-  bool valid0, valid1;
-  int pmin0, pmax0, pmin1, pmax1, tb0, te0, tb1, te1;
-  {
-    auto range = [&](int w, bool& valid, int& pmin, int& pmax, int& tb, int& te) {
-      const int r0 = q0 + w * BM;
-      valid = r0 < n_b;
-      const int nr = valid ? min(BM, n_b - r0) : 1;
-      pmin = fp + r0;
-      pmax = fp + r0 + nr - 1;
-      const int lo = window > 0 ? max(0, pmin - window + 1) : 0;
-      tb = lo / BN;
-      te = pmax / BN;
-    };
-    range(0, valid0, pmin0, pmax0, tb0, te0);
-    range(1, valid1, pmin1, pmax1, tb1, te1);
-  }
-  const int tbeg = tb0;
-  const int tend = valid1 ? te1 : te0;
-  const int n_tiles = tend - tbeg + 1;
-  auto act0 = [&](int t) { return t >= tb0 && t <= te0; };
-  auto act1 = [&](int t) { return valid1 && t >= tb1 && t <= te1; };
-
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar = sbase + OFF_BAR;
   auto B = [&](int i) { return bar + 8u * i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + N_BARS * 8);
+  Item* ring = reinterpret_cast<Item*>(smem + OFF_ITEMS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(B(B_FU + i), 2);
-      mbar_init(B(B_EM + i), 1);
-    }
-    for (int w = 0; w < NQT; ++w) {
-      mbar_init(B(B_SF + w), 1);
-      mbar_init(B(B_PF + w), BM);
-      mbar_init(B(B_OD + w), 1);
-      mbar_init(B(B_Q + w), 1);
-    }
+    for (int i = 0; i < N_BARS; ++i) mbar_init(B(i), 1);
+    for (int i = 0; i < NS; ++i) mbar_init(B(B_FU + i), 2);
+    for (int w = 0; w < NQT; ++w) mbar_init(B(B_PF + w), BM);
+    for (int i = 0; i < NI; ++i) mbar_init(B(B_IE + i), kItemReaders);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -274,38 +294,85 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const volatile int* vabort = &abort_flag;
-  const int plane = (row * prm.hkv + g) * prm.max_len;
+
+  // item-ring reader (one thread): waits for entry e, copies it, releases it
+  auto get_item = [&](int e, Item& it) -> bool {
+    const int slot = e % NI;
+    if (!mbar_wait(B(B_IF + slot), (e / NI) & 1, prm.err)) return false;
+    it = ring[slot];
+    mbar_arrive(B(B_IE + slot));
+    return true;
+  };
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
-    if (warp == 8 && lane == 0) {
-      // ---------------------------------------------------------------- TMA producer: Q and K tiles
-      // Round slot j (one ring stage) holds K(tbeg + j) and V(tbeg + j - 1): the K tile the round's scores
-      // need and the V tile its PVs need. This producer fills the K halves (slot n_tiles has none: a bare
-      // arrival). Q0 and the first K tile go first; Q1 queues behind them.
+    if (warp == 11 && lane == 0) {
+      // ---------------------------------------------------------------- item decoder
+      const int per_round = prm.n_seqs * prm.hq;
+      int e = 0, rounds = 0;
+      bool ok = true;
+      auto released = [&](int k) {   // wait until every reader has released entry k
+        return mbar_wait(B(B_IE + k % NI), (k / NI) & 1, prm.err);
+      };
+      auto put = [&](const Item& it) -> bool {
+        const int slot = e % NI;
+        if (e >= NI && !released(e - NI)) return false;
+        ring[slot] = it;
+        mbar_arrive(B(B_IF + slot));   // release: the entry's stores are visible to the acquiring readers
+        ++e;
+        return true;
+      };
+      for (int r = 0; ok && r * G < prm.n_items && !*vabort; ++r) {
+        const int id = item_of(r, cta, G);
+        if (id >= prm.n_items) continue;
+        const int y = id / per_round, x = id - y * per_round;
+        const int s = x / prm.hq, h = x - s * prm.hq;
+        Item it;
+        it.t0 = prm.q_start[s];
+        it.n_b = prm.q_start[s + 1] - it.t0;
+        it.q0 = (prm.n_qt - 1 - y) * (NQT * BM);
+        if (it.q0 >= it.n_b) continue;           // this chunk has no rows that far
+        const int row = prm.rows[s];
+        it.fp = prm.first_pos[s];
+        it.h = h;
+        const bool bad = row < 0 || row >= prm.num_rows || it.fp < 0 || it.fp + it.n_b > prm.max_len;
+        it.kind = bad ? kBad : kLive;
+        it.plane = bad ? 0 : (row * prm.hkv + h / (prm.hq / prm.hkv)) * prm.max_len;
+        it.round0 = rounds;
+        if (!bad) rounds += tiles_of(it, window).n;
+        ok = put(it);
+      }
+      if (ok) {
+        Item end;
+        end.kind = kEnd;
+        end.t0 = end.n_b = end.q0 = end.fp = end.plane = end.h = 0;
+        end.round0 = rounds;
+        ok = put(end);
+      }
+      if (!ok) abort_flag = 1;
+    } else if (warp == 8 && lane == 0) {
+      // ---------------------------------------------------------------- TMA producer: Q tiles, K halves
+      // Ring slot j holds the K tile of global round j (the tile the scores issued in round j - 1 use) and
+      // the V tile of round j - 1; this producer fills the K halves (the last slot has none: a bare
+      // arrival). Per item: Q0, the first K tile, Q1, the remaining K tiles.
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
-      auto load_q = [&](int w) {
-        const int tok = t0 + q0 + w * BM;
-        mbar_arrive_expect_tx(B(B_Q + w), TILE);
-        tma_load_3d(sbase + OFF_Q + w * TILE, &tmq, B(B_Q + w), 0, h, tok);
-        tma_load_3d(sbase + OFF_Q + w * TILE + HALF, &tmq, B(B_Q + w), 64, h, tok);
+      int qn = 0, kj = 0;   // Q tiles loaded, ring slots filled
+      bool ok = true;
+      auto load_q = [&](const Item& it, int w) -> bool {
+        const int b = qn % NQB, u = qn / NQB;
+        if (u > 0 && !mbar_wait(B(B_QE + b), (u - 1) & 1, prm.err)) return false;
+        const int tok = it.t0 + it.q0 + w * BM;
+        mbar_arrive_expect_tx(B(B_QF + b), TILE);
+        tma_load_3d(sbase + OFF_Q + b * TILE, &tmq, B(B_QF + b), 0, it.h, tok);
+        tma_load_3d(sbase + OFF_Q + b * TILE + HALF, &tmq, B(B_QF + b), 64, it.h, tok);
+        ++qn;
+        return true;
       };
-      load_q(0);
-      bool q1_loaded = false;
-      int issued = 0;
-      for (int j = 0; j <= n_tiles && !*vabort; ++j) {
-        if (j == 1 && valid1) {
-          load_q(1);
-          q1_loaded = true;
-        }
-        const int st = j % NS;
-        if (j >= NS && !mbar_wait(B(B_EM + st), ((j / NS) + 1) & 1, prm.err)) {
-          abort_flag = 1;
-          break;
-        }
-        if (j < n_tiles) {
-          const int key = plane + (tbeg + j) * BN;
+      auto fill_k = [&](int key) -> bool {   // key < 0: the slot has no K tile
+        const int st = kj % NS;
+        if (kj >= NS && !mbar_wait(B(B_EM + st), ((kj / NS) - 1) & 1, prm.err)) return false;
+        if (key >= 0) {
           const uint32_t dst = sbase + OFF_R + st * 2 * TILE;
           mbar_arrive_expect_tx(B(B_FU + st), TILE);
           tma_load_2d(dst, &tmk, B(B_FU + st), 0, key);
@@ -313,29 +380,36 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         } else {
           mbar_arrive(B(B_FU + st));
         }
-        ++issued;
-      }
-      if (valid1 && !q1_loaded && !*vabort) {
-        load_q(1);
-        q1_loaded = true;
-      }
-      // every issued copy must land before the CTA's shared memory is released
-      mbar_wait(B(B_Q + 0), 0, prm.err);
-      if (q1_loaded) mbar_wait(B(B_Q + 1), 0, prm.err);
-      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(B(B_FU + j % NS), (j / NS) & 1, prm.err);
-    } else if (warp == 10 && lane == 0) {
-      // ---------------------------------------------------------------- TMA producer: V tiles
-      // the V halves of the round slots (slot 0 has none: a bare arrival)
-      prefetch_tmap(&tmv);
-      int issued = 0;
-      for (int j = 0; j <= n_tiles && !*vabort; ++j) {
-        const int st = j % NS;
-        if (j >= NS && !mbar_wait(B(B_EM + st), ((j / NS) + 1) & 1, prm.err)) {
-          abort_flag = 1;
-          break;
+        ++kj;
+        return true;
+      };
+      for (int e = 0; ok; ++e) {
+        Item it;
+        if (!get_item(e, it)) { ok = false; break; }
+        if (it.kind == kEnd) break;
+        if (it.kind != kLive) continue;
+        const Tiles T = tiles_of(it, window);
+        if (!load_q(it, 0)) { ok = false; break; }
+        for (int i = 0; ok && i < T.n; ++i) {
+          if (*vabort || (i == 1 && T.valid1 && !load_q(it, 1)) || !fill_k(it.plane + (T.tb0 + i) * BN)) ok = false;
         }
-        if (j > 0) {
-          const int key = plane + (tbeg + j - 1) * BN;
+        if (ok && T.n == 1 && T.valid1 && !load_q(it, 1)) ok = false;
+      }
+      if (ok && !fill_k(-1)) ok = false;
+      if (!ok) abort_flag = 1;
+      // every issued copy must land before the CTA's shared memory is released
+      for (int j = max(0, qn - NQB); j < qn; ++j) mbar_wait(B(B_QF + j % NQB), (j / NQB) & 1, prm.err);
+      for (int j = max(0, kj - NS); j < kj; ++j) mbar_wait(B(B_FU + j % NS), (j / NS) & 1, prm.err);
+    } else if (warp == 10 && lane == 0) {
+      // ---------------------------------------------------------------- TMA producer: V halves
+      // slot 0 has no V tile (a bare arrival); slot j > 0 holds the V tile of global round j - 1
+      prefetch_tmap(&tmv);
+      int vj = 0;
+      bool ok = true;
+      auto fill_v = [&](int key) -> bool {
+        const int st = vj % NS;
+        if (vj >= NS && !mbar_wait(B(B_EM + st), ((vj / NS) - 1) & 1, prm.err)) return false;
+        if (key >= 0) {
           const uint32_t dst = sbase + OFF_R + st * 2 * TILE + TILE;
           mbar_arrive_expect_tx(B(B_FU + st), TILE);
           tma_load_2d(dst, &tmv, B(B_FU + st), 0, key);
@@ -343,90 +417,176 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         } else {
           mbar_arrive(B(B_FU + st));
         }
-        ++issued;
-      }
-      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(B(B_FU + j % NS), (j / NS) & 1, prm.err);
-    } else if (warp == 9 && lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer (one thread)
-      const uint32_t q0s = sbase + OFF_Q, q1s = sbase + OFF_Q + TILE;
-      const uint32_t s0t = tmem, s1t = tmem + BN, o0t = tmem + 256, o1t = tmem + 256 + D;
-      int npv0 = 0, npv1 = 0;
-      bool od0 = false;
-      bool q1_ready = false;
-      auto wait_q1 = [&]() {          // Q1 lands after the first K tile; waited on before its first scores
-        if (!q1_ready) {
-          q1_ready = mbar_wait(B(B_Q + 1), 0, prm.err);
-          tc_fence_after();
-        }
-        return q1_ready;
+        ++vj;
+        return true;
       };
-      bool ok = mbar_wait(B(B_Q + 0), 0, prm.err) && mbar_wait(B(B_FU), 0, prm.err);
-      tc_fence_after();
-      if (ok) {
-        // prologue: scores of the first key tile
-        if (act0(tbeg)) {
-          issue_s(s0t, q0s, sbase + OFF_R);
-          tc_commit(B(B_SF + 0));
-        }
-        if (act1(tbeg)) {
-          ok = wait_q1();
-          if (ok) {
-            issue_s(s1t, q1s, sbase + OFF_R);
-            tc_commit(B(B_SF + 1));
-          }
-        }
-        tc_commit(B(B_EM + 0));
-      }
-      // Per round (key tile t): PV0(t), S0(t+1), PV1(t), S1(t+1), all reading round slot i + 1 (V(t) and
-      // K(t+1)), which one commit releases at the end. Each tcgen05.mma blocks the issuing thread until the
-      // tensor core takes it (the queue is short), so any wait between two MMA groups idles the tensor
-      // core: the operand waits (the slot, Q1), normally satisfied long before, sit at the top of the
-      // round while the previous round's last group still runs, and between groups there are only the P
-      // waits. The slot's stage and phase advance by counting, not dividing.
-      int st = 1 % NS, ph = (1 / NS) & 1;
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int t = tbeg + i;
-        const bool nxt = i + 1 < n_tiles;
-        const uint32_t k1s = sbase + OFF_R + st * 2 * TILE;
-        const uint32_t vs = k1s + TILE;
-        if (!mbar_wait(B(B_FU + st), ph, prm.err) || (nxt && act1(t + 1) && !wait_q1())) {
-          ok = false;
-          break;
-        }
-        if (act0(t)) {
-          if (!mbar_wait(B(B_PF + 0), npv0 & 1, prm.err)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(o0t, s0t, vs, npv0 > 0);
-          ++npv0;
-          if (t == te0) {
-            tc_commit(B(B_OD + 0));     // Q0's output is final: its epilogue overlaps Q1's last tiles
-            od0 = true;
-          }
-        }
-        if (nxt && act0(t + 1)) {
-          issue_s(s0t, q0s, k1s);
-          tc_commit(B(B_SF + 0));
-        }
-        if (act1(t)) {
-          if (!mbar_wait(B(B_PF + 1), npv1 & 1, prm.err)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(o1t, s1t, vs, npv1 > 0);
-          ++npv1;
-        }
-        if (nxt && act1(t + 1)) {
-          issue_s(s1t, q1s, k1s);
-          tc_commit(B(B_SF + 1));
-        }
-        tc_commit(B(B_EM + st));
-        if (++st == NS) {
-          st = 0;
-          ph ^= 1;
+      ok = fill_v(-1);
+      for (int e = 0; ok; ++e) {
+        Item it;
+        if (!get_item(e, it)) { ok = false; break; }
+        if (it.kind == kEnd) break;
+        if (it.kind != kLive) continue;
+        const Tiles T = tiles_of(it, window);
+        for (int i = 0; ok && i < T.n; ++i) {
+          if (*vabort || !fill_v(it.plane + (T.tb0 + i) * BN)) ok = false;
         }
       }
       if (!ok) abort_flag = 1;
-      if (!od0) tc_commit(B(B_OD + 0));
-      tc_commit(B(B_OD + 1));
-      mbar_wait(B(B_OD + 1), 0, prm.err);   // all MMAs done before TMEM may be released
+      for (int j = max(0, vj - NS); j < vj; ++j) mbar_wait(B(B_FU + j % NS), (j / NS) & 1, prm.err);
+    } else if (warp == 9 && lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer (one thread)
+      // Rounds run over all items' key tiles in order. Round (tile t of item A, next tile u: t + 1, or the
+      // first tile of the next item B after A's last) reads ring slot g + 1 (V(t), K(u)):
+      //   PV0(t), S0(u), PV1(t), S1(u), release of the slot.
+      // Each tcgen05.mma blocks the issuing thread until the tensor core takes it (the queue is short),
+      // so every wait between two MMA groups idles the tensor core: the operand waits (the slot, a Q tile)
+      // sit at the top of the round, and between groups there are only the P waits. A Q buffer is
+      // released by a commit after the last scores that read it.
+      int qseq = 0, e = 0;
+      bool ok = true, ended = false;   // ended: the end-of-list entry has been read
+      auto next_live = [&](IssItem& I) {
+        I.live = false;
+        while (ok && !ended) {
+          Item it;
+          if (!get_item(e, it)) { ok = false; return; }
+          ++e;
+          if (it.kind == kEnd) {
+            ended = true;
+            return;
+          }
+          if (it.kind != kLive) continue;
+          const Tiles T = tiles_of(it, window);
+          I.live = true;
+          I.tb0 = T.tb0;
+          I.te0 = T.te0;
+          I.tb1 = T.tb1;
+          I.te1 = T.te1;
+          I.tend = T.tb0 + T.n - 1;
+          I.q0 = qseq;
+          I.q1 = qseq + 1;
+          qseq += T.valid1 ? 2 : 1;
+          return;
+        }
+      };
+      auto qready = [&](int q) { return mbar_wait(B(B_QF + q % NQB), (q / NQB) & 1, prm.err); };
+      auto qsmem = [&](int q) { return sbase + OFF_Q + (q % NQB) * TILE; };
+      IssItem A, Bn;
+      next_live(A);
+      next_live(Bn);
+      int st = 0, ph = 0;        // ring slot of the next round: stage, phase
+      int npv0 = 0, npv1 = 0;    // PVs issued per stream (phase of p_full)
+      bool a_q1 = false, b_q1 = false;   // Q1 of A / of B waited on
+      if (ok && A.live) {
+        // scores of A's first tile, from ring slot 0
+        ok = mbar_wait(B(B_FU), 0, prm.err) && qready(A.q0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(tmem, qsmem(A.q0), sbase + OFF_R);
+          tc_commit(B(B_SF + 0));
+          if (A.te0 == A.tb0) tc_commit(B(B_QE + A.q0 % NQB));
+          if (A.tb1 <= A.tb0 && A.tb0 <= A.te1) {
+            ok = qready(A.q1);
+            a_q1 = true;
+            if (ok) {
+              issue_s(tmem + BN, qsmem(A.q1), sbase + OFF_R);
+              tc_commit(B(B_SF + 1));
+              if (A.te1 == A.tb0) tc_commit(B(B_QE + A.q1 % NQB));
+            }
+          }
+          tc_commit(B(B_EM + 0));
+          st = 1 % NS;
+          ph = (1 / NS) & 1;
+        }
+      }
+      while (ok && A.live) {
+        bool first0 = true, first1 = true;
+        const uint32_t q0s = qsmem(A.q0), q1s = qsmem(A.q1);
+        // PVs of tile t (the P waits are the only waits between MMA groups)
+        auto pv0 = [&](int t, uint32_t vs) -> bool {
+          if (!mbar_wait(B(B_PF + 0), npv0 & 1, prm.err)) return false;
+          tc_fence_after();
+          issue_pv(tmem + 256, tmem, vs, !first0);
+          first0 = false;
+          ++npv0;
+          if (t == A.te0) tc_commit(B(B_OD + 0));   // Q0's output is final
+          return true;
+        };
+        auto pv1 = [&](int t, uint32_t vs) -> bool {
+          if (!mbar_wait(B(B_PF + 1), npv1 & 1, prm.err)) return false;
+          tc_fence_after();
+          issue_pv(tmem + 256 + D, tmem + BN, vs, !first1);
+          first1 = false;
+          ++npv1;
+          if (t == A.te1) tc_commit(B(B_OD + 1));   // Q1's output is final
+          return true;
+        };
+        // rounds inside the item: the next tile u = t + 1 is the item's own
+        for (int t = A.tb0; ok && t < A.tend; ++t) {
+          const int u = t + 1;
+          const bool s0u = u <= A.te0, s1u = A.tb1 <= u && u <= A.te1;
+          const uint32_t ks = sbase + OFF_R + st * 2 * TILE, vs = ks + TILE;
+          if (!mbar_wait(B(B_FU + st), ph, prm.err)) { ok = false; break; }
+          if (s1u && !a_q1) {
+            if (!qready(A.q1)) { ok = false; break; }
+            a_q1 = true;
+          }
+          if (t <= A.te0 && !pv0(t, vs)) { ok = false; break; }
+          if (s0u) {
+            issue_s(tmem, q0s, ks);
+            tc_commit(B(B_SF + 0));
+            if (u == A.te0) tc_commit(B(B_QE + A.q0 % NQB));
+          }
+          if (t >= A.tb1 && t <= A.te1 && !pv1(t, vs)) { ok = false; break; }
+          if (s1u) {
+            issue_s(tmem + BN, q1s, ks);
+            tc_commit(B(B_SF + 1));
+            if (u == A.te1) tc_commit(B(B_QE + A.q1 % NQB));
+          }
+          tc_commit(B(B_EM + st));
+          if (++st == NS) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        {
+          // the item's last round: the next tile is the first of the next item (its Q tiles waited here)
+          const int t = A.tend, u = Bn.tb0;
+          const bool s0u = Bn.live, s1u = Bn.live && Bn.tb1 <= u && u <= Bn.te1;
+          const uint32_t ks = sbase + OFF_R + st * 2 * TILE, vs = ks + TILE;
+          if (*vabort || !mbar_wait(B(B_FU + st), ph, prm.err) || (s0u && !qready(Bn.q0))) {
+            ok = false;
+            break;
+          }
+          b_q1 = s1u;
+          if (t <= A.te0 && !pv0(t, vs)) { ok = false; break; }
+          if (s0u) {
+            issue_s(tmem, qsmem(Bn.q0), ks);
+            tc_commit(B(B_SF + 0));
+            if (u == Bn.te0) tc_commit(B(B_QE + Bn.q0 % NQB));
+          }
+          if (t >= A.tb1 && t <= A.te1 && !pv1(t, vs)) { ok = false; break; }
+          if (s1u) {
+            // Bn's Q1 reuses A's Q1 buffer, freed by the S1 issued in the round before: waited on last
+            if (!qready(Bn.q1)) { ok = false; break; }
+            issue_s(tmem + BN, qsmem(Bn.q1), ks);
+            tc_commit(B(B_SF + 1));
+            if (u == Bn.te1) tc_commit(B(B_QE + Bn.q1 % NQB));
+          }
+          tc_commit(B(B_EM + st));
+          if (++st == NS) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        A = Bn;
+        a_q1 = b_q1;
+        b_q1 = false;
+        next_live(Bn);
+      }
+      if (!ok) abort_flag = 1;
+      tc_commit(B(B_DR));
+      mbar_wait(B(B_DR), 0, prm.err);   // all MMAs done before TMEM may be released
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));
@@ -434,9 +594,6 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const int w = warp >> 2;             // which Q tile
     const int wi = warp & 3;             // TMEM lane quarter
     const int r = wi * 32 + lane;        // row within the tile
-    const int qrow = q0 + w * BM + r;    // row within the chunk
-    const bool row_ok = qrow < n_b;
-    const int p = fp + qrow;
     const uint32_t lane_addr = static_cast<uint32_t>(wi * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + w * BN;
     const uint32_t t_o = tmem + lane_addr + 256 + w * D;
@@ -444,158 +601,241 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const float cap_in = cap > 0.f ? prm.scale / cap : 0.f;
     const float cap_l2 = cap * kLog2e;
     const float zmul = cap > 0.f ? 1.f : prm.scale * kLog2e;   // z * zmul is the logit in log2 units
-    const bool my_valid = w == 0 ? true : valid1;
-    const int my_tb = w == 0 ? tb0 : tb1;
-    const int my_te = w == 0 ? te0 : te1;
-    const int my_pmin = w == 0 ? pmin0 : pmin1;
-    const int my_pmax = w == 0 ? pmax0 : pmax1;
-    float m = -CUDART_INF_F, l = 0.f;
-    int nact = 0;
+    int ns = 0, nod = 0;
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int t = tbeg + i;
-      if (!my_valid || t < my_tb || t > my_te) continue;
-      // outcomes are made warp-uniform: the TMEM loads and stores below are warp-collective
-      if (__any_sync(0xffffffffu, *vabort != 0)) { ok = false; break; }
-      if (!__all_sync(0xffffffffu, mbar_wait(B(B_SF + w), nact & 1, prm.err))) {
-        abort_flag = 1;
-        ok = false;
-        break;
-      }
+    // The epilogue of an item (O / l out through the warp's staging slot) is deferred into the first tile
+    // of this warpgroup's next item: that tile's softmax runs first (it does not touch O), then O is read
+    // from TMEM just before the P arrival that lets the next PV overwrite it, and the stores go out while
+    // the tensor core runs that PV. The finished item's ring entry is held until then; its fields are read
+    // back from shared memory.
+    bool pend = false;      // an epilogue is pending
+    int pend_slot = 0;      // its item's ring entry
+    float pend_inv_l = 0.f; // its row's 1 / l
+    // O / l of the pending item -> pw (bf16 pairs)
+    auto epi_read = [&](uint32_t (&pw)[D / 2]) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(B(B_OD + w), nod & 1, prm.err))) return false;
+      ++nod;
       tc_fence_after();
-      uint32_t zr[BN];
-#pragma unroll
-      tmem_ld128(t_s, zr);
-      tmem_wait_ld();
-      const int kstart = t * BN;
-      const bool need_mask = !(kstart + BN - 1 <= my_pmin &&
-                               (window == 0 || my_pmax - kstart <= window - 1) && kstart + BN <= kv_len);
-      // zr: the raw score q.k (scaled into log2 units inside the exponent), or for capped layers the
-      // capped logit already in log2 units. Visible keys of this row in the tile: columns [lo_c, hi_c].
-      const int hi_c = min(p, kv_len - 1) - kstart;
-      const int lo_c = window > 0 ? p - window + 1 - kstart : -BN;
-      float tmax;
-      if (cap > 0.f) {
-        tmax = need_mask ? row_pass<true, true>(zr, cap_in, cap_l2, lo_c, hi_c)
-                         : row_pass<true, false>(zr, cap_in, cap_l2, lo_c, hi_c);
-      } else {
-        tmax = need_mask ? row_pass<false, true>(zr, cap_in, cap_l2, lo_c, hi_c)
-                         : row_pass<false, false>(zr, cap_in, cap_l2, lo_c, hi_c);
-      }
-      tmax *= zmul;
-      const float m_new = fmaxf(m, tmax);
-      const bool grow = m_new > m + kRescaleThreshold;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = ex2(m - m_new);   // 0 when m was -inf
-        l *= alpha;
-        m = m_new;
-      }
-      if (nact > 0 && __any_sync(0xffffffffu, grow)) {
-        // O row *= alpha (rows that did not grow multiply by 1). PV of the previous tile has completed:
-        // its commit preceded the S commit just waited on.
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
-          uint32_t ov[32];
-          tmem_ld32(t_o + j * 32, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32(t_o + j * 32, ov);
-        }
-      }
-      const float nmu = (m == -CUDART_INF_F) ? 0.f : -m;
-      // p = 2^(z * zmul - m) two scores at a time (packed fp32 pairs), row sum in 4 packed accumulators
-      const uint64_t zmul2 = f2_pack(zmul, zmul), nmu2 = f2_pack(nmu, nmu);
-      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int e = 0; e < BN / 2; ++e) {
-        float xa, xb;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(zr[2 * e]), __uint_as_float(zr[2 * e + 1])), zmul2, nmu2), xa, xb);
-        const float pa = ex2(xa), pb = ex2(xb);
-        ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(pa, pb));
-        pk[e] = pack_bf16(pa, pb);
-      }
-      tmem_st64(t_s, pk);     // P (bf16, 2 per column) over the first half of the S columns
-      {
-        float a0, a1, b0, b1, c0, c1, d0, d1;
-        f2_unpack(f2_add(ls2[0], ls2[1]), a0, a1);
-        f2_unpack(f2_add(ls2[2], ls2[3]), b0, b1);
-        (void)c0; (void)c1; (void)d0; (void)d1;
-        l += (a0 + a1) + (b0 + b1);
-      }
-      tmem_wait_st();
-      if (kstart + BN > kv_len) {
-        // V rows past the row's last key hold whatever the cache holds there (maybe NaN); P is 0 there,
-        // but 0 * NaN is NaN, so zero those rows before the tensor core reads them (after the V copy has
-        // landed; the stage cannot be refilled before this tile's PV, which waits for us).
-        if (!__all_sync(0xffffffffu, mbar_wait(B(B_FU + (i + 1) % NS), ((i + 1) / NS) & 1, prm.err))) {
-          abort_flag = 1;
-          ok = false;
-          break;
-        }
-        if (kstart + r >= kv_len) {
-          uint8_t* vtile = smem + OFF_R + ((i + 1) % NS) * 2 * TILE + TILE;   // V(t), in round slot i + 1
-          uint4* vrow0 = reinterpret_cast<uint4*>(vtile + r * 128);
-          uint4* vrow1 = reinterpret_cast<uint4*>(vtile + HALF + r * 128);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            vrow0[e] = make_uint4(0, 0, 0, 0);
-            vrow1[e] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(B(B_PF + w));
-      ++nact;
-    }
-    // ------------------------------------------------------------ epilogue: O / l -> out
-    // Each warp normalises its 32 rows into the Q tile's shared memory (free once every MMA is done) in the
-    // 128-byte-swizzled layout and writes them with two TMA tensor stores; a warp whose rows run past the
-    // chunk stores row by row instead (a whole box would overwrite the next sequence's rows).
-    if (ok && __all_sync(0xffffffffu, mbar_wait(B(B_OD + w), 0, prm.err))) {
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool full_tile = q0 + w * BM + wi * 32 + 32 <= n_b;   // warp-uniform
-      uint4* orow = reinterpret_cast<uint4*>(prm.out + (static_cast<long long>(t0 + qrow) * prm.hq + h) * D);
-      uint8_t* srow = smem + OFF_Q + w * TILE + r * 128;
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         uint32_t ov[32];
         tmem_ld32(t_o + j * 32, ov);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint4 u;
-          u.x = pack_bf16(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
-          u.y = pack_bf16(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
-          u.z = pack_bf16(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
-          u.w = pack_bf16(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
-          const int c16 = j * 4 + e;                 // 16-byte chunk of the row, 0..15
-          if (full_tile) {
-            *reinterpret_cast<uint4*>(srow + (c16 >> 3) * HALF + (((c16 & 7) ^ (r & 7)) << 4)) = u;
-          } else if (row_ok) {
-            orow[c16] = u;
+        for (int c = 0; c < 16; ++c)
+          pw[j * 16 + c] =
+              pack_bf16(__uint_as_float(ov[2 * c]) * pend_inv_l, __uint_as_float(ov[2 * c + 1]) * pend_inv_l);
+      }
+      tc_fence_before();   // O_w has been read
+      return true;
+    };
+    // Two groups of 16 rows per warp: the group's lanes write their rows into the warp's staging slot in the
+    // 128-byte-swizzled layout (two 64-wide halves) and lane 0 stores them with two TMA tensor stores; a
+    // group whose rows run past the chunk stores row by row instead (a whole box would overwrite the next
+    // chunk's rows). Then the pending item's ring entry is released.
+    auto epi_store = [&](const uint32_t (&pw)[D / 2]) {
+      const Item& pi = ring[pend_slot];
+      const int t0 = pi.t0, n_b = pi.n_b, h = pi.h;
+      const int row0 = pi.q0 + w * BM + wi * 32;   // chunk row of this warp's lane 0
+      mbar_arrive(B(B_IE + pend_slot));
+      uint8_t* stg = smem + OFF_E + warp * STG;
+      const uint32_t stg_a = sbase + OFF_E + warp * STG;
+      const int rr = lane & 15;
+#pragma unroll
+      for (int hg = 0; hg < 2; ++hg) {
+        const int g0 = row0 + hg * 16;
+        const bool mine = (lane >> 4) == hg;
+        if (g0 + 16 <= n_b) {
+          if (mine) {
+#pragma unroll
+            for (int c16 = 0; c16 < 16; ++c16)
+              *reinterpret_cast<uint4*>(stg + (c16 >> 3) * (STG / 2) + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4)) =
+                  make_uint4(pw[4 * c16], pw[4 * c16 + 1], pw[4 * c16 + 2], pw[4 * c16 + 3]);
+          }
+          fence_proxy_async_smem();          // generic-proxy writes -> visible to the copy engine
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmo, stg_a, 0, h, t0 + g0);
+            tma_store_3d(&tmo, stg_a + STG / 2, 64, h, t0 + g0);
+            bulk_commit();
+            bulk_wait_read();                // the slot is rewritten by the next group
+          }
+          __syncwarp();
+        } else if (mine && g0 + rr < n_b) {
+          uint4* orow = reinterpret_cast<uint4*>(prm.out + (static_cast<long long>(t0 + g0 + rr) * prm.hq + h) * D);
+#pragma unroll
+          for (int c16 = 0; c16 < 16; ++c16)
+            orow[c16] = make_uint4(pw[4 * c16], pw[4 * c16 + 1], pw[4 * c16 + 2], pw[4 * c16 + 3]);
+        }
+      }
+    };
+    // A pending epilogue is flushed at once on an item this warpgroup takes no part in (nothing overwrites
+    // its O there), so that its ring entry is never held across several items.
+    auto flush = [&]() {
+      if (!pend) return;
+      uint32_t pw[D / 2];
+      if (epi_read(pw)) epi_store(pw);
+      else ok = false;
+      pend = false;
+    };
+    for (int e = 0; ok; ++e) {
+      const int slot = e % NI;
+      if (!__all_sync(0xffffffffu, mbar_wait(B(B_IF + slot), (e / NI) & 1, prm.err))) {
+        abort_flag = 1;
+        break;
+      }
+      const Item& it = ring[slot];
+      const int kind = it.kind;
+      int my_tb = 0, my_te = -1, my_pmin = 0, my_pmax = 0, kv_len = 0;
+      if (kind == kLive) {
+        const Item itc = it;
+        const Tiles T = tiles_of(itc, window);
+        if (w == 0 || T.valid1) {
+          my_tb = w == 0 ? T.tb0 : T.tb1;
+          my_te = w == 0 ? T.te0 : T.te1;
+          my_pmin = w == 0 ? T.pmin0 : T.pmin1;
+          my_pmax = w == 0 ? T.pmax0 : T.pmax1;
+          kv_len = itc.fp + itc.n_b;
+        }
+      }
+      if (my_te < my_tb) {
+        // an entry this warpgroup takes no part in: the end of the list, a chunk whose rows the tables place
+        // outside the cache (zero outputs, error word set, nothing loaded), or an item without this Q tile
+        flush();
+        if (kind == kBad) {
+          const int qrow = it.q0 + w * BM + r;
+          if (w == 0 && r == 0) set_error(prm.err, kErrIndex);
+          if (qrow < it.n_b) {
+            uint4* o = reinterpret_cast<uint4*>(prm.out + (static_cast<long long>(it.t0 + qrow) * prm.hq + it.h) * D);
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) o[j] = make_uint4(0, 0, 0, 0);
           }
         }
+        mbar_arrive(B(B_IE + slot));
+        if (kind == kEnd) break;
+        continue;
       }
-      if (full_tile) {
-        fence_proxy_async_smem();                    // generic-proxy writes -> visible to the copy engine
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t src = sbase + OFF_Q + w * TILE + wi * 32 * 128;   // 4 KB aligned: swizzle phase 0
-          const int tok = t0 + q0 + w * BM + wi * 32;
-          tma_store_3d(&tmo, src, 0, h, tok);
-          tma_store_3d(&tmo, src + HALF, 64, h, tok);
-          bulk_commit();
-          bulk_wait_read();                          // shared memory stays valid until the copies read it
+      const int p = my_pmin + r;         // this row's position
+      float m = -CUDART_INF_F, l = 0.f;
+      int nact = 0;
+      for (int t = my_tb; t <= my_te; ++t) {
+        // outcomes are made warp-uniform: the TMEM loads and stores below are warp-collective
+        if (__any_sync(0xffffffffu, *vabort != 0)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(B(B_SF + w), ns & 1, prm.err))) {
+          abort_flag = 1;
+          ok = false;
+          break;
         }
+        ++ns;
+        tc_fence_after();
+        uint32_t zr[BN];
+        tmem_ld128(t_s, zr);
+        tmem_wait_ld();
+        const int kstart = t * BN;
+        const bool need_mask = !(kstart + BN - 1 <= my_pmin &&
+                                 (window == 0 || my_pmax - kstart <= window - 1) && kstart + BN <= kv_len);
+        // zr: the raw score q.k (scaled into log2 units inside the exponent), or for capped layers the
+        // capped logit already in log2 units. Visible keys of this row in the tile: columns [lo_c, hi_c].
+        const int hi_c = min(p, kv_len - 1) - kstart;
+        const int lo_c = window > 0 ? p - window + 1 - kstart : -BN;
+        float tmax;
+        if (cap > 0.f) {
+          tmax = need_mask ? row_pass<true, true>(zr, cap_in, cap_l2, lo_c, hi_c)
+                           : row_pass<true, false>(zr, cap_in, cap_l2, lo_c, hi_c);
+        } else {
+          tmax = need_mask ? row_pass<false, true>(zr, cap_in, cap_l2, lo_c, hi_c)
+                           : row_pass<false, false>(zr, cap_in, cap_l2, lo_c, hi_c);
+        }
+        tmax *= zmul;
+        const float m_new = fmaxf(m, tmax);
+        const bool grow = m_new > m + kRescaleThreshold;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ex2(m - m_new);   // 0 when m was -inf
+          l *= alpha;
+          m = m_new;
+        }
+        if (nact > 0 && __any_sync(0xffffffffu, grow)) {
+          // O row *= alpha (rows that did not grow multiply by 1). PV of the previous tile has completed:
+          // its commit preceded the S commit just waited on.
+#pragma unroll
+          for (int j = 0; j < D / 32; ++j) {
+            uint32_t ov[32];
+            tmem_ld32(t_o + j * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(t_o + j * 32, ov);
+          }
+        }
+        const float nmu = (m == -CUDART_INF_F) ? 0.f : -m;
+        // p = 2^(z * zmul - m) two scores at a time (packed fp32 pairs), row sum in 4 packed accumulators
+        const uint64_t zmul2 = f2_pack(zmul, zmul), nmu2 = f2_pack(nmu, nmu);
+        uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int e = 0; e < BN / 2; ++e) {
+          float xa, xb;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(zr[2 * e]), __uint_as_float(zr[2 * e + 1])), zmul2, nmu2), xa, xb);
+          const float pa = ex2(xa), pb = ex2(xb);
+          ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(pa, pb));
+          pk[e] = pack_bf16(pa, pb);
+        }
+        tmem_st64(t_s, pk);     // P (bf16, 2 per column) over the first half of the S columns
+        {
+          float a0, a1, b0, b1, c0, c1, d0, d1;
+          f2_unpack(f2_add(ls2[0], ls2[1]), a0, a1);
+          f2_unpack(f2_add(ls2[2], ls2[3]), b0, b1);
+          (void)c0; (void)c1; (void)d0; (void)d1;
+          l += (a0 + a1) + (b0 + b1);
+        }
+        tmem_wait_st();
+        if (kstart + BN > kv_len) {
+          // V rows past the row's last key hold whatever the cache holds there (maybe NaN); P is 0 there,
+          // but 0 * NaN is NaN, so zero those rows before the tensor core reads them (after the V copy has
+          // landed; the stage cannot be refilled before this tile's PV, which waits for us).
+          const int tb0 = (window > 0 ? max(0, it.fp + it.q0 - window + 1) : 0) / BN;   // the item's first tile
+          const int g = it.round0 + t - tb0 + 1;   // ring slot of this tile's round
+          if (!__all_sync(0xffffffffu, mbar_wait(B(B_FU + g % NS), (g / NS) & 1, prm.err))) {
+            abort_flag = 1;
+            ok = false;
+            break;
+          }
+          if (kstart + r >= kv_len) {
+            uint8_t* vtile = smem + OFF_R + (g % NS) * 2 * TILE + TILE;   // V(t), in the round slot of tile t
+            uint4* vrow0 = reinterpret_cast<uint4*>(vtile + r * 128);
+            uint4* vrow1 = reinterpret_cast<uint4*>(vtile + HALF + r * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              vrow0[c] = make_uint4(0, 0, 0, 0);
+              vrow1[c] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        if (pend) {
+          // the previous item's O is read before this P lets the next PV overwrite it
+          uint32_t pw[D / 2];
+          if (!epi_read(pw)) {
+            abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive(B(B_PF + w));
+          epi_store(pw);
+          pend = false;
+        } else {
+          mbar_arrive(B(B_PF + w));
+        }
+        ++nact;
       }
-    } else {
-      abort_flag = 1;
+      if (!ok) break;
+      pend = true;                        // this item's epilogue: deferred (its ring entry stays held)
+      pend_slot = slot;
+      pend_inv_l = l > 0.f ? 1.f / l : 0.f;
     }
+    if (!ok) abort_flag = 1;
   }
 
   tc_fence_before();
@@ -612,13 +852,16 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   CUtensorMap tmq, tmk, tmv, tmo;
   const uint64_t rows_total = static_cast<uint64_t>(a.num_rows) * a.hkv * a.max_len;
   // q_rot and out [N, Hq, D]: q rows past N are zero-filled by the copy engine, never read from memory; out
-  // boxes are only stored whole when all their rows belong to the chunk
+  // boxes (16 rows) are only stored whole when all their rows belong to the chunk
   const uint64_t n_tok = static_cast<uint64_t>(a.n_tokens);
   if (!encode_tmap_3d_bf16(&tmq, a.q_rot, D, a.hq, n_tok, D * 2, static_cast<uint64_t>(a.hq) * D * 2, 64, 1, BM) ||
-      !encode_tmap_3d_bf16(&tmo, a.out, D, a.hq, n_tok, D * 2, static_cast<uint64_t>(a.hq) * D * 2, 64, 1, 32) ||
+      !encode_tmap_3d_bf16(&tmo, a.out, D, a.hq, n_tok, D * 2, static_cast<uint64_t>(a.hq) * D * 2, 64, 1, 16) ||
       !encode_tmap_2d_bf16(&tmk, a.k_cache, D, rows_total, D * 2, 64, BN) ||
       !encode_tmap_2d_bf16(&tmv, a.v_cache, D, rows_total, D * 2, 64, BN))
     return cudaErrorInvalidValue;
+  const long long n_qt = (a.max_q_len + NQT * BM - 1) / (NQT * BM);
+  const long long n_items = n_qt * a.n_seqs * a.hq;
+  if (n_items > 0x3fffffffLL) return cudaErrorInvalidValue;
   Params prm;
   prm.q_start = a.q_start;
   prm.rows = a.rows;
@@ -629,13 +872,20 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   prm.max_len = a.max_len;
   prm.num_rows = a.num_rows;
   prm.window = a.window;
+  prm.n_seqs = a.n_seqs;
+  prm.n_qt = static_cast<int>(n_qt);
+  prm.n_items = static_cast<int>(n_items);
   prm.softcap = a.softcap;
   prm.scale = a.scale;
   prm.err = a.err;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int n_qt = (a.max_q_len + NQT * BM - 1) / (NQT * BM);
-  dim3 grid(a.hq * a.n_seqs, n_qt);
+  int dev = 0, n_sm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // persistent: one CTA per SM (shared memory and all 512 TMEM columns allow no second one)
+  const int grid = static_cast<int>(std::min<long long>(n_items, n_sm));
   prefill_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
   return cudaGetLastError();
 }

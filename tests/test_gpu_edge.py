@@ -230,3 +230,16 @@ def test_rope_tables_at_long_positions(cuda):
         rc, rsn = A.rope_tables_for_tokens(spec, r, pos.numpy(), lens.numpy())
         np.testing.assert_allclose(cos.cpu().double().numpy(), rc, atol=5e-7, rtol=0)
         np.testing.assert_allclose(sin.cpu().double().numpy(), rsn, atol=5e-7, rtol=0)
+
+
+@pytest.mark.parametrize("window", [0, 96])
+def test_short_chunks_after_a_long_one(cuda, window):
+    """A long chunk then twenty chunks too short for a second query tile: the warpgroup of the second tile
+    finishes its only item early and then has nothing to do for a long run of items (its finished item must
+    not hold the item ring meanwhile); a window makes the two tiles of an item start on different key tiles."""
+    lens = [300] + [50] * 20
+    fps = [0] + [37 * i for i in range(1, 21)]
+    call = _prefill_call(lens, fps, hq=4, hkv=2, window=window, seed=13)
+    ref = ostep.run_layer_call(call)["out"]
+    st, _ = _run(call, cuda)
+    _close(st.out, ref)
