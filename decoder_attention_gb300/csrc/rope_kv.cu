@@ -264,6 +264,180 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
   }
 }
 
+// Bulk-copy form (SHFL layouts with cos/sin rows a multiple of 16 bytes). A block walks tokens blockIdx.x,
+// blockIdx.x + gridDim.x, ... through KB_STAGES shared-memory stages. Per token one thread copies the
+// token's q, k and v rows and its cos/sin rows into a stage with cp.async.bulk (so the loads in flight do not
+// depend on registers); warps 0-7 normalise and rotate the q and k heads in place (same lane layout as
+// above); the same thread then stores the q row to q_rot and each K and V head to its cache slot with bulk
+// copies (V never passes through registers) and refills the stage once the stores have read it.
+constexpr int KB_STAGES = 4;
+constexpr int KB_THREADS = 288;           // 8 computing warps + 1 copy warp
+struct KbLayout {                         // byte offsets within a stage
+  int k, v, cos, sin, hdr, bytes;         // q at 0; hdr: the token's row and position (8 bytes)
+};
+static KbLayout kb_layout(int hq, int hkv, int d, int half, int es) {
+  KbLayout L;
+  L.k = hq * d * es;
+  L.v = L.k + hkv * d * es;
+  L.cos = L.v + hkv * d * es;
+  L.sin = L.cos + half * 4;
+  L.hdr = L.sin + half * 4;
+  L.bytes = (L.hdr + 16 + 127) / 128 * 128;
+  return L;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpdateArgs a, const KbLayout L) {
+  using V = Vec16<T>;
+  constexpr int VEC = V::N;
+  constexpr int TPV = D / VEC;
+  constexpr int HPW = 32 / TPV;
+  extern __shared__ __align__(128) uint8_t kb_smem[];
+  __shared__ uint64_t bars[2 * KB_STAGES];   // full[s] (copy + bytes), done[s] (256 computing threads)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int half = a.rot >> 1;
+  const int heads = a.hq + a.hkv;
+  const int n_mine = a.n > static_cast<int>(blockIdx.x) ? (a.n - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const uint32_t sbase = smem_u32(kb_smem);
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto done = [&](int s) { return smem_u32(&bars[KB_STAGES + s]); };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < KB_STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(done(s), 256);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int es = static_cast<int>(sizeof(T));
+  const uint32_t in_bytes = static_cast<uint32_t>(L.hdr);   // q, k, v, cos, sin
+
+  if (warp == 8) {
+    if (lane != 0) return;
+    // ------------------------------------------------------------------ copies in and out
+    auto issue = [&](int kk) {
+      const int t = blockIdx.x + kk * gridDim.x;
+      const int s = kk % KB_STAGES;
+      const uint32_t st = sbase + s * L.bytes;
+      mbar_arrive_expect_tx(full(s), in_bytes);
+      bulk_load(st, static_cast<const T*>(a.q) + static_cast<long long>(t) * a.hq * D, a.hq * D * es, full(s));
+      bulk_load(st + L.k, static_cast<const T*>(a.k) + static_cast<long long>(t) * a.hkv * D, a.hkv * D * es, full(s));
+      bulk_load(st + L.v, static_cast<const T*>(a.v) + static_cast<long long>(t) * a.hkv * D, a.hkv * D * es, full(s));
+      bulk_load(st + L.cos, a.cos + static_cast<long long>(t) * half, half * 4, full(s));
+      bulk_load(st + L.sin, a.sin + static_cast<long long>(t) * half, half * 4, full(s));
+    };
+    for (int kk = 0; kk < n_mine && kk < KB_STAGES; ++kk) issue(kk);
+    for (int kk = 0; kk < n_mine; ++kk) {
+      const int t = blockIdx.x + kk * gridDim.x;
+      const int s = kk % KB_STAGES;
+      const uint32_t st = sbase + s * L.bytes;
+      if (!mbar_wait(done(s), (kk / KB_STAGES) & 1, a.err)) break;
+      const int* hdr = reinterpret_cast<const int*>(kb_smem + s * L.bytes + L.hdr);
+      const int row = hdr[0], pos = hdr[1];
+      bulk_store(static_cast<T*>(a.q_rot) + static_cast<long long>(t) * a.hq * D, st, a.hq * D * es);
+      if (row >= 0 && row < a.num_rows && pos >= 0 && pos < a.max_len) {
+        for (int g = 0; g < a.hkv; ++g) {
+          const long long off = ((static_cast<long long>(row) * a.hkv + g) * a.max_len + pos) * D;
+          bulk_store(static_cast<T*>(a.k_cache) + off, st + L.k + g * D * es, D * es);
+          bulk_store(static_cast<T*>(a.v_cache) + off, st + L.v + g * D * es, D * es);
+        }
+      }
+      bulk_commit();
+      if (kk + KB_STAGES < n_mine) {
+        bulk_wait_read();   // the stage is refilled only after its stores have read it
+        issue(kk + KB_STAGES);
+      }
+    }
+    bulk_wait_all();
+    return;
+  }
+
+  // -------------------------------------------------------------------- normalise and rotate (warps 0-7)
+  const int sub = lane % TPV, slot = lane / TPV, e0 = sub * VEC;
+  const int hc = half / VEC;
+  const bool lower = sub < hc, upper = sub >= hc && sub < 2 * hc;
+  const int psub = lower ? sub + hc : (upper ? sub - hc : sub);
+  const int src_lane = slot * TPV + psub;
+  const int ci = (lower ? sub : sub - hc) * VEC;   // this piece's pairs (lower or upper half)
+  const bool norm = a.q_norm_w != nullptr;
+  float wq[VEC], wk[VEC];
+  if (norm) {
+#pragma unroll
+    for (int j = 0; j < VEC; j += 4) {
+      const float4 q4 = *reinterpret_cast<const float4*>(a.q_norm_w + e0 + j);
+      const float4 k4 = *reinterpret_cast<const float4*>(a.k_norm_w + e0 + j);
+      wq[j] = q4.x; wq[j + 1] = q4.y; wq[j + 2] = q4.z; wq[j + 3] = q4.w;
+      wk[j] = k4.x; wk[j + 1] = k4.y; wk[j + 2] = k4.z; wk[j + 3] = k4.w;
+    }
+  }
+  const int steps = (heads + HPW - 1) / HPW;
+  for (int kk = 0; kk < n_mine; ++kk) {
+    const int t = blockIdx.x + kk * gridDim.x;
+    const int s = kk % KB_STAGES;
+    uint8_t* st = kb_smem + s * L.bytes;
+    int row = 0, pos = 0;
+    if (warp == 0 && lane == 0) {
+      row = a.rows[t];
+      pos = a.positions[t];
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait(full(s), (kk / KB_STAGES) & 1, a.err))) break;
+    if (warp == 0 && lane == 0) {
+      // the token's cache slot, for the copy thread (published by this thread's arrival on done[s]); written
+      // only now: the stage's full barrier is armed after the copy thread has read the previous token's slot
+      if (row < 0 || row >= a.num_rows || pos < 0 || pos >= a.max_len) set_error(a.err, kErrIndex);
+      int* hdr = reinterpret_cast<int*>(st + L.hdr);
+      hdr[0] = row;
+      hdr[1] = pos;
+    }
+    float c[VEC], sv[VEC];
+    if (lower || upper) {
+#pragma unroll
+      for (int j = 0; j < VEC; j += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(st + L.cos + (ci + j) * 4);
+        const float4 s4 = *reinterpret_cast<const float4*>(st + L.sin + (ci + j) * 4);
+        c[j] = c4.x; c[j + 1] = c4.y; c[j + 2] = c4.z; c[j + 3] = c4.w;
+        sv[j] = s4.x; sv[j + 1] = s4.y; sv[j + 2] = s4.z; sv[j + 3] = s4.w;
+      }
+    }
+    for (int step = warp; step < steps; step += 8) {
+      const int hh = step * HPW + slot;
+      const bool live = hh < heads;
+      const bool is_q = hh < a.hq;
+      T* vec = reinterpret_cast<T*>(st + (is_q ? hh * D * es : L.k + (hh - a.hq) * D * es)) + e0;
+      float x[VEC];
+      if (live) V::load(vec, x);
+      else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) x[j] = 0.f;
+      }
+      if (norm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) ss = fmaf(x[j], x[j], ss);
+#pragma unroll
+        for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
+        const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * (is_q ? wq[j] : wk[j]);
+      }
+      float px[VEC], y[VEC];
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) px[j] = __shfl_sync(0xffffffffu, x[j], src_lane);
+      if (lower || upper) {
+        const float sgn = lower ? -1.f : 1.f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) y[j] = fmaf(sgn * px[j], sv[j], x[j] * c[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) y[j] = x[j];
+      }
+      if (live) V::store(vec, y);
+    }
+    fence_proxy_async_smem();   // the rotated vectors (generic proxy) -> visible to the bulk stores
+    mbar_arrive(done(s));
+  }
+}
+
 template <typename T, int D>
 static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
   if (a.n == 0) return cudaSuccess;
@@ -272,6 +446,23 @@ static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
   const int groups = (a.hq + a.hkv + HPW - 1) / HPW;
   KvUpdateArgs b = a;
   b.wpt = std::max(1, std::min(groups, (2048 + a.n - 1) / a.n));
+  constexpr int VEC = Vec16<T>::N;
+  const int half = a.rot / 2;
+  if (half % VEC == 0 && half % 4 == 0) {
+    const KbLayout L = kb_layout(a.hq, a.hkv, D, half, static_cast<int>(sizeof(T)));
+    const int smem = KB_STAGES * L.bytes;
+    if (smem <= 200 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kv_update_bulk_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      int per_sm = 0, dev = 0, n_sm = 0;
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_update_bulk_kernel<T, D>, KB_THREADS, smem);
+      if (e == cudaSuccess) e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      const int grid = std::max(1, std::min(a.n, n_sm * std::max(per_sm, 1)));
+      kv_update_bulk_kernel<T, D><<<grid, KB_THREADS, smem, stream>>>(a, L);
+      return cudaGetLastError();
+    }
+  }
   const long long warps = static_cast<long long>(a.n) * b.wpt;
   const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);   // 8 warps per block
   if ((a.rot / 2) % Vec16<T>::N == 0)
