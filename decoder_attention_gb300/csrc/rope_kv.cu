@@ -38,39 +38,57 @@ RopeTurns rope_turns(const RopeFreqs& f) {
   return t;
 }
 
-// One thread per (token, pair). p * turns (mod 2^64) is the angle's fraction of a full turn, exactly up to
-// the table's 53 significant bits; its top 32 bits, read as a signed fraction x in [-1, 1), give the angle
-// pi * x in [-pi, pi), whose sine and cosine sincospif takes in fp32. At p ~ 131071 an fp32 product
-// p * inv would be off by up to 4e-3 rad; this stays within ~2e-7.
+// One thread per (token, four consecutive pairs): the token's position (and sequence length) is loaded once
+// for the four. p * turns (mod 2^64) is the angle's fraction of a full turn, exactly up to the table's 53
+// significant bits; its top 32 bits, read as a signed fraction x in [-1, 1), give the angle pi * x in
+// [-pi, pi), whose sine and cosine sincospif takes in fp32. At p ~ 131071 an fp32 product p * inv would be
+// off by up to 4e-3 rad; this stays within ~2e-7.
+constexpr int kRopePairs = 4;
 __global__ void rope_tables_kernel(const __grid_constant__ RopeTurns f, const int32_t* __restrict__ positions,
                                    const int32_t* __restrict__ seq_len, int n, float* __restrict__ cos_out,
                                    float* __restrict__ sin_out, int* err) {
+  const int groups = (f.half + kRopePairs - 1) / kRopePairs;   // pair groups per token
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(n) * f.half;
-  if (idx >= total) return;
-  const int t = static_cast<int>(idx / f.half);
-  const int i = static_cast<int>(idx - static_cast<long long>(t) * f.half);
+  if (idx >= static_cast<long long>(n) * groups) return;
+  const int t = static_cast<int>(idx / groups);
+  const int i0 = static_cast<int>(idx - static_cast<long long>(t) * groups) * kRopePairs;
   const int p = positions[t];
-  if (p < 0) {
-    set_error(err, kErrIndex);
-    cos_out[idx] = 0.f;
-    sin_out[idx] = 0.f;
-    return;
-  }
   const bool use_long = f.use_seq_len && seq_len[t] > f.switch_len;
-  const unsigned long long turn = use_long ? f.turn_long[i] : f.turn_short[i];
-  const unsigned long long frac = static_cast<unsigned long long>(p) * turn;     // mod 2^64
-  const int top = static_cast<int>(static_cast<unsigned int>(frac >> 32));      // signed fraction of 2^31
-  const float x = static_cast<float>(top) * 4.656612873077393e-10f;             // top / 2^31
-  float s, c;
-  sincospif(x, &s, &c);
-  cos_out[idx] = c * f.af;
-  sin_out[idx] = s * f.af;
+  float c[kRopePairs], s[kRopePairs];
+#pragma unroll
+  for (int j = 0; j < kRopePairs; ++j) {
+    const int i = i0 + j;
+    const unsigned long long turn = i < f.half ? (use_long ? f.turn_long[i] : f.turn_short[i]) : 0ull;
+    const unsigned long long frac = static_cast<unsigned long long>(p) * turn;     // mod 2^64
+    const int top = static_cast<int>(static_cast<unsigned int>(frac >> 32));      // signed fraction of 2^31
+    const float x = static_cast<float>(top) * 4.656612873077393e-10f;             // top / 2^31
+    sincospif(x, &s[j], &c[j]);
+    c[j] *= f.af;
+    s[j] *= f.af;
+  }
+  if (p < 0) {
+    if (i0 == 0) set_error(err, kErrIndex);
+#pragma unroll
+    for (int j = 0; j < kRopePairs; ++j) c[j] = s[j] = 0.f;
+  }
+  const long long o = static_cast<long long>(t) * f.half + i0;
+  if (f.half % kRopePairs == 0) {   // rows of 16-byte multiples: vector stores
+    *reinterpret_cast<float4*>(cos_out + o) = make_float4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<float4*>(sin_out + o) = make_float4(s[0], s[1], s[2], s[3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kRopePairs; ++j) {
+      if (i0 + j < f.half) {
+        cos_out[o + j] = c[j];
+        sin_out[o + j] = s[j];
+      }
+    }
+  }
 }
 
 cudaError_t launch_rope_tables(const RopeFreqs& f, const int32_t* positions, const int32_t* seq_len, int n,
                                float* cos, float* sin, int* err, cudaStream_t stream) {
-  const long long total = static_cast<long long>(n) * f.half;
+  const long long total = static_cast<long long>(n) * ((f.half + kRopePairs - 1) / kRopePairs);
   if (total == 0) return cudaSuccess;
   const RopeTurns turns = rope_turns(f);
   const int threads = 256;
