@@ -72,7 +72,11 @@ constexpr int B_QF = 0, B_QE = B_QF + NQB, B_FU = B_QE + NQB, B_EM = B_FU + NS, 
               N_BARS = B_DR + 1;
 constexpr int OFF_ITEMS = (OFF_BAR + N_BARS * 8 + 15) / 16 * 16;
 constexpr int OFF_SLOT = OFF_ITEMS + NI * 32;
-constexpr int SMEM_BYTES = OFF_SLOT + 16 + 1024;   // + TMEM address slot + alignment slack
+constexpr int kMaxPairs = 512;                     // (chunk, q-tile) pairs the schedule table ranks
+constexpr int OFF_ORD = OFF_SLOT + 16;             // schedule table: pair of each cost rank (uint16)
+constexpr int SMEM_BYTES = OFF_ORD + kMaxPairs * 2 + 1024;   // + alignment slack
+// scratch of the schedule build, in the output staging area: pair costs, then one counter per cost
+constexpr int kMaxCostBins = (8 * STG - kMaxPairs * 4) / 4;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -129,7 +133,8 @@ __device__ __forceinline__ Tiles tiles_of(const Item& it, int window) {
   return T;
 }
 
-// Item of round r for CTA c of G: snake order over the heaviest-first numbering.
+// Schedule rank of the item CTA c of G takes in its round r: a snake over the ranks, so that CTAs that take
+// a heavier item in one round take a lighter one in the next.
 __device__ __forceinline__ int item_of(int r, int c, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -306,50 +311,120 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
-    if (warp == 11 && lane == 0) {
-      // ---------------------------------------------------------------- item decoder
-      const int per_round = prm.n_seqs * prm.hq;
-      int e = 0, rounds = 0;
-      bool ok = true;
-      auto released = [&](int k) {   // wait until every reader has released entry k
-        return mbar_wait(B(B_IE + k % NI), (k / NI) & 1, prm.err);
-      };
-      auto put = [&](const Item& it) -> bool {
-        const int slot = e % NI;
-        if (e >= NI && !released(e - NI)) return false;
-        ring[slot] = it;
-        mbar_arrive(B(B_IF + slot));   // release: the entry's stores are visible to the acquiring readers
-        ++e;
-        return true;
-      };
-      for (int r = 0; ok && r * G < prm.n_items && !*vabort; ++r) {
-        const int id = item_of(r, cta, G);
-        if (id >= prm.n_items) continue;
-        const int y = id / per_round, x = id - y * per_round;
-        const int s = x / prm.hq, h = x - s * prm.hq;
-        Item it;
-        it.t0 = prm.q_start[s];
-        it.n_b = prm.q_start[s + 1] - it.t0;
-        it.q0 = (prm.n_qt - 1 - y) * (NQT * BM);
-        if (it.q0 >= it.n_b) continue;           // this chunk has no rows that far
-        const int row = prm.rows[s];
-        it.fp = prm.first_pos[s];
-        it.h = h;
-        const bool bad = row < 0 || row >= prm.num_rows || it.fp < 0 || it.fp + it.n_b > prm.max_len;
-        it.kind = bad ? kBad : kLive;
-        it.plane = bad ? 0 : (row * prm.hkv + h / (prm.hq / prm.hkv)) * prm.max_len;
-        it.round0 = rounds;
-        if (!bad) rounds += tiles_of(it, window).n;
-        ok = put(it);
+    if (warp == 11) {
+      // ---------------------------------------------------------------- schedule (whole warp)
+      // Items are the (chunk, q-tile) pairs times the query heads. The pairs are ranked by key-tile count,
+      // heaviest first, ties in numbering order (pair p = y * n_seqs + chunk, y counting q-tiles from each
+      // chunk's last); pairs without rows are dropped. Every CTA builds the same table, so the snake over
+      // its ranks hands each item to exactly one CTA. The costs and counters live in the output staging
+      // area, which no epilogue touches before this warp has published its first item. Batches with more
+      // pairs (or larger costs) than the table holds keep the numbering order.
+      uint16_t* order = reinterpret_cast<uint16_t*>(smem + OFF_ORD);
+      int n_live = -1;   // pairs in the table; -1: no table
+      const int n_pairs = prm.n_qt * prm.n_seqs;
+      if (n_pairs <= kMaxPairs) {
+        int* cost = reinterpret_cast<int*>(smem + OFF_E);
+        int* bin = cost + kMaxPairs;   // bin b: pairs of cost cmax - b, then the first rank they take
+        int cmax = -1;
+        for (int p = lane; p < n_pairs; p += 32) {
+          const int y = p / prm.n_seqs, s = p - y * prm.n_seqs;
+          Item it;
+          it.n_b = prm.q_start[s + 1] - prm.q_start[s];
+          it.q0 = (prm.n_qt - 1 - y) * (NQT * BM);
+          it.fp = prm.first_pos[s];
+          int c = -1;
+          if (it.q0 < it.n_b) {
+            const int row = prm.rows[s];
+            const bool bad = row < 0 || row >= prm.num_rows || it.fp < 0 || it.fp + it.n_b > prm.max_len;
+            c = bad ? 0 : tiles_of(it, window).n;
+          }
+          cost[p] = c;
+          cmax = max(cmax, c);
+        }
+        for (int o = 16; o > 0; o >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+        const int nb = cmax + 1;
+        if (nb <= kMaxCostBins) {
+          for (int b = lane; b < nb; b += 32) bin[b] = 0;
+          __syncwarp();
+          for (int p = lane; p < n_pairs; p += 32)
+            if (cost[p] >= 0) atomicAdd(&bin[cmax - cost[p]], 1);
+          __syncwarp();
+          int carry = 0;   // exclusive scan of the counts: first rank of each bin
+          for (int b0 = 0; b0 < nb; b0 += 32) {
+            const int b = b0 + lane;
+            const int v = b < nb ? bin[b] : 0;
+            int incl = v;
+            for (int o = 1; o < 32; o <<= 1) {
+              const int t = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += t;
+            }
+            if (b < nb) bin[b] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+          }
+          __syncwarp();
+          n_live = carry;
+          for (int p0 = 0; p0 < n_pairs; p0 += 32) {   // stable placement, 32 pairs at a time
+            const int p = p0 + lane;
+            const int c = p < n_pairs ? cost[p] : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, c);
+            const int before = __popc(peers & ((1u << lane) - 1u));
+            const int first = c >= 0 ? bin[cmax - c] : 0;
+            __syncwarp();
+            if (c >= 0) {
+              order[first + before] = static_cast<uint16_t>(p);
+              if (before == 0) bin[cmax - c] = first + __popc(peers);
+            }
+            __syncwarp();
+          }
+        }
       }
-      if (ok) {
-        Item end;
-        end.kind = kEnd;
-        end.t0 = end.n_b = end.q0 = end.fp = end.plane = end.h = 0;
-        end.round0 = rounds;
-        ok = put(end);
+      __syncwarp();
+      // ---------------------------------------------------------------- item decoder (lane 0)
+      if (lane == 0) {
+        const int n_sched = n_live >= 0 ? n_live * prm.hq : prm.n_items;
+        int e = 0, rounds = 0;
+        bool ok = true;
+        auto released = [&](int k) {   // wait until every reader has released entry k
+          return mbar_wait(B(B_IE + k % NI), (k / NI) & 1, prm.err);
+        };
+        auto put = [&](const Item& it) -> bool {
+          const int slot = e % NI;
+          if (e >= NI && !released(e - NI)) return false;
+          ring[slot] = it;
+          mbar_arrive(B(B_IF + slot));   // release: the entry's stores are visible to the acquiring readers
+          ++e;
+          return true;
+        };
+        for (int r = 0; ok && r * G < n_sched && !*vabort; ++r) {
+          const int id = item_of(r, cta, G);
+          if (id >= n_sched) continue;
+          const int pr = id / prm.hq, h = id - pr * prm.hq;
+          const int p = n_live >= 0 ? order[pr] : pr;
+          const int y = p / prm.n_seqs, s = p - y * prm.n_seqs;
+          Item it;
+          it.t0 = prm.q_start[s];
+          it.n_b = prm.q_start[s + 1] - it.t0;
+          it.q0 = (prm.n_qt - 1 - y) * (NQT * BM);
+          if (it.q0 >= it.n_b) continue;           // this chunk has no rows that far
+          const int row = prm.rows[s];
+          it.fp = prm.first_pos[s];
+          it.h = h;
+          const bool bad = row < 0 || row >= prm.num_rows || it.fp < 0 || it.fp + it.n_b > prm.max_len;
+          it.kind = bad ? kBad : kLive;
+          it.plane = bad ? 0 : (row * prm.hkv + h / (prm.hq / prm.hkv)) * prm.max_len;
+          it.round0 = rounds;
+          if (!bad) rounds += tiles_of(it, window).n;
+          ok = put(it);
+        }
+        if (ok) {
+          Item end;
+          end.kind = kEnd;
+          end.t0 = end.n_b = end.q0 = end.fp = end.plane = end.h = 0;
+          end.round0 = rounds;
+          ok = put(end);
+        }
+        if (!ok) abort_flag = 1;
       }
-      if (!ok) abort_flag = 1;
     } else if (warp == 8 && lane == 0) {
       // ---------------------------------------------------------------- TMA producer: Q tiles, K halves
       // Ring slot j holds the K tile of global round j (the tile the scores issued in round j - 1 use) and

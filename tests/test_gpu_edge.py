@@ -243,3 +243,27 @@ def test_short_chunks_after_a_long_one(cuda, window):
     ref = ostep.run_layer_call(call)["out"]
     st, _ = _run(call, cuda)
     _close(st.out, ref)
+
+
+@pytest.mark.parametrize("window", [0, 300])
+def test_mixed_lengths_and_offsets(cuda, window):
+    """Chunks whose work differs widely (lengths 1 to 700, first positions 0 to 1500): the items are handed out
+    by their key-tile count, not by chunk order, with ties and chunks too short for the later query tiles."""
+    lens = [40, 700, 130, 513, 1, 256, 257, 600]
+    fps = [900, 0, 1300, 17, 1500, 600, 333, 450]
+    call = _prefill_call(lens, fps, hq=4, hkv=2, window=window, seed=21)
+    ref = ostep.run_layer_call(call)["out"]
+    st, _ = _run(call, cuda)
+    _close(st.out, ref)
+
+
+def test_more_chunk_tiles_than_the_schedule_table(cuda):
+    """520 chunks of one query tile each: more (chunk, query tile) pairs than the cost ranking holds, so the
+    items go out in chunk order."""
+    g = torch.Generator().manual_seed(3)
+    lens = torch.randint(1, 6, (520,), generator=g).tolist()
+    fps = torch.randint(0, 100, (520,), generator=g).tolist()
+    call = _prefill_call(lens, fps, hq=2, hkv=1, seed=22)
+    ref = ostep.run_layer_call(call)["out"]
+    st, _ = _run(call, cuda)
+    _close(st.out, ref)
