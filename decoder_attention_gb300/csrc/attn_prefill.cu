@@ -181,18 +181,27 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
 
 // One pass over a row's 128 scores: soft-cap (CAP), mask to the visible column range [lo_c, hi_c] (MASK),
 // and the row max with 8 independent partial maxima (one running max would be a 128-long dependency chain).
-template <bool CAP, bool MASK>
-__device__ __forceinline__ float row_pass(uint32_t (&zr)[BN], float cap_in, float cap_l2, int lo_c, int hi_c) {
-  if (CAP || MASK) {
+// Soft-capped logits in log2 units: cap_l2 * tanh(z * cap_in) written as cap_l2 - 2 cap_l2 / (2^(z * cap_k) + 1)
+// with cap_k = 2 log2(e) * cap_in (tanh x = 1 - 2 / (e^2x + 1)). It saturates to -cap_l2 / +cap_l2 as the
+// power underflows to 0 / overflows to inf; its absolute error is a few ulp of cap_l2.
+__device__ __forceinline__ void cap_pass(uint32_t (&zr)[BN], float cap_k, float cap_l2) {
+  const float m2 = -2.f * cap_l2;
 #pragma unroll
-    for (int c = 0; c < BN; ++c) {
-      float v = __uint_as_float(zr[c]);
-      if (CAP) v = cap_l2 * tanh_fast(v * cap_in);
-      if (MASK) v = (c >= lo_c && c <= hi_c) ? v : -CUDART_INF_F;
-      zr[c] = __float_as_uint(v);
-    }
-  }
-  // 8 independent partial maxima, two new scores per 3-input max
+  for (int c = 0; c < BN; ++c)
+    zr[c] = __float_as_uint(fmaf(rcp_approx(ex2(__uint_as_float(zr[c]) * cap_k) + 1.f), m2, cap_l2));
+}
+
+// Columns outside [lo_c, hi_c] (keys this row does not see) set to -inf: one unsigned compare per column.
+__device__ __forceinline__ void mask_pass(uint32_t (&zr)[BN], int lo_c, int hi_c) {
+  if (hi_c < lo_c) lo_c = BN, hi_c = BN;   // no visible column: c - lo_c wraps above the span for every c
+  const uint32_t span = static_cast<uint32_t>(hi_c - lo_c);
+#pragma unroll
+  for (int c = 0; c < BN; ++c)
+    zr[c] = static_cast<uint32_t>(c - lo_c) <= span ? zr[c] : __float_as_uint(-CUDART_INF_F);
+}
+
+// Row maximum: 8 independent partial maxima, two new scores per 3-input max.
+__device__ __forceinline__ float row_max(const uint32_t (&zr)[BN]) {
   float mx[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(zr[2 * e]), __uint_as_float(zr[2 * e + 1]));
@@ -673,7 +682,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const uint32_t t_s = tmem + lane_addr + w * BN;
     const uint32_t t_o = tmem + lane_addr + 256 + w * D;
     const float cap = prm.softcap;
-    const float cap_in = cap > 0.f ? prm.scale / cap : 0.f;
+    const float cap_k = cap > 0.f ? 2.f * kLog2e * prm.scale / cap : 0.f;
     const float cap_l2 = cap * kLog2e;
     const float zmul = cap > 0.f ? 1.f : prm.scale * kLog2e;   // z * zmul is the logit in log2 units
     int ns = 0, nod = 0;
@@ -813,15 +822,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         // capped logit already in log2 units. Visible keys of this row in the tile: columns [lo_c, hi_c].
         const int hi_c = min(p, kv_len - 1) - kstart;
         const int lo_c = window > 0 ? p - window + 1 - kstart : -BN;
-        float tmax;
-        if (cap > 0.f) {
-          tmax = need_mask ? row_pass<true, true>(zr, cap_in, cap_l2, lo_c, hi_c)
-                           : row_pass<true, false>(zr, cap_in, cap_l2, lo_c, hi_c);
-        } else {
-          tmax = need_mask ? row_pass<false, true>(zr, cap_in, cap_l2, lo_c, hi_c)
-                           : row_pass<false, false>(zr, cap_in, cap_l2, lo_c, hi_c);
-        }
-        tmax *= zmul;
+        if (cap > 0.f) cap_pass(zr, cap_k, cap_l2);
+        if (need_mask) mask_pass(zr, lo_c, hi_c);
+        const float tmax = row_max(zr) * zmul;
         const float m_new = fmaxf(m, tmax);
         const bool grow = m_new > m + kRescaleThreshold;
         float alpha = 1.f;

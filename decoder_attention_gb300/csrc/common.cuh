@@ -244,6 +244,12 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Packed fp32 pairs (Blackwell executes these as one instruction on two lanes of a 64-bit register pair).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
