@@ -5,12 +5,13 @@
 // families" and "Sliding windows"; soft-capping as "Model resolution" lists it for Gemma 2): for every
 // query row, softmax over its visible keys of scale * q.k (optionally c * tanh(. / c)), times V.
 //
-// Persistent: one CTA per SM walks a fixed list of work items. An item is 256 query rows (two 128-row
-// tiles Q0, Q1) of one (sequence, query head); items are numbered with the latest query tiles (the most
-// keys) first and dealt to the CTAs in snake order. The items' key tiles form one sequence that streams
-// by TMA (128-byte swizzle) through a 2-stage ring; a stage holds one round's K and V tiles. Each Q tile's
-// buffer is freed as soon as its last scores are done, so the next item's Q tiles load while the current
-// item finishes; the output leaves through a per-warp staging slot by TMA tensor stores. Roles:
+// Persistent: one CTA per SM walks a fixed list of work items. An item is two 128-row query tiles Q0, Q1
+// that read the same KV head: the same 128 rows of two query heads when the heads per KV head are even
+// (both tiles then see the same key tiles), else 256 consecutive rows of one head. Every CTA ranks the
+// items by key-tile count and takes its share in snake order. The items' key tiles form one sequence that
+// streams by TMA (128-byte swizzle) through a 2-stage ring; a stage holds one round's K and V tiles. Each Q
+// tile's buffer is freed as soon as its last scores are done, so the next item's Q tiles load while the
+// current item finishes; the output leaves through a per-warp staging slot by TMA tensor stores. Roles:
 //   warp 11     item decoder: reads the chunk tables into a small ring of decoded items in shared memory
 //               that every other role walks in the same order
 //   warp 8      TMA producer of Q tiles and of the K halves of the ring
@@ -91,6 +92,7 @@ struct Params {
   __nv_bfloat16* out;
   int hq, hkv, max_len, num_rows, window;
   int n_seqs, n_qt, n_items;
+  int hpair;   // 1: an item is 128 rows of two query heads sharing a KV head; 0: 256 rows of one head
   float softcap, scale;
   int* err;
 };
@@ -108,6 +110,12 @@ struct Item {
 };
 constexpr int kEnd = 0, kLive = 1, kBad = 2;
 
+// The two Q tiles of an item. Head-pair items (query heads per KV head even): the same 128 chunk rows of
+// query heads h and h + 1, which share a KV head, so both tiles see the same key tiles. Row-pair items: chunk
+// rows q0 .. q0 + 255 of head h, Q1 the upper 128 (its causal range one key tile longer).
+__device__ __forceinline__ int qt_row(const Item& it, int w, int hpair) { return it.q0 + (hpair ? 0 : w * BM); }
+__device__ __forceinline__ int qt_head(const Item& it, int w, int hpair) { return it.h + (hpair ? w : 0); }
+
 // Key-tile ranges of an item's two Q tiles: each from the tile holding its oldest query's first visible
 // key to the tile holding its newest query's own key. Q0's range starts and ends no later than Q1's, and
 // together they cover tb0 .. max(te0, te1) without a gap.
@@ -117,14 +125,14 @@ struct Tiles {
   int tb0, te0, tb1, te1;  // tile ranges (te1 < tb1 when Q1 has no rows)
   int n;                   // tiles tb0 .. max(te0, te1)
 };
-__device__ __forceinline__ Tiles tiles_of(const Item& it, int window) {
+__device__ __forceinline__ Tiles tiles_of(const Item& it, int window, int hpair) {
   Tiles T;
-  T.valid1 = it.q0 + BM < it.n_b;
+  T.valid1 = hpair || it.q0 + BM < it.n_b;
   const int nr0 = min(BM, it.n_b - it.q0);
   T.pmin0 = it.fp + it.q0;
   T.pmax0 = T.pmin0 + nr0 - 1;
-  T.pmin1 = T.pmin0 + BM;
-  T.pmax1 = T.valid1 ? it.fp + min(it.q0 + 2 * BM, it.n_b) - 1 : T.pmin1;
+  T.pmin1 = hpair ? T.pmin0 : T.pmin0 + BM;
+  T.pmax1 = hpair ? T.pmax0 : T.valid1 ? it.fp + min(it.q0 + 2 * BM, it.n_b) - 1 : T.pmin1;
   T.tb0 = (window > 0 ? max(0, T.pmin0 - window + 1) : 0) / BN;
   T.te0 = T.pmax0 / BN;
   T.tb1 = (window > 0 ? max(0, T.pmin1 - window + 1) : 0) / BN;
@@ -285,6 +293,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x, G = gridDim.x;
   const int window = prm.window;
+  const int hpair = prm.hpair;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar = sbase + OFF_BAR;
   auto B = [&](int i) { return bar + 8u * i; };
@@ -339,13 +348,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           const int y = p / prm.n_seqs, s = p - y * prm.n_seqs;
           Item it;
           it.n_b = prm.q_start[s + 1] - prm.q_start[s];
-          it.q0 = (prm.n_qt - 1 - y) * (NQT * BM);
+          it.q0 = (prm.n_qt - 1 - y) * (hpair ? BM : NQT * BM);
           it.fp = prm.first_pos[s];
           int c = -1;
           if (it.q0 < it.n_b) {
             const int row = prm.rows[s];
             const bool bad = row < 0 || row >= prm.num_rows || it.fp < 0 || it.fp + it.n_b > prm.max_len;
-            c = bad ? 0 : tiles_of(it, window).n;
+            c = bad ? 0 : tiles_of(it, window, hpair).n;
           }
           cost[p] = c;
           cmax = max(cmax, c);
@@ -390,7 +399,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       __syncwarp();
       // ---------------------------------------------------------------- item decoder (lane 0)
       if (lane == 0) {
-        const int n_sched = n_live >= 0 ? n_live * prm.hq : prm.n_items;
+        const int hpu = hpair ? prm.hq / 2 : prm.hq;   // items per (chunk, q-tile) pair
+        const int n_sched = n_live >= 0 ? n_live * hpu : prm.n_items;
         int e = 0, rounds = 0;
         bool ok = true;
         auto released = [&](int k) {   // wait until every reader has released entry k
@@ -407,13 +417,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         for (int r = 0; ok && r * G < n_sched && !*vabort; ++r) {
           const int id = item_of(r, cta, G);
           if (id >= n_sched) continue;
-          const int pr = id / prm.hq, h = id - pr * prm.hq;
+          const int pr = id / hpu, h = (id - pr * hpu) << hpair;
           const int p = n_live >= 0 ? order[pr] : pr;
           const int y = p / prm.n_seqs, s = p - y * prm.n_seqs;
           Item it;
           it.t0 = prm.q_start[s];
           it.n_b = prm.q_start[s + 1] - it.t0;
-          it.q0 = (prm.n_qt - 1 - y) * (NQT * BM);
+          it.q0 = (prm.n_qt - 1 - y) * (hpair ? BM : NQT * BM);
           if (it.q0 >= it.n_b) continue;           // this chunk has no rows that far
           const int row = prm.rows[s];
           it.fp = prm.first_pos[s];
@@ -422,7 +432,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           it.kind = bad ? kBad : kLive;
           it.plane = bad ? 0 : (row * prm.hkv + h / (prm.hq / prm.hkv)) * prm.max_len;
           it.round0 = rounds;
-          if (!bad) rounds += tiles_of(it, window).n;
+          if (!bad) rounds += tiles_of(it, window, hpair).n;
           ok = put(it);
         }
         if (ok) {
@@ -441,15 +451,16 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       // arrival). Per item: Q0, the first K tile, Q1, the remaining K tiles.
       prefetch_tmap(&tmq);
       prefetch_tmap(&tmk);
+      prefetch_tmap(&tmv);
       int qn = 0, kj = 0;   // Q tiles loaded, ring slots filled
       bool ok = true;
       auto load_q = [&](const Item& it, int w) -> bool {
         const int b = qn % NQB, u = qn / NQB;
         if (u > 0 && !mbar_wait(B(B_QE + b), (u - 1) & 1, prm.err)) return false;
-        const int tok = it.t0 + it.q0 + w * BM;
+        const int tok = it.t0 + qt_row(it, w, hpair), hd = qt_head(it, w, hpair);
         mbar_arrive_expect_tx(B(B_QF + b), TILE);
-        tma_load_3d(sbase + OFF_Q + b * TILE, &tmq, B(B_QF + b), 0, it.h, tok);
-        tma_load_3d(sbase + OFF_Q + b * TILE + HALF, &tmq, B(B_QF + b), 64, it.h, tok);
+        tma_load_3d(sbase + OFF_Q + b * TILE, &tmq, B(B_QF + b), 0, hd, tok);
+        tma_load_3d(sbase + OFF_Q + b * TILE + HALF, &tmq, B(B_QF + b), 64, hd, tok);
         ++qn;
         return true;
       };
@@ -467,12 +478,33 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         ++kj;
         return true;
       };
+      // The next item's Q tiles and first K/V tiles are fetched into L2 when this item starts: its Q buffers
+      // free only about one round before the tensor core needs them, too late for a DRAM round trip.
+      auto prefetch_next = [&](int e) -> bool {
+        const int slot = e % NI;
+        if (!mbar_wait(B(B_IF + slot), (e / NI) & 1, prm.err)) return false;
+        const Item& nx = ring[slot];   // read without releasing: get_item(e) releases it later
+        if (nx.kind != kLive) return true;
+        const Tiles T = tiles_of(nx, window, hpair);
+        for (int w = 0; w < (T.valid1 ? 2 : 1); ++w) {
+          const int tok = nx.t0 + qt_row(nx, w, hpair), hd = qt_head(nx, w, hpair);
+          tma_prefetch_3d(&tmq, 0, hd, tok);
+          tma_prefetch_3d(&tmq, 64, hd, tok);
+        }
+        const int key = nx.plane + T.tb0 * BN;
+        tma_prefetch_2d(&tmk, 0, key);
+        tma_prefetch_2d(&tmk, 64, key);
+        tma_prefetch_2d(&tmv, 0, key);
+        tma_prefetch_2d(&tmv, 64, key);
+        return true;
+      };
       for (int e = 0; ok; ++e) {
         Item it;
         if (!get_item(e, it)) { ok = false; break; }
         if (it.kind == kEnd) break;
+        if (!prefetch_next(e + 1)) { ok = false; break; }
         if (it.kind != kLive) continue;
-        const Tiles T = tiles_of(it, window);
+        const Tiles T = tiles_of(it, window, hpair);
         if (!load_q(it, 0)) { ok = false; break; }
         for (int i = 0; ok && i < T.n; ++i) {
           if (*vabort || (i == 1 && T.valid1 && !load_q(it, 1)) || !fill_k(it.plane + (T.tb0 + i) * BN)) ok = false;
@@ -510,7 +542,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         if (!get_item(e, it)) { ok = false; break; }
         if (it.kind == kEnd) break;
         if (it.kind != kLive) continue;
-        const Tiles T = tiles_of(it, window);
+        const Tiles T = tiles_of(it, window, hpair);
         for (int i = 0; ok && i < T.n; ++i) {
           if (*vabort || !fill_v(it.plane + (T.tb0 + i) * BN)) ok = false;
         }
@@ -539,7 +571,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             return;
           }
           if (it.kind != kLive) continue;
-          const Tiles T = tiles_of(it, window);
+          const Tiles T = tiles_of(it, window, hpair);
           I.live = true;
           I.tb0 = T.tb0;
           I.te0 = T.te0;
@@ -719,8 +751,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     // chunk's rows). Then the pending item's ring entry is released.
     auto epi_store = [&](const uint32_t (&pw)[D / 2]) {
       const Item& pi = ring[pend_slot];
-      const int t0 = pi.t0, n_b = pi.n_b, h = pi.h;
-      const int row0 = pi.q0 + w * BM + wi * 32;   // chunk row of this warp's lane 0
+      const int t0 = pi.t0, n_b = pi.n_b, h = qt_head(pi, w, hpair);
+      const int row0 = qt_row(pi, w, hpair) + wi * 32;   // chunk row of this warp's lane 0
       mbar_arrive(B(B_IE + pend_slot));
       uint8_t* stg = smem + OFF_E + warp * STG;
       const uint32_t stg_a = sbase + OFF_E + warp * STG;
@@ -773,7 +805,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       int my_tb = 0, my_te = -1, my_pmin = 0, my_pmax = 0, kv_len = 0;
       if (kind == kLive) {
         const Item itc = it;
-        const Tiles T = tiles_of(itc, window);
+        const Tiles T = tiles_of(itc, window, hpair);
         if (w == 0 || T.valid1) {
           my_tb = w == 0 ? T.tb0 : T.tb1;
           my_te = w == 0 ? T.te0 : T.te1;
@@ -787,10 +819,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         // outside the cache (zero outputs, error word set, nothing loaded), or an item without this Q tile
         flush();
         if (kind == kBad) {
-          const int qrow = it.q0 + w * BM + r;
+          const int qrow = qt_row(it, w, hpair) + r;
           if (w == 0 && r == 0) set_error(prm.err, kErrIndex);
           if (qrow < it.n_b) {
-            uint4* o = reinterpret_cast<uint4*>(prm.out + (static_cast<long long>(it.t0 + qrow) * prm.hq + it.h) * D);
+            uint4* o = reinterpret_cast<uint4*>(
+                prm.out + (static_cast<long long>(it.t0 + qrow) * prm.hq + qt_head(it, w, hpair)) * D);
 #pragma unroll
             for (int j = 0; j < D / 8; ++j) o[j] = make_uint4(0, 0, 0, 0);
           }
@@ -937,8 +970,10 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
       !encode_tmap_2d_bf16(&tmk, a.k_cache, D, rows_total, D * 2, 64, BN) ||
       !encode_tmap_2d_bf16(&tmv, a.v_cache, D, rows_total, D * 2, 64, BN))
     return cudaErrorInvalidValue;
-  const long long n_qt = (a.max_q_len + NQT * BM - 1) / (NQT * BM);
-  const long long n_items = n_qt * a.n_seqs * a.hq;
+  const int hpair = (a.hq / a.hkv) % 2 == 0 ? 1 : 0;
+  const int item_rows = hpair ? BM : NQT * BM;
+  const long long n_qt = (a.max_q_len + item_rows - 1) / item_rows;
+  const long long n_items = n_qt * a.n_seqs * (hpair ? a.hq / 2 : a.hq);
   if (n_items > 0x3fffffffLL) return cudaErrorInvalidValue;
   Params prm;
   prm.q_start = a.q_start;
@@ -953,6 +988,7 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   prm.n_seqs = a.n_seqs;
   prm.n_qt = static_cast<int>(n_qt);
   prm.n_items = static_cast<int>(n_items);
+  prm.hpair = hpair;
   prm.softcap = a.softcap;
   prm.scale = a.scale;
   prm.err = a.err;

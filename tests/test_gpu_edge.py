@@ -245,13 +245,16 @@ def test_short_chunks_after_a_long_one(cuda, window):
     _close(st.out, ref)
 
 
+@pytest.mark.parametrize("heads", [(4, 2), (3, 1), (2, 2)])
 @pytest.mark.parametrize("window", [0, 300])
-def test_mixed_lengths_and_offsets(cuda, window):
+def test_mixed_lengths_and_offsets(cuda, window, heads):
     """Chunks whose work differs widely (lengths 1 to 700, first positions 0 to 1500): the items are handed out
-    by their key-tile count, not by chunk order, with ties and chunks too short for the later query tiles."""
+    by their key-tile count, not by chunk order, with ties and chunks too short for the later query tiles.
+    Query heads per KV head 2 (items pair two heads on the same rows), 3 and 1 (items pair two row tiles of
+    one head)."""
     lens = [40, 700, 130, 513, 1, 256, 257, 600]
     fps = [900, 0, 1300, 17, 1500, 600, 333, 450]
-    call = _prefill_call(lens, fps, hq=4, hkv=2, window=window, seed=21)
+    call = _prefill_call(lens, fps, hq=heads[0], hkv=heads[1], window=window, seed=21)
     ref = ostep.run_layer_call(call)["out"]
     st, _ = _run(call, cuda)
     _close(st.out, ref)
