@@ -23,6 +23,9 @@ Where the pages leave a step open the oracle takes one reading; each is named wh
   R7  a query with no allowed key gets output 0.
   R8  a window of w admits w keys including the query's own: key position j is allowed for a query at
       position p iff j <= p and p - j <= w - 1 (w = 0: no window).
+  R9  a learned sink (page "Model resolution", gpt_oss entry: one extra logit per head in every query's
+      softmax whose share is dropped) is a logit in the units of the scaled scores, after any soft-cap and
+      not capped itself, seen by every query whatever its window; its probability multiplies no value.
 
 Parity pins for every function live in ``tests/test_oracle_*.py``; none is left unpinned.
 """
@@ -192,14 +195,15 @@ def window_allowed(q_pos, k_pos, window):
     return ok
 
 
-def causal_attention(q, k, v, q_pos, k_pos, window=0, softcap=0.0, scale=None):
+def causal_attention(q, k, v, q_pos, k_pos, window=0, softcap=0.0, scale=None, sinks=None):
     """GQA softmax attention for one cache row.
 
     q [T, Hq, d] (already rotated), k/v [Hkv, S, d], q_pos [T], k_pos [S] (negative = empty slot).
     For query head h the KV head is floor(h / G) (reading R4). Logits z = scale * q.k with scale
     1/sqrt(d) by default (page 3 §3.4); soft-capped by cap * tanh(z / cap) when softcap > 0 (R5);
     softmax over the allowed keys only (page 3 §2.3: a masked logit is -inf, probability 0); output
-    0 for a query that sees no key (R7). Returns float64 [T, Hq, d].
+    0 for a query that sees no key (R7). With sinks [Hq], head h's softmax also takes the logit sinks[h],
+    whose probability is dropped (R9). Returns float64 [T, Hq, d].
     """
     q = np.asarray(q, dtype=F64)
     k = np.asarray(k, dtype=F64)
@@ -221,9 +225,14 @@ def causal_attention(q, k, v, q_pos, k_pos, window=0, softcap=0.0, scale=None):
         z = np.where(allowed, z, -np.inf)
         zmax = np.max(z, axis=1, keepdims=True)
         has_key = np.isfinite(zmax[:, 0])
+        sink = None if sinks is None else float(sinks[h])
+        if sink is not None:
+            zmax = np.maximum(zmax, sink)
         zmax = np.where(np.isfinite(zmax), zmax, 0.0)
         e = np.where(allowed, np.exp(z - zmax), 0.0)
         den = e.sum(axis=1, keepdims=True)
+        if sink is not None:
+            den = den + np.exp(sink - zmax)
         w = np.divide(e, den, out=np.zeros_like(e), where=den > 0)
         o = w @ v[g]
         o[~has_key] = 0.0
@@ -248,6 +257,7 @@ class Layer:
     window: int = 0                         # 0: full attention
     softcap: float = 0.0                    # 0: off
     scale: float = 0.0                      # 0: 1/sqrt(head_dim)
+    sinks: np.ndarray | None = None         # [Hq] learned sink logits (R9), or None
 
 
 @dataclass
@@ -320,7 +330,8 @@ def attn_prefill(layer: Layer, q_rot, k_cache, v_cache, q_start, rows, first_pos
         else:
             kp = np.asarray(key_positions[row], dtype=np.int64)
             kk, vv = k_cache[row], v_cache[row]
-        out[t0:t1] = causal_attention(q_rot[t0:t1], kk, vv, qp, kp, layer.window, layer.softcap, layer.scale)
+        out[t0:t1] = causal_attention(q_rot[t0:t1], kk, vv, qp, kp, layer.window, layer.softcap, layer.scale,
+                                      layer.sinks)
     return out
 
 
@@ -340,7 +351,8 @@ def attn_decode(layer: Layer, q_rot, k_cache, v_cache, rows, positions, key_posi
         else:
             kp = np.asarray(key_positions[row], dtype=np.int64)
             kk, vv = k_cache[row], v_cache[row]
-        out[s:s + 1] = causal_attention(q_rot[s:s + 1], kk, vv, [p], kp, layer.window, layer.softcap, layer.scale)
+        out[s:s + 1] = causal_attention(q_rot[s:s + 1], kk, vv, [p], kp, layer.window, layer.softcap, layer.scale,
+                                        layer.sinks)
     return out
 
 
@@ -350,4 +362,4 @@ def attn_decode_one(layer: Layer, q_vec, k_row, v_row, p):
     lo = max(0, p - layer.window + 1) if layer.window else 0
     kp = np.arange(lo, p + 1)
     return causal_attention(np.asarray(q_vec, dtype=F64)[None], k_row[:, lo:p + 1], v_row[:, lo:p + 1],
-                            [p], kp, layer.window, layer.softcap, layer.scale)[0]
+                            [p], kp, layer.window, layer.softcap, layer.scale, layer.sinks)[0]

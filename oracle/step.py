@@ -24,7 +24,8 @@ def layer_of(call) -> A.Layer:
                    num_key_value_heads=call.num_key_value_heads, rotary_dim=rot,
                    q_norm_w=_np64(call.q_norm_w) if call.q_norm_w is not None else None,
                    k_norm_w=_np64(call.k_norm_w) if call.k_norm_w is not None else None,
-                   eps=call.eps, window=call.window, softcap=call.softcap, scale=0.0)
+                   eps=call.eps, window=call.window, softcap=call.softcap, scale=0.0,
+                   sinks=_np64(call.sinks) if getattr(call, "sinks", None) is not None else None)
 
 
 def spec_of(call) -> A.RopeSpec:

@@ -237,8 +237,9 @@ def test_window_masks_golden():
     np.testing.assert_array_equal(O.window_allowed([3], [-1, 2, -1, 3], 0), [[False, True, False, True]])
 
 
-def _bruteforce(q, k, v, masks, scale, cap=0.0):
-    """Per query and head: softmax over the explicitly listed visible keys (scipy's softmax)."""
+def _bruteforce(q, k, v, masks, scale, cap=0.0, sinks=None):
+    """Per query and head: softmax over the explicitly listed visible keys (scipy's softmax); with sinks, the
+    head's sink logit joins the list and its weight is then dropped."""
     T, hq, d = q.shape
     hkv = k.shape[0]
     out = np.zeros_like(q)
@@ -251,7 +252,7 @@ def _bruteforce(q, k, v, masks, scale, cap=0.0):
             z = np.array([scale * float(np.dot(q[t, h], k[g, j])) for j in js])
             if cap:
                 z = cap * np.tanh(z / cap)
-            w = sp_softmax(z)
+            w = sp_softmax(z) if sinks is None else sp_softmax(np.append(z, sinks[h]))[:-1]
             out[t, h] = sum(wi * v[g, j] for wi, j in zip(w, js))
     return out
 
@@ -267,6 +268,56 @@ def test_attention_bruteforce_tiny(w):
     np.testing.assert_allclose(got, _bruteforce(q, k, v, masks, 1 / math.sqrt(d)), atol=1e-13)
     got = O.causal_attention(q, k, v, pos, pos, window=w, softcap=0.7)
     np.testing.assert_allclose(got, _bruteforce(q, k, v, masks, 1 / math.sqrt(d), cap=0.7), atol=1e-13)
+
+
+# ------------------------------------------------------------------ learned sinks (page "Model resolution", gpt_oss)
+
+def test_sink_single_key_is_a_sigmoid():
+    """One visible key and a sink: the key's weight is e^z / (e^z + e^s) = 1 / (1 + e^(s - z)); the rest of the
+    mass (the sink's share) reaches no value."""
+    d = 16
+    q, k, v = _rand(1, 3, d), _rand(3, 1, d), _rand(3, 1, d)
+    sinks = np.array([-1.5, 0.25, 3.0])
+    got = O.causal_attention(q, k, v, [0], [0], sinks=sinks)
+    for h in range(3):
+        z = float(np.dot(q[0, h], k[h, 0])) / math.sqrt(d)
+        np.testing.assert_allclose(got[0, h], v[h, 0] / (1.0 + math.exp(sinks[h] - z)), atol=1e-15)
+
+
+@pytest.mark.parametrize("w,cap", [(0, 0.0), (2, 0.0), (0, 0.7), (3, 0.7)])
+def test_sink_bruteforce_tiny(w, cap):
+    """Brute force with the sink as one more softmax entry whose weight is dropped: GQA, windows, and a
+    soft-cap that applies to the scores but not to the sink (sinks up to 2.5 lie beyond a 0.7 cap)."""
+    T, hq, hkv, d = 6, 4, 2, 8
+    q, k, v = _rand(T, hq, d), _rand(hkv, T, d), _rand(hkv, T, d)
+    pos = np.arange(T)
+    sinks = np.array([0.3, -2.0, 2.5, 1.1])
+    got = O.causal_attention(q, k, v, pos, pos, window=w, softcap=cap, sinks=sinks)
+    want = _bruteforce(q, k, v, _golden_masks()[w], 1 / math.sqrt(d), cap=cap, sinks=sinks)
+    np.testing.assert_allclose(got, want, atol=1e-13)
+
+
+def test_sink_at_minus_infinity_is_no_sink():
+    """A sink of -inf has weight 0: the result is the plain softmax, bit for bit."""
+    q, k, v = _rand(5, 4, 16), _rand(2, 5, 16), _rand(2, 5, 16)
+    pos = np.arange(5)
+    np.testing.assert_array_equal(O.causal_attention(q, k, v, pos, pos, window=3, sinks=np.full(4, -np.inf)),
+                                  O.causal_attention(q, k, v, pos, pos, window=3))
+
+
+def test_sink_share_with_unit_values():
+    """With every value equal to 1 the output is the mass the keys keep: 1 - 1 / (1 + sum_j e^(z_j - s))."""
+    T, d = 4, 8
+    q, k = _rand(T, 2, d), _rand(1, T, d)
+    v = np.ones((1, T, d))
+    pos = np.arange(T)
+    sinks = np.array([0.5, -0.75])
+    got = O.causal_attention(q, k, v, pos, pos, sinks=sinks)
+    for t in range(T):
+        for h in range(2):
+            zs = [float(np.dot(q[t, h], k[0, j])) / math.sqrt(d) for j in range(t + 1)]
+            keep = 1.0 - 1.0 / (1.0 + sum(math.exp(z - sinks[h]) for z in zs))
+            np.testing.assert_allclose(got[t, h], np.full(d, keep), atol=1e-14)
 
 
 def test_default_scale_is_inverse_sqrt_d():
