@@ -49,7 +49,8 @@ class DaLayer(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("head_dim", ctypes.c_int), ("num_attention_heads", ctypes.c_int),
                 ("num_key_value_heads", ctypes.c_int), ("rotary_dim", ctypes.c_int),
                 ("q_norm_w", ctypes.c_void_p), ("k_norm_w", ctypes.c_void_p), ("eps", ctypes.c_double),
-                ("window", ctypes.c_int), ("softcap", ctypes.c_float), ("scale", ctypes.c_float)]
+                ("window", ctypes.c_int), ("softcap", ctypes.c_float), ("scale", ctypes.c_float),
+                ("sinks", ctypes.c_void_p)]
 
 
 def _load():
@@ -141,8 +142,9 @@ def rope_scaling(theta, rotary_dim, scaling=None, max_position_embeddings=0):
 
 
 def layer(dtype, head_dim, num_attention_heads, num_key_value_heads, rotary_dim=None, q_norm_w=None,
-          k_norm_w=None, eps=1e-6, window=0, softcap=0.0, scale=0.0):
-    """DaLayer for one layer; q_norm_w/k_norm_w are fp32 device tensors [head_dim] or None."""
+          k_norm_w=None, eps=1e-6, window=0, softcap=0.0, scale=0.0, sinks=None):
+    """DaLayer for one layer; q_norm_w/k_norm_w are fp32 device tensors [head_dim] or None, sinks an fp32
+    device tensor [num_attention_heads] of learned sink logits or None."""
     L = DaLayer()
     L.dtype = DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     L.head_dim = int(head_dim)
@@ -155,6 +157,7 @@ def layer(dtype, head_dim, num_attention_heads, num_key_value_heads, rotary_dim=
     L.window = int(window)
     L.softcap = float(softcap)
     L.scale = float(scale)
+    L.sinks = sinks.data_ptr() if sinks is not None else None
     return L
 
 

@@ -321,6 +321,7 @@ static da::AttnArgs make_args(const da_layer* L, const void* q_rot, const void* 
   a.window = L->window;
   a.softcap = L->softcap;
   a.scale = layer_scale(L);
+  a.sinks = L->sinks;
   a.err = err;
   return a;
 }

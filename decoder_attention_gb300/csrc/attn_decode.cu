@@ -44,6 +44,7 @@ struct Params {
   __nv_bfloat16* out; // [S, Hq, D]
   int hq, hkv, max_len, num_rows, window;
   float softcap, scale;
+  const float* sinks;   // [Hq] sink logits (natural units) or NULL
   int chunk, n_splits;
   int* err;
 };
@@ -320,8 +321,10 @@ __global__ void __launch_bounds__(D) merge_kernel(const Params prm) {
   const long long base = (static_cast<long long>(s) * prm.hq + h) * prm.n_splits;
   float M = -CUDART_INF_F;
   for (int c = 0; c < n_spl; ++c) M = fmaxf(M, prm.ws_ml[base + c].x);
+  const float sink = prm.sinks ? prm.sinks[h] * kLog2e : -CUDART_INF_F;   // log2 units, like the partials
+  M = fmaxf(M, sink);
   const float Mu = (M == -CUDART_INF_F) ? 0.f : M;
-  float acc = 0.f, L = 0.f;
+  float acc = 0.f, L = prm.sinks ? ex2(sink - Mu) : 0.f;   // the sink's share joins the sum, no value
   for (int c = 0; c < n_spl; ++c) {
     const float2 ml = prm.ws_ml[base + c];
     const float wt = ex2(ml.x - Mu);
@@ -400,6 +403,7 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const DecodePlan& plan, void* 
   prm.num_rows = a.num_rows;
   prm.window = a.window;
   prm.softcap = a.softcap;
+  prm.sinks = a.sinks;
   prm.scale = a.scale;
   prm.chunk = plan.chunk;
   prm.n_splits = plan.n_splits;

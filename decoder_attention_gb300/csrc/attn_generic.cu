@@ -116,7 +116,9 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
   float M = -CUDART_INF_F;
 #pragma unroll
   for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_m[w]);
-  float L = 0.f;
+  const float sink = a.sinks ? a.sinks[h] : -CUDART_INF_F;   // one more logit; its share reaches no value
+  M = fmaxf(M, sink);
+  float L = (a.sinks && M != -CUDART_INF_F) ? __expf(sink - M) : 0.f;
   float wgt[4];
 #pragma unroll
   for (int w = 0; w < 4; ++w) {

@@ -94,6 +94,7 @@ struct Params {
   int n_seqs, n_qt, n_items;
   int hpair;   // 1: an item is 128 rows of two query heads sharing a KV head; 0: 256 rows of one head
   float softcap, scale;
+  const float* sinks;   // [Hq] sink logits (natural units) or NULL
   int* err;
 };
 
@@ -944,6 +945,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       if (!ok) break;
       pend = true;                        // this item's epilogue: deferred (its ring entry stays held)
       pend_slot = slot;
+      if (prm.sinks) l += ex2(prm.sinks[qt_head(it, w, hpair)] * kLog2e - m);   // one more logit, no value
       pend_inv_l = l > 0.f ? 1.f / l : 0.f;
     }
     if (!ok) abort_flag = 1;
@@ -990,6 +992,7 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   prm.n_items = static_cast<int>(n_items);
   prm.hpair = hpair;
   prm.softcap = a.softcap;
+  prm.sinks = a.sinks;
   prm.scale = a.scale;
   prm.err = a.err;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);

@@ -83,6 +83,7 @@ struct AttnArgs {
   int window;
   float softcap;
   float scale;
+  const float* sinks;             // [Hq] sink logits (natural units) or NULL
   int* err;
 };
 cudaError_t launch_attn_generic(const AttnArgs& a, bool bf16, cudaStream_t stream);

@@ -60,6 +60,7 @@ class LayerCall:
     eps: float = 1e-6
     q_norm_w: torch.Tensor | None = None        # fp32 [d] or None
     k_norm_w: torch.Tensor | None = None
+    sinks: torch.Tensor | None = None           # fp32 [Hq] learned sink logits or None
     # new tokens
     q: torch.Tensor = None                       # [N, Hq, d]
     k: torch.Tensor = None                       # [N, Hkv, d]

@@ -32,8 +32,9 @@ class AttentionStep:
         self.rs, self._keep = _abi.rope_scaling(c.rope_theta, self.rot, c.rope_scaling, c.max_position_embeddings)
         self.q_norm_w = c.q_norm_w.to(dev, torch.float32).contiguous() if c.q_norm_w is not None else None
         self.k_norm_w = c.k_norm_w.to(dev, torch.float32).contiguous() if c.k_norm_w is not None else None
+        self.sinks = c.sinks.to(dev, torch.float32).contiguous() if c.sinks is not None else None
         self.L = _abi.layer(c.dtype, c.head_dim, c.num_attention_heads, c.num_key_value_heads, self.rot,
-                            self.q_norm_w, self.k_norm_w, c.eps, c.window, c.softcap, 0.0)
+                            self.q_norm_w, self.k_norm_w, c.eps, c.window, c.softcap, 0.0, self.sinks)
         n = c.n_tokens
         self.cos = torch.empty((max(n, 1), self.rot // 2), dtype=torch.float32, device=dev)
         self.sin = torch.empty_like(self.cos)

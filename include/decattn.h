@@ -98,6 +98,11 @@ typedef struct {
     int         window;                       /* sliding window w >= 0 (0 = full attention)           */
     float       softcap;                      /* logit soft-cap c >= 0: z -> c tanh(z / c); 0 = off    */
     float       scale;                        /* softmax scale; 0 means 1/sqrt(d)                     */
+    const float* sinks;                       /* device [Hq] fp32 learned sink logits, or NULL (page  */
+                                              /*   "Model resolution", gpt_oss: one extra logit per   */
+                                              /*   head in every query's softmax, its share dropped;  */
+                                              /*   in the units of the scaled, capped scores, not     */
+                                              /*   capped itself, seen whatever the window)           */
 } da_layer;
 
 /*
@@ -154,6 +159,8 @@ int da_kv_cache_update(const da_layer* layer, const void* q, const void* k, cons
  * must already be written, e.g. by da_kv_cache_update). For query head h with KV head g:
  *     z_j = scale * q_rot[t, h] . k_cache[row, g, j];   z_j = c tanh(z_j / c) when softcap c > 0
  *     out[t, h] = sum_j softmax(z)_j v_cache[row, g, j]   over the visible j; 0 if none is visible
+ * With layer->sinks, head h's softmax also takes the logit sinks[h] (page "Model resolution", gpt_oss):
+ *     out[t, h] = sum_j e^(z_j - m) v_j / (sum_j e^(z_j - m) + e^(sinks[h] - m)),  m = max(max_j z_j, sinks[h])
  * bf16 layers run on the tcgen05 tensor cores (bf16 operands, fp32 accumulation and softmax); fp32 layers
  * and calls with key_positions run a CUDA-core kernel in fp32.
  *

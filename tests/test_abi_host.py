@@ -141,3 +141,32 @@ def test_window_for_layer():
     assert [w(gemma, i) for i in range(4)] == [4096, 0, 4096, 0]
     llama = {"model_type": "llama", "sliding_window": None, "num_hidden_layers": 2}
     assert [w(llama, i) for i in range(2)] == [0, 0]
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes mirrors of da_layer and da_rope_scaling have the header's size and field offsets (a C
+    program built from include/decattn.h prints them)."""
+    import shutil
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    structs = {"da_layer": _abi.DaLayer, "da_rope_scaling": _abi.DaRopeScaling}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "decattn.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    cuda_inc = os.environ.get("CUDA_HOME", "/usr/local/cuda") + "/include"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    got = {}
+    for ln in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        cname, fname, val = ln.split()
+        got[(cname, fname)] = int(val)
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)

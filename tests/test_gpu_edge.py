@@ -46,7 +46,7 @@ def _close(got, ref, fp32=False):
 
 
 def _prefill_call(lens, first_pos, hq=8, hkv=2, d=128, window=0, softcap=0.0, dtype=torch.bfloat16, seed=5,
-                  M=None, rot=None):
+                  M=None, rot=None, sinks=None, rope_scaling=None, theta=1e4, max_pos=None):
     """A prefill-only call with random caches for the positions before each chunk."""
     from decoder_attention_gb300 import inputs
     g = torch.Generator().manual_seed(seed)
@@ -60,8 +60,9 @@ def _prefill_call(lens, first_pos, hq=8, hkv=2, d=128, window=0, softcap=0.0, dt
     vc = torch.randn((R, hkv, M, d), generator=g).to(dtype)
     qs, tr, tp, tl = inputs._prefill_meta(lens, first_pos, list(range(R)))
     return inputs.LayerCall(head_dim=d, num_attention_heads=hq, num_key_value_heads=hkv,
-                            partial_rotary_factor=(rot or d) / d, rope_theta=1e4, rope_scaling=None,
-                            max_position_embeddings=M, dtype=dtype, window=window, softcap=softcap,
+                            partial_rotary_factor=(rot or d) / d, rope_theta=theta, rope_scaling=rope_scaling,
+                            max_position_embeddings=max_pos or M, dtype=dtype, window=window, softcap=softcap,
+                            sinks=sinks,
                             q=q, k=k, v=v, tok_rows=inputs._i32(tr), tok_pos=inputs._i32(tp),
                             tok_seq_len=inputs._i32(tl), n_prefill=n, q_start=inputs._i32(qs),
                             pf_rows=inputs._i32(list(range(R))), pf_first_pos=inputs._i32(first_pos),
@@ -69,7 +70,7 @@ def _prefill_call(lens, first_pos, hq=8, hkv=2, d=128, window=0, softcap=0.0, dt
                             k_cache=kc, v_cache=vc)
 
 
-def _decode_call(lens, hq=8, hkv=2, d=128, window=0, dtype=torch.bfloat16, seed=6):
+def _decode_call(lens, hq=8, hkv=2, d=128, window=0, dtype=torch.bfloat16, seed=6, sinks=None, softcap=0.0):
     from decoder_attention_gb300 import inputs
     g = torch.Generator().manual_seed(seed)
     S = len(lens)
@@ -83,7 +84,7 @@ def _decode_call(lens, hq=8, hkv=2, d=128, window=0, dtype=torch.bfloat16, seed=
     rows = list(range(S))
     return inputs.LayerCall(head_dim=d, num_attention_heads=hq, num_key_value_heads=hkv, partial_rotary_factor=1.0,
                             rope_theta=1e4, rope_scaling=None, max_position_embeddings=M, dtype=dtype,
-                            window=window, q=q, k=k, v=v, tok_rows=inputs._i32(rows), tok_pos=inputs._i32(pos),
+                            window=window, softcap=softcap, sinks=sinks, q=q, k=k, v=v, tok_rows=inputs._i32(rows), tok_pos=inputs._i32(pos),
                             tok_seq_len=inputs._i32(lens), n_prefill=0, q_start=inputs._i32([0]),
                             pf_rows=inputs._i32([]), pf_first_pos=inputs._i32([]), max_q_len=0,
                             dec_rows=inputs._i32(rows), dec_pos=inputs._i32(pos), k_cache=kc, v_cache=vc)
@@ -270,3 +271,75 @@ def test_more_chunk_tiles_than_the_schedule_table(cuda):
     ref = ostep.run_layer_call(call)["out"]
     st, _ = _run(call, cuda)
     _close(st.out, ref)
+
+
+def _sinks(hq, seed):
+    """Learned sink logits for hq heads: N(0, 2) with one far above every score and one far below."""
+    g = torch.Generator().manual_seed(seed)
+    s = torch.randn(hq, generator=g) * 2
+    s[0] = 30.0
+    s[-1] = -40.0
+    return s
+
+
+@pytest.mark.parametrize("window,cap", [(0, 0.0), (200, 0.0), (0, 30.0)])
+def test_prefill_with_sinks(cuda, window, cap):
+    """Learned sinks on the tensor-core prefill: one extra logit per head whose share reaches no value,
+    with a window (the sink is seen whatever the window) and with a soft-cap (the sink is not capped)."""
+    lens, fps = [300, 129, 40], [0, 500, 77]
+    call = _prefill_call(lens, fps, hq=8, hkv=2, window=window, softcap=cap, seed=31, sinks=_sinks(8, 1))
+    ref = ostep.run_layer_call(call)["out"]
+    st, _ = _run(call, cuda)
+    _close(st.out, ref)
+
+
+@pytest.mark.parametrize("window", [0, 1000])
+def test_decode_with_sinks(cuda, window):
+    """Learned sinks on the split-K decode: the sink joins the merge of the per-chunk partials."""
+    call = _decode_call([5000, 1, 2047, 300], hq=8, hkv=2, window=window, seed=32, sinks=_sinks(8, 2))
+    ref = ostep.run_layer_call(call)["out"]
+    st, _ = _run(call, cuda)
+    _close(st.out, ref)
+
+
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_sinks_on_the_generic_path(cuda, kind):
+    """fp32 and head_dim 64 go through the CUDA-core kernel; its sinks follow the same definition."""
+    if kind == "prefill":
+        call = _prefill_call([70, 33], [0, 40], hq=4, hkv=2, d=64, seed=33, sinks=_sinks(4, 3))
+    else:
+        call = _decode_call([900, 3], hq=4, hkv=2, dtype=torch.float32, seed=34, sinks=_sinks(4, 4))
+    ref = ostep.run_layer_call(call)["out"]
+    st, _ = _run(call, cuda)
+    _close(st.out, ref, fp32=call.dtype == torch.float32)
+
+
+YARN = {"rope_type": "yarn", "factor": 32.0, "original_max_position_embeddings": 4096, "beta_fast": 32.0,
+        "beta_slow": 1.0}
+
+
+@pytest.mark.parametrize("window,truncate", [(128, False), (0, True)])
+def test_yarn_prefill_with_sinks(cuda, window, truncate):
+    """A GPT-OSS-style layer (page "Model resolution", gpt_oss: YaRN rotation, a learned sink per head, layers
+    alternating a 128-key window and full attention) at positions far past the original context: YaRN's
+    ramp and attention factor in the tables, then the tensor-core prefill with sinks."""
+    sc = dict(YARN, truncate=truncate)
+    call = _prefill_call([100, 37], [9000, 0], hq=8, hkv=2, window=window, seed=41, sinks=_sinks(8, 5),
+                         rope_scaling=sc, theta=150000.0, max_pos=131072)
+    res = ostep.run_layer_call(call)
+    st, _ = _run(call, cuda)
+    n = call.n_tokens
+    np.testing.assert_allclose(st.cos[:n].double().cpu().numpy(), res["cos"], atol=5e-7, rtol=0)
+    np.testing.assert_allclose(st.sin[:n].double().cpu().numpy(), res["sin"], atol=5e-7, rtol=0)
+    _close(st.out, res["out"])
+
+
+def test_yarn_mscale_ratio_decode(cuda):
+    """YaRN with mscale and mscale_all_dim both set (the attention factor is their ratio) on the decode path."""
+    sc = dict(YARN, mscale=0.707, mscale_all_dim=0.707 * 1.5)
+    call = _decode_call([30000, 5000], hq=8, hkv=2, seed=42, sinks=_sinks(8, 6))
+    call.rope_scaling, call.rope_theta, call.max_position_embeddings = sc, 150000.0, 131072
+    res = ostep.run_layer_call(call)
+    st, _ = _run(call, cuda)
+    np.testing.assert_allclose(st.cos[:2].double().cpu().numpy(), res["cos"], atol=5e-7, rtol=0)
+    _close(st.out, res["out"])
