@@ -23,7 +23,7 @@ Where the pages leave a step open the oracle takes one reading; each is named wh
   R7  a query with no allowed key gets output 0.
   R8  a window of w admits w keys including the query's own: key position j is allowed for a query at
       position p iff j <= p and p - j <= w - 1 (w = 0: no window).
-  R9  a learned sink (page "Model resolution", gpt_oss entry: one extra logit per head in every query's
+  R16 a learned sink (page "Model resolution", gpt_oss entry: one extra logit per head in every query's
       softmax whose share is dropped) is a logit in the units of the scaled scores, after any soft-cap and
       not capped itself, seen by every query whatever its window; its probability multiplies no value.
 
@@ -203,7 +203,7 @@ def causal_attention(q, k, v, q_pos, k_pos, window=0, softcap=0.0, scale=None, s
     1/sqrt(d) by default (page 3 §3.4); soft-capped by cap * tanh(z / cap) when softcap > 0 (R5);
     softmax over the allowed keys only (page 3 §2.3: a masked logit is -inf, probability 0); output
     0 for a query that sees no key (R7). With sinks [Hq], head h's softmax also takes the logit sinks[h],
-    whose probability is dropped (R9). Returns float64 [T, Hq, d].
+    whose probability is dropped (R16). Returns float64 [T, Hq, d].
     """
     q = np.asarray(q, dtype=F64)
     k = np.asarray(k, dtype=F64)
@@ -257,7 +257,7 @@ class Layer:
     window: int = 0                         # 0: full attention
     softcap: float = 0.0                    # 0: off
     scale: float = 0.0                      # 0: 1/sqrt(head_dim)
-    sinks: np.ndarray | None = None         # [Hq] learned sink logits (R9), or None
+    sinks: np.ndarray | None = None         # [Hq] learned sink logits (R16), or None
 
 
 @dataclass
