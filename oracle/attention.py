@@ -23,6 +23,10 @@ Where the pages leave a step open the oracle takes one reading; each is named wh
   R7  a query with no allowed key gets output 0.
   R8  a window of w admits w keys including the query's own: key position j is allowed for a query at
       position p iff j <= p and p - j <= w - 1 (w = 0: no window).
+  R17 paged cache: position p of cache row `row` lives in pool block block_table[row, p // block_size] at
+      offset p % block_size (page 1 "Sliding windows" names the engine's blocks and block tables but not
+      their layout); a block that lies wholly before the first position a call's oldest query can see is
+      never read, so it may be recycled (its table slot -1).
   R16 a learned sink (page "Model resolution", gpt_oss entry: one extra logit per head in every query's
       softmax whose share is dropped) is a logit in the units of the scaled scores, after any soft-cap and
       not capped itself, seen by every query whatever its window; its probability multiplies no value.
@@ -363,3 +367,88 @@ def attn_decode_one(layer: Layer, q_vec, k_row, v_row, p):
     kp = np.arange(lo, p + 1)
     return causal_attention(np.asarray(q_vec, dtype=F64)[None], k_row[:, lo:p + 1], v_row[:, lo:p + 1],
                             [p], kp, layer.window, layer.softcap, layer.scale, layer.sinks)[0]
+
+
+# --------------------------------------------------------------------------------------------------
+# Paged KV cache  (page 1 "Sliding windows": the engine's cache is a pool of fixed-size blocks that each
+# request maps through its own block table, and blocks that every query has moved past can be recycled)
+# --------------------------------------------------------------------------------------------------
+
+def paged_view(pool, block_table, block_size, row, lo, hi):
+    """Keys (or values) of positions lo .. hi-1 of cache row `row`, [Hkv, hi - lo, d] float64.
+
+    pool [n_blocks, Hkv, block_size, d]; block_table [R, max_blocks] int (-1 = no block). Position p of the
+    row lives at pool[block_table[row, p // block_size], :, p % block_size]. A position whose block is not
+    mapped raises: nothing the step reads may be unmapped."""
+    pool = np.asarray(pool)
+    hkv, d = pool.shape[1], pool.shape[3]
+    out = np.empty((hkv, max(hi - lo, 0), d), dtype=F64)
+    for p in range(lo, hi):
+        b = int(block_table[row][p // block_size])
+        if b < 0:
+            raise ValueError(f"position {p} of row {row} has no block")
+        out[:, p - lo] = pool[b, :, p % block_size]
+    return out
+
+
+def kv_cache_update_paged(layer: Layer, q, k, v, rows, positions, cos, sin, k_pool, v_pool, block_table,
+                          block_size):
+    """kv_cache_update with the cache slot of (row, position) found through the row's block table."""
+    q = np.asarray(q, dtype=F64)
+    k = np.asarray(k, dtype=F64)
+    if layer.q_norm_w is not None:
+        q = rms_norm(q, layer.q_norm_w, layer.eps)
+        k = rms_norm(k, layer.k_norm_w, layer.eps)
+    c = np.asarray(cos, dtype=F64)[:, None, :]
+    s = np.asarray(sin, dtype=F64)[:, None, :]
+    q_rot = apply_rope(q, c, s)
+    k_rot = apply_rope(k, c, s)
+    for t in range(q.shape[0]):
+        p = int(positions[t])
+        b = int(block_table[rows[t]][p // block_size])
+        if b < 0:
+            raise ValueError(f"position {p} of row {rows[t]} has no block")
+        k_pool[b, :, p % block_size, :] = k_rot[t]
+        v_pool[b, :, p % block_size, :] = np.asarray(v[t], dtype=F64)
+    return q_rot
+
+
+def _first_visible(first_pos, window):
+    """Oldest position any query from first_pos on can see: keys before it are masked for all of them."""
+    return max(0, first_pos - window + 1) if window else 0
+
+
+def attn_prefill_paged(layer: Layer, q_rot, k_pool, v_pool, block_table, block_size, q_start, rows, first_pos):
+    """attn_prefill over a paged cache: chunk b sees positions lo .. first_pos[b] + n_b - 1 of its row, lo
+    the first position its oldest query can see (blocks wholly before lo may be unmapped)."""
+    q_rot = np.asarray(q_rot, dtype=F64)
+    out = np.zeros_like(q_rot)
+    for b in range(len(rows)):
+        t0, t1 = int(q_start[b]), int(q_start[b + 1])
+        if t1 <= t0:
+            continue
+        fp = int(first_pos[b])
+        qp = fp + np.arange(t1 - t0)
+        kv_len = fp + (t1 - t0)
+        lo = _first_visible(fp, layer.window)
+        row = int(rows[b])
+        kk = paged_view(k_pool, block_table, block_size, row, lo, kv_len)
+        vv = paged_view(v_pool, block_table, block_size, row, lo, kv_len)
+        out[t0:t1] = causal_attention(q_rot[t0:t1], kk, vv, qp, np.arange(lo, kv_len), layer.window, layer.softcap,
+                                      layer.scale, layer.sinks)
+    return out
+
+
+def attn_decode_paged(layer: Layer, q_rot, k_pool, v_pool, block_table, block_size, rows, positions):
+    """attn_decode over a paged cache: the token at position p of row rows[s] sees positions lo .. p."""
+    q_rot = np.asarray(q_rot, dtype=F64)
+    out = np.zeros_like(q_rot)
+    for s in range(len(rows)):
+        p, row = int(positions[s]), int(rows[s])
+        lo = _first_visible(p, layer.window)
+        kk = paged_view(k_pool, block_table, block_size, row, lo, p + 1)
+        vv = paged_view(v_pool, block_table, block_size, row, lo, p + 1)
+        out[s:s + 1] = causal_attention(q_rot[s:s + 1], kk, vv, [p], np.arange(lo, p + 1), layer.window,
+                                        layer.softcap, layer.scale, layer.sinks)
+    return out
+
