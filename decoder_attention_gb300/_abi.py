@@ -53,6 +53,12 @@ class DaLayer(ctypes.Structure):
                 ("sinks", ctypes.c_void_p)]
 
 
+class DaPagedKv(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("n_blocks", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("block_table", ctypes.c_void_p), ("num_rows", ctypes.c_int),
+                ("max_blocks", ctypes.c_int)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
@@ -66,6 +72,12 @@ def _load():
         "da_decode_workspace_bytes": (Z, [ctypes.POINTER(DaLayer), I, I]),
         "da_attn_decode_noalloc": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, I, P, P, P, P, P]),
         "da_decode_noalloc_max_scratch_bytes": (Z, []),
+        "da_kv_cache_update_paged": (I, [ctypes.POINTER(DaLayer), P, P, P, I, P, P, P, P, P,
+                                         ctypes.POINTER(DaPagedKv), P]),
+        "da_attn_prefill_paged": (I, [ctypes.POINTER(DaLayer), P, I, ctypes.POINTER(DaPagedKv), I, P, P, P, I, P,
+                                      P]),
+        "da_attn_decode_paged": (I, [ctypes.POINTER(DaLayer), P, ctypes.POINTER(DaPagedKv), I, P, P, P, P, Z, P]),
+        "da_decode_workspace_bytes_paged": (Z, [ctypes.POINTER(DaLayer), I, I]),
         "da_check_device_error": (I, [P]),
         "da_last_error": (ctypes.c_char_p, []),
         "da_version": (I, []),
@@ -224,6 +236,41 @@ def decode_noalloc_max_scratch_bytes() -> int:
 
 def decode_workspace_bytes(L, n_seqs, max_len) -> int:
     return int(LIB.da_decode_workspace_bytes(ctypes.byref(L), int(n_seqs), int(max_len)))
+
+
+def paged_kv(k_pool, v_pool, block_table, block_size):
+    """DaPagedKv for device pools [n_blocks, Hkv, block_size, d] and an int32 block table [num_rows, max_blocks]
+    (keep the tensors alive while the struct is in use)."""
+    kv = DaPagedKv()
+    kv.k_pool = k_pool.data_ptr()
+    kv.v_pool = v_pool.data_ptr()
+    kv.n_blocks = int(k_pool.shape[0])
+    kv.block_size = int(block_size)
+    kv.block_table = block_table.data_ptr()
+    kv.num_rows = int(block_table.shape[0])
+    kv.max_blocks = int(block_table.shape[1])
+    return kv
+
+
+def kv_cache_update_paged(L, q, k, v, n, rows, positions, cos, sin, q_rot, kv, stream=None):
+    _check(LIB.da_kv_cache_update_paged(ctypes.byref(L), _ptr(q), _ptr(k), _ptr(v), int(n), _ptr(rows),
+                                        _ptr(positions), _ptr(cos), _ptr(sin), _ptr(q_rot), ctypes.byref(kv),
+                                        _stream(stream)))
+
+
+def attn_prefill_paged(L, q_rot, n_tokens, kv, n_seqs, q_start, rows, first_pos, max_q_len, out, stream=None):
+    _check(LIB.da_attn_prefill_paged(ctypes.byref(L), _ptr(q_rot), int(n_tokens), ctypes.byref(kv), int(n_seqs),
+                                     _ptr(q_start), _ptr(rows), _ptr(first_pos), int(max_q_len), _ptr(out),
+                                     _stream(stream)))
+
+
+def attn_decode_paged(L, q_rot, kv, n_seqs, rows, positions, out, workspace, ws_bytes, stream=None):
+    _check(LIB.da_attn_decode_paged(ctypes.byref(L), _ptr(q_rot), ctypes.byref(kv), int(n_seqs), _ptr(rows),
+                                    _ptr(positions), _ptr(out), _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def decode_workspace_bytes_paged(L, n_seqs, max_positions) -> int:
+    return int(LIB.da_decode_workspace_bytes_paged(ctypes.byref(L), int(n_seqs), int(max_positions)))
 
 
 def check_device_error(stream=None):

@@ -243,9 +243,38 @@ int da_rope_tables_build(const da_rope_scaling* rs, const int32_t* positions, co
   return ok();
 }
 
-int da_kv_cache_update(const da_layer* L, const void* q, const void* k, const void* v, int n, const int32_t* rows,
-                       const int32_t* positions, const float* cos, const float* sin, void* q_rot, void* k_cache,
-                       void* v_cache, int num_rows, int max_len, cudaStream_t stream) {
+// A paged pool's description, checked; fills the layout fields the kernels read.
+static int check_paged(const da_layer* L, const da_paged_kv* kv) {
+  if (!kv) return fail(DA_ERR_INVALID_ARG, "the paged pool description is NULL");
+  if (!kv->k_pool || !kv->v_pool || !kv->block_table) return fail(DA_ERR_INVALID_ARG, "a pool pointer is NULL");
+  if (kv->n_blocks < 1 || kv->block_size < 1 || kv->num_rows < 1 || kv->max_blocks < 1)
+    return fail(DA_ERR_INVALID_ARG, "n_blocks, block_size, num_rows and max_blocks must be >= 1");
+  if (static_cast<long long>(kv->max_blocks) * kv->block_size > 0x7fffffffLL)
+    return fail(DA_ERR_UNSUPPORTED, "max_blocks * block_size exceeds 2^31 positions");
+  if (static_cast<long long>(kv->n_blocks) * L->num_key_value_heads * kv->block_size > 0x7fffffffLL)
+    return fail(DA_ERR_UNSUPPORTED, "n_blocks * Hkv * block_size exceeds 2^31 key slots");
+  if (!aligned16(kv->k_pool) || !aligned16(kv->v_pool)) return fail(DA_ERR_INVALID_ARG, "the pools must be 16-byte aligned");
+  return DA_OK;
+}
+
+extern "C++" {
+template <typename Args>
+static void set_paged(Args& a, const da_paged_kv* kv) {
+  if (kv) {
+    a.block_table = kv->block_table;
+    a.block_size = kv->block_size;
+    a.max_blocks = kv->max_blocks;
+    a.n_blocks = kv->n_blocks;
+  } else {
+    a.block_table = nullptr;
+    a.block_size = a.max_blocks = a.n_blocks = 0;
+  }
+}
+}
+
+static int kv_update_impl(const da_layer* L, const void* q, const void* k, const void* v, int n, const int32_t* rows,
+                          const int32_t* positions, const float* cos, const float* sin, void* q_rot, void* k_cache,
+                          void* v_cache, int num_rows, int max_len, const da_paged_kv* kv, cudaStream_t stream) {
   int rc = check_layer(L);
   if (rc) return rc;
   if (n < 0) return fail(DA_ERR_INVALID_ARG, "n = %d < 0", n);
@@ -279,14 +308,35 @@ int da_kv_cache_update(const da_layer* L, const void* q, const void* k, const vo
   a.v_cache = v_cache;
   a.num_rows = num_rows;
   a.max_len = max_len;
+  set_paged(a, kv);
   a.err = err;
   cudaError_t e = da::launch_kv_update(a, L->dtype == DA_BF16, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kv_cache_update launch");
   return ok();
 }
 
+int da_kv_cache_update(const da_layer* L, const void* q, const void* k, const void* v, int n, const int32_t* rows,
+                       const int32_t* positions, const float* cos, const float* sin, void* q_rot, void* k_cache,
+                       void* v_cache, int num_rows, int max_len, cudaStream_t stream) {
+  return kv_update_impl(L, q, k, v, n, rows, positions, cos, sin, q_rot, k_cache, v_cache, num_rows, max_len, nullptr,
+                        stream);
+}
+
+int da_kv_cache_update_paged(const da_layer* L, const void* q, const void* k, const void* v, int n, const int32_t* rows,
+                             const int32_t* positions, const float* cos, const float* sin, void* q_rot,
+                             const da_paged_kv* kv, cudaStream_t stream) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n == 0) return ok();
+  rc = check_paged(L, kv);
+  if (rc) return rc;
+  return kv_update_impl(L, q, k, v, n, rows, positions, cos, sin, q_rot, kv->k_pool, kv->v_pool, kv->num_rows,
+                        kv->max_blocks * kv->block_size, kv, stream);
+}
+
 static int attn_common_checks(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache,
-                              int num_rows, int max_len, int n_seqs, const int32_t* rows, void* out) {
+                              int num_rows, int max_len, int n_seqs, const int32_t* rows, void* out,
+                              bool paged = false) {
   int rc = check_layer(L);
   if (rc) return rc;
   if (n_seqs < 0) return fail(DA_ERR_INVALID_ARG, "n_seqs = %d < 0", n_seqs);
@@ -294,7 +344,7 @@ static int attn_common_checks(const da_layer* L, const void* q_rot, const void* 
   if (n_seqs == 0) return DA_OK;
   if (!q_rot || !k_cache || !v_cache || !rows || !out) return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
-  if (static_cast<long long>(num_rows) * L->num_key_value_heads * max_len > 0x7fffffffLL)
+  if (!paged && static_cast<long long>(num_rows) * L->num_key_value_heads * max_len > 0x7fffffffLL)
     return fail(DA_ERR_UNSUPPORTED, "num_rows * Hkv * max_len exceeds 2^31 key slots");
   if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return fail(DA_ERR_INVALID_ARG, "q_rot, the caches and out must be 16-byte aligned");
@@ -326,13 +376,11 @@ static da::AttnArgs make_args(const da_layer* L, const void* q_rot, const void* 
   return a;
 }
 
-int da_attn_prefill(const da_layer* L, const void* q_rot, int n_tokens, const void* k_cache, const void* v_cache,
-                    int num_rows, int max_len, int n_seqs, const int32_t* q_start, const int32_t* rows,
-                    const int32_t* first_pos, int max_q_len, const int32_t* key_positions, void* out, void* workspace,
-                    size_t ws_bytes, cudaStream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
-  int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out);
+static int prefill_impl(const da_layer* L, const void* q_rot, int n_tokens, const void* k_cache, const void* v_cache,
+                        int num_rows, int max_len, int n_seqs, const int32_t* q_start, const int32_t* rows,
+                        const int32_t* first_pos, int max_q_len, const int32_t* key_positions, void* out,
+                        const da_paged_kv* kv, cudaStream_t stream) {
+  int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out, kv != nullptr);
   if (rc) return rc;
   if (n_tokens < 0 || max_q_len < 0) return fail(DA_ERR_INVALID_ARG, "n_tokens and max_q_len must be >= 0");
   if (n_seqs == 0 || n_tokens == 0 || max_q_len == 0) return ok();
@@ -344,10 +392,34 @@ int da_attn_prefill(const da_layer* L, const void* q_rot, int n_tokens, const vo
   a.first_pos = first_pos;
   a.max_q_len = max_q_len;
   a.n_tokens = n_tokens;
-  const bool fast = L->dtype == DA_BF16 && L->head_dim == 128 && key_positions == nullptr;
+  set_paged(a, kv);
+  const bool fast = L->dtype == DA_BF16 && L->head_dim == 128 && key_positions == nullptr &&
+                    (kv == nullptr || kv->block_size % 64 == 0);
   cudaError_t e = fast ? da::launch_prefill_bf16(a, stream) : da::launch_attn_generic(a, L->dtype == DA_BF16, stream);
   if (e != cudaSuccess) return cuda_fail(e, fast ? "prefill (tcgen05) launch" : "prefill (generic) launch");
   return ok();
+}
+
+int da_attn_prefill(const da_layer* L, const void* q_rot, int n_tokens, const void* k_cache, const void* v_cache,
+                    int num_rows, int max_len, int n_seqs, const int32_t* q_start, const int32_t* rows,
+                    const int32_t* first_pos, int max_q_len, const int32_t* key_positions, void* out, void* workspace,
+                    size_t ws_bytes, cudaStream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  return prefill_impl(L, q_rot, n_tokens, k_cache, v_cache, num_rows, max_len, n_seqs, q_start, rows, first_pos,
+                      max_q_len, key_positions, out, nullptr, stream);
+}
+
+int da_attn_prefill_paged(const da_layer* L, const void* q_rot, int n_tokens, const da_paged_kv* kv, int n_seqs,
+                          const int32_t* q_start, const int32_t* rows, const int32_t* first_pos, int max_q_len,
+                          void* out, cudaStream_t stream) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n_seqs == 0) return ok();
+  rc = check_paged(L, kv);
+  if (rc) return rc;
+  return prefill_impl(L, q_rot, n_tokens, kv->k_pool, kv->v_pool, kv->num_rows, kv->max_blocks * kv->block_size,
+                      n_seqs, q_start, rows, first_pos, max_q_len, nullptr, out, kv, stream);
 }
 
 static bool decode_fast(const da_layer* L, const int32_t* key_positions) {
@@ -358,14 +430,23 @@ static bool decode_fast(const da_layer* L, const int32_t* key_positions) {
 size_t da_decode_workspace_bytes(const da_layer* L, int n_seqs, int max_len) {
   if (check_layer(L) != DA_OK || n_seqs <= 0 || max_len <= 0) return 0;
   if (!decode_fast(L, nullptr)) return 0;
-  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window);
+  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window, false);
   return da::decode_workspace_bytes(L->num_attention_heads, n_seqs, p);
 }
 
-int da_attn_decode(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache, int num_rows,
-                   int max_len, int n_seqs, const int32_t* rows, const int32_t* positions,
-                   const int32_t* key_positions, void* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out);
+size_t da_decode_workspace_bytes_paged(const da_layer* L, int n_seqs, int max_positions) {
+  if (check_layer(L) != DA_OK || n_seqs <= 0 || max_positions <= 0) return 0;
+  if (!decode_fast(L, nullptr)) return 0;
+  // chunks start at the window start rounded down to a 64-key tile: up to 63 more keys per sequence
+  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_positions, L->window, true);
+  return da::decode_workspace_bytes(L->num_attention_heads, n_seqs, p);
+}
+
+static int decode_impl(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache, int num_rows,
+                       int max_len, int n_seqs, const int32_t* rows, const int32_t* positions,
+                       const int32_t* key_positions, void* out, void* workspace, size_t ws_bytes,
+                       const da_paged_kv* kv, cudaStream_t stream) {
+  int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out, kv != nullptr);
   if (rc) return rc;
   if (n_seqs == 0) return ok();
   if (!positions) return fail(DA_ERR_INVALID_ARG, "positions must be non-NULL");
@@ -375,12 +456,13 @@ int da_attn_decode(const da_layer* L, const void* q_rot, const void* k_cache, co
   a.positions = positions;
   a.max_q_len = 1;
   a.n_tokens = n_seqs;
-  if (!decode_fast(L, key_positions)) {
+  set_paged(a, kv);
+  if (!decode_fast(L, key_positions) || (kv && kv->block_size % 64 != 0)) {
     cudaError_t e = da::launch_attn_generic(a, L->dtype == DA_BF16, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode (generic) launch");
     return ok();
   }
-  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window);
+  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window, kv != nullptr);
   const size_t need = da::decode_workspace_bytes(L->num_attention_heads, n_seqs, p);
   if (!workspace || ws_bytes < need)
     return fail(DA_ERR_INVALID_ARG, "decode workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
@@ -388,6 +470,24 @@ int da_attn_decode(const da_layer* L, const void* q_rot, const void* k_cache, co
   cudaError_t e = da::launch_decode_bf16(a, p, workspace, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode (split-K) launch");
   return ok();
+}
+
+int da_attn_decode(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache, int num_rows,
+                   int max_len, int n_seqs, const int32_t* rows, const int32_t* positions,
+                   const int32_t* key_positions, void* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return decode_impl(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, positions, key_positions, out,
+                     workspace, ws_bytes, nullptr, stream);
+}
+
+int da_attn_decode_paged(const da_layer* L, const void* q_rot, const da_paged_kv* kv, int n_seqs, const int32_t* rows,
+                         const int32_t* positions, void* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n_seqs == 0) return ok();
+  rc = check_paged(L, kv);
+  if (rc) return rc;
+  return decode_impl(L, q_rot, kv->k_pool, kv->v_pool, kv->num_rows, kv->max_blocks * kv->block_size, n_seqs, rows,
+                     positions, nullptr, out, workspace, ws_bytes, kv, stream);
 }
 
 int da_attn_decode_noalloc(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache,
@@ -408,7 +508,7 @@ int da_attn_decode_noalloc(const da_layer* L, const void* q_rot, const void* k_c
     if (e != cudaSuccess) return cuda_fail(e, "decode (generic) launch");
     return ok();
   }
-  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window);
+  const da::DecodePlan p = da::decode_plan(L->num_key_value_heads, n_seqs, max_len, L->window, false);
   const size_t need = da::decode_workspace_bytes(L->num_attention_heads, n_seqs, p);
   if (need > da::kDecodeStaticScratchBytes)
     return fail(DA_ERR_INVALID_ARG,

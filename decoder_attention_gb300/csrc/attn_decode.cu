@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "kvmap.cuh"
 
 namespace da {
 namespace dec {
@@ -45,6 +46,8 @@ struct Params {
   int hq, hkv, max_len, num_rows, window;
   float softcap, scale;
   const float* sinks;   // [Hq] sink logits (natural units) or NULL
+  const int32_t* block_table;   // paged pool: [num_rows, max_blocks] block ids; NULL: contiguous cache
+  int block_size, max_blocks, n_blocks;
   int chunk, n_splits;
   int* err;
 };
@@ -83,10 +86,13 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c16) {
   return static_cast<uint32_t>((c16 >> 3) * HALF_BYTES + r * 128 + (((c16 & 7) ^ (r & 7)) << 4));
 }
 
-// Keys [lo, p] of the sequence are visible; the chunk c covers [lo + c*chunk, min(lo + (c+1)*chunk, p+1)).
-__device__ __forceinline__ void key_range(int p, int window, int& lo, int& n_keys) {
-  n_keys = window > 0 ? min(p + 1, window) : p + 1;
-  lo = p + 1 - n_keys;
+// Keys [lo, p] of the sequence are visible. Chunk c covers [base + c*chunk, min(base + (c+1)*chunk, p+1)):
+// base = lo for a contiguous cache; for a paged pool lo rounded down to a multiple of the 64-key tile, so
+// that a tile never straddles two blocks (block sizes are multiples of 64), the keys below lo masked.
+__device__ __forceinline__ void key_range(int p, int window, bool paged, int& lo, int& base, int& n_span) {
+  lo = window > 0 ? max(0, p + 1 - window) : 0;
+  base = paged ? (lo & ~(BK - 1)) : lo;
+  n_span = p + 1 - base;
 }
 
 template <int NST>
@@ -105,9 +111,9 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const __grid_constant__
     if (threadIdx.x == 0 && c == 0 && g == 0) set_error(prm.err, kErrIndex);
     return;   // the merge kernel writes zeros for this sequence
   }
-  int lo, n_keys;
-  key_range(p, prm.window, lo, n_keys);
-  const int k0 = lo + c * prm.chunk;
+  int lo, base, n_span;
+  key_range(p, prm.window, prm.block_table != nullptr, lo, base, n_span);
+  const int k0 = base + c * prm.chunk;
   if (k0 > p) return;                       // this sequence has fewer chunks
   const int k1 = min(k0 + prm.chunk, p + 1);
   const int n_tiles = (k1 - k0 + BK - 1) / BK;
@@ -133,14 +139,25 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const __grid_constant__
       prefetch_tmap(&tmk);
       prefetch_tmap(&tmv);
       const uint64_t pol = policy_evict_first();
-      const int plane = (row * prm.hkv + g) * prm.max_len;
+      const KvLayout kvl = kv_layout(prm);
+      const long long plane = (static_cast<long long>(row) * prm.hkv + g) * prm.max_len;   // contiguous
+      const long long head_off = g * kv_head_stride(kvl);                                    // paged
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int st = i % NST;
         if (i >= NST && !mbar_wait(empty_bar(st), ((i / NST) + 1) & 1, prm.err)) break;
         const uint32_t dst = sbase + st * STAGE_BYTES;
         mbar_arrive_expect_tx(full_bar(st), STAGE_BYTES);
-        const int key = plane + k0 + i * BK;
+        long long slot = plane + k0 + i * BK;
+        if (prm.block_table) {   // the tile's 64 keys lie in one block
+          slot = kv_slot(kvl, row, k0 + i * BK);
+          if (slot < 0) {        // no block: reported; a slot inside the pool keeps the copy's byte count
+            set_error(prm.err, kErrIndex);
+            slot = 0;
+          }
+          slot += head_off;
+        }
+        const int key = static_cast<int>(slot);
         tma_load_2d_hint(dst, &tmk, full_bar(st), 0, key, pol);
         tma_load_2d_hint(dst + HALF_BYTES, &tmk, full_bar(st), 64, key, pol);
         tma_load_2d_hint(dst + TILE_BYTES, &tmv, full_bar(st), 0, key, pol);
@@ -184,6 +201,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const __grid_constant__
     const uint32_t sV = sK + TILE_BYTES;
     const int kb = k0 + i * BK + warp * 16;        // first key of this warp's 16
     const int n_valid = k1 - kb;                   // keys of the 16 that are in the chunk (may be <= 0)
+    const int n_lo = lo - kb;                      // keys of the 16 below the window (paged tiles only)
 
     // S^T[16 keys x 8 heads]
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -198,7 +216,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const __grid_constant__
       }
     }
     // logits in log2 units, masked
-    const bool v0 = gq < n_valid, v1 = gq + 8 < n_valid;
+    const bool v0 = gq >= n_lo && gq < n_valid, v1 = gq + 8 >= n_lo && gq + 8 < n_valid;
     float z[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -239,10 +257,11 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const __grid_constant__
     {
       const int mi = lane >> 3, r8 = lane & 7;
       const int vr = warp * 16 + (mi >> 1) * 8 + r8;
-      const bool partial = n_valid < 16;
+      const bool partial = n_valid < 16 || n_lo > 0;
       // keys this thread's A-fragment halves belong to: 2cq, 2cq+1 (regs 0,1) and 8+2cq, 9+2cq (regs 2,3)
-      const uint32_t keep01 = (2 * cq < n_valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < n_valid ? 0xffff0000u : 0u);
-      const uint32_t keep23 = (2 * cq + 8 < n_valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < n_valid ? 0xffff0000u : 0u);
+      auto in = [&](int k) { return k >= n_lo && k < n_valid; };
+      const uint32_t keep01 = (in(2 * cq) ? 0x0000ffffu : 0u) | (in(2 * cq + 1) ? 0xffff0000u : 0u);
+      const uint32_t keep23 = (in(2 * cq + 8) ? 0x0000ffffu : 0u) | (in(2 * cq + 9) ? 0xffff0000u : 0u);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t a0, a1, a2, a3;
@@ -315,9 +334,9 @@ __global__ void __launch_bounds__(D) merge_kernel(const Params prm) {
     out[dd] = __float2bfloat16_rn(0.f);
     return;
   }
-  int lo, n_keys;
-  key_range(p, prm.window, lo, n_keys);
-  const int n_spl = (n_keys + prm.chunk - 1) / prm.chunk;
+  int lo, k_base, n_span;
+  key_range(p, prm.window, prm.block_table != nullptr, lo, k_base, n_span);
+  const int n_spl = (n_span + prm.chunk - 1) / prm.chunk;
   const long long base = (static_cast<long long>(s) * prm.hq + h) * prm.n_splits;
   float M = -CUDART_INF_F;
   for (int c = 0; c < n_spl; ++c) M = fmaxf(M, prm.ws_ml[base + c].x);
@@ -356,9 +375,10 @@ void* static_scratch() {
   return ptrs[dev];
 }
 
-DecodePlan decode_plan(int hkv, int n_seqs, int max_len, int window) {
+DecodePlan decode_plan(int hkv, int n_seqs, int max_len, int window, bool aligned) {
   DecodePlan p;
-  const int max_keys = window > 0 ? std::min(window, max_len) : max_len;
+  // keys a chunk sequence spans at most (aligned: from the window start rounded down to a 64-key tile)
+  const int max_keys = (window > 0 ? std::min(window, max_len) : max_len) + (aligned ? dec::BK - 1 : 0);
   int chunk = 512;
   const char* env = std::getenv("DA_DECODE_CHUNK");   // tuning override (multiple of 64)
   if (env && std::atoi(env) >= 64 && std::atoi(env) % 64 == 0) {
@@ -385,7 +405,8 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const DecodePlan& plan, void* 
   if (a.n_seqs == 0) return cudaSuccess;
   constexpr int NST = 3;
   CUtensorMap tmk, tmv;
-  const uint64_t rows_total = static_cast<uint64_t>(a.num_rows) * a.hkv * a.max_len;
+  const uint64_t rows_total = a.block_table ? static_cast<uint64_t>(a.n_blocks) * a.hkv * a.block_size
+                                            : static_cast<uint64_t>(a.num_rows) * a.hkv * a.max_len;
   if (!encode_tmap_2d_bf16(&tmk, a.k_cache, D, rows_total, D * 2, 64, BK) ||
       !encode_tmap_2d_bf16(&tmv, a.v_cache, D, rows_total, D * 2, 64, BK))
     return cudaErrorInvalidValue;
@@ -404,6 +425,10 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const DecodePlan& plan, void* 
   prm.window = a.window;
   prm.softcap = a.softcap;
   prm.sinks = a.sinks;
+  prm.block_table = a.block_table;
+  prm.block_size = a.block_size;
+  prm.max_blocks = a.max_blocks;
+  prm.n_blocks = a.n_blocks;
   prm.scale = a.scale;
   prm.chunk = plan.chunk;
   prm.n_splits = plan.n_splits;

@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "kvmap.cuh"
 
 namespace da {
 
@@ -65,9 +66,11 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
 #pragma unroll
   for (int j = 0; j < PER; ++j) q[j] = ld_elem<T>(qv + lane + 32 * j);
 
-  const long long plane = (static_cast<long long>(row) * a.hkv + g) * a.max_len;
-  const T* kb = static_cast<const T*>(a.k_cache) + plane * D;
-  const T* vb = static_cast<const T*>(a.v_cache) + plane * D;
+  const KvLayout kvl = kv_layout(a);
+  const long long plane = (static_cast<long long>(row) * a.hkv + g) * a.max_len;   // contiguous caches
+  const long long head_off = g * kv_head_stride(kvl);                                   // paged pools
+  const T* kb = static_cast<const T*>(a.k_cache);
+  const T* vb = static_cast<const T*>(a.v_cache);
   const float scale = a.scale;
 
   int j_lo = 0, j_hi;
@@ -89,7 +92,16 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
       const int kpos = kp[j];
       if (kpos < 0 || kpos > p || (a.window > 0 && p - kpos > a.window - 1)) continue;
     }
-    const T* kr = kb + static_cast<long long>(j) * D;
+    long long kslot = plane + j;
+    if (a.block_table) {
+      kslot = kv_slot(kvl, row, j);
+      if (kslot < 0) {   // a visible position without a block: reported, and left out
+        if (lane == 0) set_error(a.err, kErrIndex);
+        continue;
+      }
+      kslot += head_off;
+    }
+    const T* kr = kb + kslot * D;
     float dot = 0.f;
 #pragma unroll
     for (int e = 0; e < PER; ++e) dot = fmaf(q[e], ld_elem<T>(kr + lane + 32 * e), dot);
@@ -101,7 +113,7 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
     const float alpha = __expf(m - m_new);   // m = -inf on the first key: alpha = 0
     const float pj = __expf(z - m_new);
     l = l * alpha + pj;
-    const T* vr = vb + static_cast<long long>(j) * D;
+    const T* vr = vb + kslot * D;
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = fmaf(pj, ld_elem<T>(vr + lane + 32 * e), acc[e] * alpha);
     m = m_new;

@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "kvmap.cuh"
 
 namespace da {
 namespace pf {
@@ -95,6 +96,9 @@ struct Params {
   int hpair;   // 1: an item is 128 rows of two query heads sharing a KV head; 0: 256 rows of one head
   float softcap, scale;
   const float* sinks;   // [Hq] sink logits (natural units) or NULL
+  const int32_t* block_table;   // paged pool: [num_rows, max_blocks] block ids; NULL: contiguous cache
+  int block_size, max_blocks, n_blocks;
+  int kbox;             // key rows per K/V box: BN, or 64 for pools whose blocks are not multiples of BN
   int* err;
 };
 
@@ -104,7 +108,7 @@ struct Item {
   int n_b;     // chunk length
   int q0;      // first chunk row of the item
   int fp;      // position of the chunk's first token
-  int plane;   // cache row index of (row, kv head, position 0)
+  int plane;   // contiguous cache: row index of (row, kv head, position 0); paged pool: row * Hkv + kv head
   int h;       // query head
   int kind;    // kEnd, kLive, kBad
   int round0;  // global round of the item's first key tile (rounds count the CTA's key tiles in order)
@@ -282,6 +286,9 @@ struct IssItem {
   int q0, q1;   // Q tile sequence numbers (buffer = q % NQB)
 };
 
+// PAGED: keys come from a paged pool through the block table (a separate instantiation, so that the
+// contiguous form carries none of the lookups).
+template <bool PAGED>
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmq,
                                                              const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
@@ -318,6 +325,48 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const volatile int* vabort = &abort_flag;
+
+  // Cache row of key `key` of an item's plane: contiguous caches number rows plane + key; paged pools look
+  // the key's block up (a K/V box of kbox rows never straddles two blocks); -1 when the block is missing.
+  const KvLayout kvl = kv_layout(prm);
+  auto key_row = [&](int plane, int key) -> int {
+    if constexpr (!PAGED) return plane + key;
+    const int row = plane / prm.hkv, g = plane - row * prm.hkv;
+    const long long s = kv_slot(kvl, row, key);
+    return s < 0 ? -1 : static_cast<int>(s + static_cast<long long>(g) * prm.block_size);
+  };
+  // One 128-key K or V tile (two 64-column halves, 128-byte swizzled) from boxes of kbox key rows, armed on
+  // `bar` for the bytes it copies. A box wholly before the item's first visible key whose block is gone (a
+  // pool that recycles out-of-window blocks) is skipped: its keys are masked for every query of the item
+  // and the softmax warps zero its V rows. Any other missing block is reported and read from row 0, so
+  // that the copy still delivers the bytes its barrier expects.
+  auto load_kv_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int plane, int key, int first_vis) {
+    if constexpr (!PAGED) {
+      const int r = plane + key;
+      mbar_arrive_expect_tx(bar, TILE);
+      tma_load_2d(dst, tm, bar, 0, r);
+      tma_load_2d(dst + HALF, tm, bar, 64, r);
+    } else {
+      int rows[BN / 64];
+      uint32_t bytes = 0;
+      for (int j = 0, b = 0; j < BN; j += prm.kbox, ++b) {
+        rows[b] = key_row(plane, key + j);
+        if (rows[b] < 0 && key + j + prm.kbox > first_vis) {
+          set_error(prm.err, kErrIndex);
+          rows[b] = 0;
+        }
+        if (rows[b] >= 0) bytes += prm.kbox * 2 * 128;
+      }
+      mbar_arrive_expect_tx(bar, bytes);
+      for (int j = 0, b = 0; j < BN; j += prm.kbox, ++b) {
+        if (rows[b] < 0) continue;
+        tma_load_2d(dst + j * 128, tm, bar, 0, rows[b]);
+        tma_load_2d(dst + HALF + j * 128, tm, bar, 64, rows[b]);
+      }
+    }
+  };
+  // first key any query of an item sees (keys before it are masked for all of its rows)
+  auto first_visible = [&](const Item& it) { return window > 0 ? max(0, it.fp + it.q0 - window + 1) : 0; };
 
   // item-ring reader (one thread): waits for entry e, copies it, releases it
   auto get_item = [&](int e, Item& it) -> bool {
@@ -431,7 +480,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           it.h = h;
           const bool bad = row < 0 || row >= prm.num_rows || it.fp < 0 || it.fp + it.n_b > prm.max_len;
           it.kind = bad ? kBad : kLive;
-          it.plane = bad ? 0 : (row * prm.hkv + h / (prm.hq / prm.hkv)) * prm.max_len;
+          it.plane = bad ? 0 : (row * prm.hkv + h / (prm.hq / prm.hkv)) * (PAGED ? 1 : prm.max_len);
           it.round0 = rounds;
           if (!bad) rounds += tiles_of(it, window, hpair).n;
           ok = put(it);
@@ -465,14 +514,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         ++qn;
         return true;
       };
-      auto fill_k = [&](int key) -> bool {   // key < 0: the slot has no K tile
+      auto fill_k = [&](int plane, int key, int first_vis) -> bool {   // plane < 0: the slot has no K tile
         const int st = kj % NS;
         if (kj >= NS && !mbar_wait(B(B_EM + st), ((kj / NS) - 1) & 1, prm.err)) return false;
-        if (key >= 0) {
-          const uint32_t dst = sbase + OFF_R + st * 2 * TILE;
-          mbar_arrive_expect_tx(B(B_FU + st), TILE);
-          tma_load_2d(dst, &tmk, B(B_FU + st), 0, key);
-          tma_load_2d(dst + HALF, &tmk, B(B_FU + st), 64, key);
+        if (plane >= 0) {
+          load_kv_tile(sbase + OFF_R + st * 2 * TILE, &tmk, B(B_FU + st), plane, key, first_vis);
         } else {
           mbar_arrive(B(B_FU + st));
         }
@@ -492,11 +538,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           tma_prefetch_3d(&tmq, 0, hd, tok);
           tma_prefetch_3d(&tmq, 64, hd, tok);
         }
-        const int key = nx.plane + T.tb0 * BN;
-        tma_prefetch_2d(&tmk, 0, key);
-        tma_prefetch_2d(&tmk, 64, key);
-        tma_prefetch_2d(&tmv, 0, key);
-        tma_prefetch_2d(&tmv, 64, key);
+        const int key = key_row(nx.plane, first_visible(nx) / prm.kbox * prm.kbox);
+        if (key >= 0) {
+          tma_prefetch_2d(&tmk, 0, key);
+          tma_prefetch_2d(&tmk, 64, key);
+          tma_prefetch_2d(&tmv, 0, key);
+          tma_prefetch_2d(&tmv, 64, key);
+        }
         return true;
       };
       for (int e = 0; ok; ++e) {
@@ -508,11 +556,12 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const Tiles T = tiles_of(it, window, hpair);
         if (!load_q(it, 0)) { ok = false; break; }
         for (int i = 0; ok && i < T.n; ++i) {
-          if (*vabort || (i == 1 && T.valid1 && !load_q(it, 1)) || !fill_k(it.plane + (T.tb0 + i) * BN)) ok = false;
+          if (*vabort || (i == 1 && T.valid1 && !load_q(it, 1)) || !fill_k(it.plane, (T.tb0 + i) * BN, first_visible(it)))
+            ok = false;
         }
         if (ok && T.n == 1 && T.valid1 && !load_q(it, 1)) ok = false;
       }
-      if (ok && !fill_k(-1)) ok = false;
+      if (ok && !fill_k(-1, 0, 0)) ok = false;
       if (!ok) abort_flag = 1;
       // every issued copy must land before the CTA's shared memory is released
       for (int j = max(0, qn - NQB); j < qn; ++j) mbar_wait(B(B_QF + j % NQB), (j / NQB) & 1, prm.err);
@@ -523,21 +572,18 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       prefetch_tmap(&tmv);
       int vj = 0;
       bool ok = true;
-      auto fill_v = [&](int key) -> bool {
+      auto fill_v = [&](int plane, int key, int first_vis) -> bool {   // plane < 0: the slot has no V tile
         const int st = vj % NS;
         if (vj >= NS && !mbar_wait(B(B_EM + st), ((vj / NS) - 1) & 1, prm.err)) return false;
-        if (key >= 0) {
-          const uint32_t dst = sbase + OFF_R + st * 2 * TILE + TILE;
-          mbar_arrive_expect_tx(B(B_FU + st), TILE);
-          tma_load_2d(dst, &tmv, B(B_FU + st), 0, key);
-          tma_load_2d(dst + HALF, &tmv, B(B_FU + st), 64, key);
+        if (plane >= 0) {
+          load_kv_tile(sbase + OFF_R + st * 2 * TILE + TILE, &tmv, B(B_FU + st), plane, key, first_vis);
         } else {
           mbar_arrive(B(B_FU + st));
         }
         ++vj;
         return true;
       };
-      ok = fill_v(-1);
+      ok = fill_v(-1, 0, 0);
       for (int e = 0; ok; ++e) {
         Item it;
         if (!get_item(e, it)) { ok = false; break; }
@@ -545,7 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         if (it.kind != kLive) continue;
         const Tiles T = tiles_of(it, window, hpair);
         for (int i = 0; ok && i < T.n; ++i) {
-          if (*vabort || !fill_v(it.plane + (T.tb0 + i) * BN)) ok = false;
+          if (*vabort || !fill_v(it.plane, (T.tb0 + i) * BN, first_visible(it))) ok = false;
         }
       }
       if (!ok) abort_flag = 1;
@@ -902,18 +948,21 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           l += (a0 + a1) + (b0 + b1);
         }
         tmem_wait_st();
-        if (kstart + BN > kv_len) {
-          // V rows past the row's last key hold whatever the cache holds there (maybe NaN); P is 0 there,
-          // but 0 * NaN is NaN, so zero those rows before the tensor core reads them (after the V copy has
-          // landed; the stage cannot be refilled before this tile's PV, which waits for us).
-          const int tb0 = (window > 0 ? max(0, it.fp + it.q0 - window + 1) : 0) / BN;   // the item's first tile
+        // keys before lo_zero: boxes a paged pool may have recycled (not loaded when their block is gone)
+        const int lo_zero = (PAGED && prm.kbox < BN) ? first_visible(it) : 0;
+        if (kstart + BN > kv_len || kstart < lo_zero) {
+          // V rows past the row's last key hold whatever the cache holds there (maybe NaN), and rows of a
+          // skipped box whatever the stage held before; P is 0 there, but 0 * NaN is NaN, so zero those rows
+          // before the tensor core reads them (after the V copy has landed; the stage cannot be refilled
+          // before this tile's PV, which waits for us).
+          const int tb0 = first_visible(it) / BN;   // the item's first tile
           const int g = it.round0 + t - tb0 + 1;   // ring slot of this tile's round
           if (!__all_sync(0xffffffffu, mbar_wait(B(B_FU + g % NS), (g / NS) & 1, prm.err))) {
             abort_flag = 1;
             ok = false;
             break;
           }
-          if (kstart + r >= kv_len) {
+          if (kstart + r >= kv_len || kstart + r < lo_zero) {
             uint8_t* vtile = smem + OFF_R + (g % NS) * 2 * TILE + TILE;   // V(t), in the round slot of tile t
             uint4* vrow0 = reinterpret_cast<uint4*>(vtile + r * 128);
             uint4* vrow1 = reinterpret_cast<uint4*>(vtile + HALF + r * 128);
@@ -963,14 +1012,16 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   using namespace pf;
   if (a.n_seqs == 0 || a.max_q_len == 0 || a.n_tokens == 0) return cudaSuccess;
   CUtensorMap tmq, tmk, tmv, tmo;
-  const uint64_t rows_total = static_cast<uint64_t>(a.num_rows) * a.hkv * a.max_len;
+  const uint64_t rows_total = a.block_table ? static_cast<uint64_t>(a.n_blocks) * a.hkv * a.block_size
+                                            : static_cast<uint64_t>(a.num_rows) * a.hkv * a.max_len;
+  const int kbox = (a.block_table && a.block_size % BN != 0) ? 64 : BN;   // pools: block sizes are multiples of 64
   // q_rot and out [N, Hq, D]: q rows past N are zero-filled by the copy engine, never read from memory; out
   // boxes (16 rows) are only stored whole when all their rows belong to the chunk
   const uint64_t n_tok = static_cast<uint64_t>(a.n_tokens);
   if (!encode_tmap_3d_bf16(&tmq, a.q_rot, D, a.hq, n_tok, D * 2, static_cast<uint64_t>(a.hq) * D * 2, 64, 1, BM) ||
       !encode_tmap_3d_bf16(&tmo, a.out, D, a.hq, n_tok, D * 2, static_cast<uint64_t>(a.hq) * D * 2, 64, 1, 16) ||
-      !encode_tmap_2d_bf16(&tmk, a.k_cache, D, rows_total, D * 2, 64, BN) ||
-      !encode_tmap_2d_bf16(&tmv, a.v_cache, D, rows_total, D * 2, 64, BN))
+      !encode_tmap_2d_bf16(&tmk, a.k_cache, D, rows_total, D * 2, 64, kbox) ||
+      !encode_tmap_2d_bf16(&tmv, a.v_cache, D, rows_total, D * 2, 64, kbox))
     return cudaErrorInvalidValue;
   const int hpair = (a.hq / a.hkv) % 2 == 0 ? 1 : 0;
   const int item_rows = hpair ? BM : NQT * BM;
@@ -993,9 +1044,16 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   prm.hpair = hpair;
   prm.softcap = a.softcap;
   prm.sinks = a.sinks;
+  prm.block_table = a.block_table;
+  prm.block_size = a.block_size;
+  prm.max_blocks = a.max_blocks;
+  prm.n_blocks = a.n_blocks;
+  prm.kbox = kbox;
   prm.scale = a.scale;
   prm.err = a.err;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  const bool paged = a.block_table != nullptr;
+  cudaError_t e = cudaFuncSetAttribute(paged ? prefill_kernel<true> : prefill_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int dev = 0, n_sm = 0;
   e = cudaGetDevice(&dev);
@@ -1003,7 +1061,10 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (shared memory and all 512 TMEM columns allow no second one)
   const int grid = static_cast<int>(std::min<long long>(n_items, n_sm));
-  prefill_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
+  if (paged)
+    prefill_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
+  else
+    prefill_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
   return cudaGetLastError();
 }
 

@@ -43,6 +43,16 @@ RopeTurns rope_turns(const RopeFreqs& f);
 cudaError_t launch_rope_tables(const RopeFreqs& f, const int32_t* positions, const int32_t* seq_len, int n,
                                float* cos, float* sin, int* err, cudaStream_t stream);
 
+// Where the cache slot of (row, KV head, position) lives. Contiguous caches [num_rows, Hkv, max_len, d]:
+// block_table == NULL. Paged pools [n_blocks, Hkv, block_size, d]: position p of a row lives in block
+// block_table[row * max_blocks + p / block_size] at offset p % block_size, and max_len = max_blocks *
+// block_size.
+struct KvLayout {
+  const int32_t* block_table;
+  int num_rows, max_len, hkv;
+  int block_size, max_blocks, n_blocks;
+};
+
 struct KvUpdateArgs {
   const void* q;
   const void* k;
@@ -59,6 +69,8 @@ struct KvUpdateArgs {
   void* k_cache;
   void* v_cache;
   int num_rows, max_len;
+  const int32_t* block_table;     // paged pool: [num_rows, max_blocks] block ids; NULL: contiguous cache
+  int block_size, max_blocks, n_blocks;
   int* err;
   int wpt;                        // warps per token (set by the launcher)
 };
@@ -80,6 +92,8 @@ struct AttnArgs {
   int max_q_len;                  // prefill: grid bound; decode: 1
   int n_tokens;                   // rows of q_rot/out (prefill: q_start[S]; decode: S)
   const int32_t* key_positions;   // [R, M] or NULL
+  const int32_t* block_table;     // paged pool: [num_rows, max_blocks] block ids; NULL: contiguous cache
+  int block_size, max_blocks, n_blocks;
   int window;
   float softcap;
   float scale;
@@ -93,7 +107,8 @@ struct DecodePlan {
   int chunk;      // keys per split (multiple of 64)
   int n_splits;   // splits per (sequence, KV head) at most
 };
-DecodePlan decode_plan(int hkv, int n_seqs, int max_len, int window);
+// aligned: chunks start at the window start rounded down to a 64-key tile (paged pools)
+DecodePlan decode_plan(int hkv, int n_seqs, int max_len, int window, bool aligned);
 size_t decode_workspace_bytes(int hq, int n_seqs, const DecodePlan& p);
 cudaError_t launch_decode_bf16(const AttnArgs& a, const DecodePlan& p, void* workspace, cudaStream_t stream);
 

@@ -11,6 +11,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "kvmap.cuh"
 
 namespace da {
 
@@ -188,11 +189,12 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
       wk[j] = k4.x; wk[j + 1] = k4.y; wk[j + 2] = k4.z; wk[j + 3] = k4.w;
     }
   }
-  const int row = a.rows[t];
-  const int pos = a.positions[t];
-  const bool slot_ok = row >= 0 && row < a.num_rows && pos >= 0 && pos < a.max_len;
+  const KvLayout kvl = kv_layout(a);
+  const long long cslot = kv_slot(kvl, a.rows[t], a.positions[t]);
+  const bool slot_ok = cslot >= 0;
   if (!slot_ok && lane == 0) set_error(a.err, kErrIndex);
-  const long long slot_base = slot_ok ? (static_cast<long long>(row) * a.hkv * a.max_len + pos) * D : 0;
+  const long long slot_base = slot_ok ? cslot * D : 0;
+  const long long head_step = kv_head_stride(kvl) * D;
 
   // U heads per lane are loaded before any is processed: enough loads in flight to cover HBM latency
   constexpr int U = 4;
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
       if (is_q) {
         V::store(static_cast<T*>(a.q_rot) + (static_cast<long long>(t) * a.hq + hh) * D + e0, y);
       } else if (slot_ok) {
-        const long long off = slot_base + static_cast<long long>(g) * a.max_len * D + e0;
+        const long long off = slot_base + g * head_step + e0;
         V::store(static_cast<T*>(a.k_cache) + off, y);
         *reinterpret_cast<uint4*>(static_cast<T*>(a.v_cache) + off) = vv;
       }
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
 constexpr int KB_STAGES = 4;
 constexpr int KB_THREADS = 288;           // 8 computing warps + 1 copy warp
 struct KbLayout {                         // byte offsets within a stage
-  int k, v, cos, sin, hdr, bytes;         // q at 0; hdr: the token's row and position (8 bytes)
+  int k, v, cos, sin, hdr, bytes;         // q at 0; hdr: the token's cache slot (8 bytes, -1: none)
 };
 static KbLayout kb_layout(int hq, int hkv, int d, int half, int es) {
   KbLayout L;
@@ -350,12 +352,11 @@ __global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpda
       const int s = kk % KB_STAGES;
       const uint32_t st = sbase + s * L.bytes;
       if (!mbar_wait(done(s), (kk / KB_STAGES) & 1, a.err)) break;
-      const int* hdr = reinterpret_cast<const int*>(kb_smem + s * L.bytes + L.hdr);
-      const int row = hdr[0], pos = hdr[1];
+      const long long slot = *reinterpret_cast<const long long*>(kb_smem + s * L.bytes + L.hdr);
       bulk_store(static_cast<T*>(a.q_rot) + static_cast<long long>(t) * a.hq * D, st, a.hq * D * es);
-      if (row >= 0 && row < a.num_rows && pos >= 0 && pos < a.max_len) {
+      if (slot >= 0) {
         for (int g = 0; g < a.hkv; ++g) {
-          const long long off = ((static_cast<long long>(row) * a.hkv + g) * a.max_len + pos) * D;
+          const long long off = (slot + g * kv_head_stride(kv_layout(a))) * D;
           bulk_store(static_cast<T*>(a.k_cache) + off, st + L.k + g * D * es, D * es);
           bulk_store(static_cast<T*>(a.v_cache) + off, st + L.v + g * D * es, D * es);
         }
@@ -402,10 +403,9 @@ __global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpda
     if (warp == 0 && lane == 0) {
       // the token's cache slot, for the copy thread (published by this thread's arrival on done[s]); written
       // only now: the stage's full barrier is armed after the copy thread has read the previous token's slot
-      if (row < 0 || row >= a.num_rows || pos < 0 || pos >= a.max_len) set_error(a.err, kErrIndex);
-      int* hdr = reinterpret_cast<int*>(st + L.hdr);
-      hdr[0] = row;
-      hdr[1] = pos;
+      const long long slot = kv_slot(kv_layout(a), row, pos);
+      if (slot < 0) set_error(a.err, kErrIndex);
+      *reinterpret_cast<long long*>(st + L.hdr) = slot;
     }
     float c[VEC], sv[VEC];
     if (lower || upper) {

@@ -108,6 +108,37 @@ class LayerCall:
         return out
 
 
+
+def paged_from_contiguous(k_cache, v_cache, block_size, seed=0, spare_blocks=0, unmap_before=None):
+    """A paged pool holding the blocks of contiguous caches [R, Hkv, M, d] in a seeded random order.
+
+    Returns (k_pool, v_pool, block_table): pools [n_blocks, Hkv, block_size, d] (n_blocks = R * ceil(M /
+    block_size) + spare_blocks; spare blocks and the tail of a row's last block hold NaN) and an int32 table
+    [R, ceil(M / block_size)]. unmap_before[r], if given, unmaps (-1, contents NaN) every block of row r that
+    lies wholly before that position, as a pool that recycles out-of-window blocks leaves them."""
+    R, hkv, M, d = k_cache.shape
+    nb = (M + block_size - 1) // block_size
+    n_blocks = R * nb + spare_blocks
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(n_blocks, generator=g)[:R * nb].reshape(R, nb)
+    kp = torch.full((n_blocks, hkv, block_size, d), float("nan"), dtype=k_cache.dtype, device=k_cache.device)
+    vp = torch.full_like(kp, float("nan"))
+    pad = nb * block_size - M
+    kc = torch.nn.functional.pad(k_cache, (0, 0, 0, pad), value=float("nan")) if pad else k_cache
+    vc = torch.nn.functional.pad(v_cache, (0, 0, 0, pad), value=float("nan")) if pad else v_cache
+    idx = perm.reshape(-1).to(k_cache.device)
+    kp[idx] = kc.reshape(R, hkv, nb, block_size, d).transpose(1, 2).reshape(R * nb, hkv, block_size, d)
+    vp[idx] = vc.reshape(R, hkv, nb, block_size, d).transpose(1, 2).reshape(R * nb, hkv, block_size, d)
+    table = perm.clone().to(torch.int32)
+    if unmap_before is not None:
+        for r in range(R):
+            for b in range(nb):
+                if (b + 1) * block_size <= int(unmap_before[r]):
+                    kp[perm[r, b]] = float("nan")
+                    vp[perm[r, b]] = float("nan")
+                    table[r, b] = -1
+    return kp, vp, table.to(k_cache.device)
+
 @dataclass
 class Workload:
     number: int

@@ -87,3 +87,40 @@ class AttentionStep:
         if c.n_decode:
             n += 2 if self.workspace is not None else 1
         return n
+
+
+class PagedAttentionStep(AttentionStep):
+    """AttentionStep over a paged KV pool: k_pool/v_pool [n_blocks, Hkv, block_size, d] and an int32 block
+    table [num_rows, max_blocks] on the device stand in for the call's contiguous caches."""
+
+    def __init__(self, call, k_pool, v_pool, block_table, block_size, device=None):
+        super().__init__(call, device)
+        self.k_pool, self.v_pool, self.block_table = k_pool, v_pool, block_table
+        self.block_size = int(block_size)
+        self.kv = _abi.paged_kv(k_pool, v_pool, block_table, block_size)
+        self.max_positions = int(block_table.shape[1]) * self.block_size
+        self.ws_bytes = 0
+        self.workspace = None
+        c = call
+        if c.n_decode:
+            self.ws_bytes = _abi.decode_workspace_bytes_paged(self.L, c.n_decode, self.max_positions)
+            if self.ws_bytes:
+                self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+
+    def cache_update(self, stream=None):
+        c = self.call
+        _abi.kv_cache_update_paged(self.L, c.q, c.k, c.v, c.n_tokens, c.tok_rows, c.tok_pos, self.cos, self.sin,
+                                   self.q_rot, self.kv, stream)
+
+    def prefill(self, stream=None):
+        c = self.call
+        if c.n_prefill:
+            _abi.attn_prefill_paged(self.L, self.q_rot, c.n_prefill, self.kv, len(c.pf_rows), c.q_start, c.pf_rows,
+                                    c.pf_first_pos, c.max_q_len, self.out, stream)
+
+    def decode(self, stream=None):
+        c = self.call
+        if c.n_decode:
+            _abi.attn_decode_paged(self.L, self.q_rot[c.n_prefill:], self.kv, c.n_decode, c.dec_rows, c.dec_pos,
+                                   self.out[c.n_prefill:], self.workspace, self.ws_bytes, stream)
+

@@ -234,6 +234,56 @@ int da_attn_decode_noalloc(const da_layer* layer, const void* q_rot, const void*
 /* Size in bytes of the fixed scratch behind da_attn_decode_noalloc. */
 size_t da_decode_noalloc_max_scratch_bytes(void);
 
+/*
+ * Paged KV pool (page 1, "Sliding windows": the engine keeps keys and values in fixed-size blocks that each
+ * request maps through its own block table, so that blocks every query has moved past can be recycled).
+ * Position p of cache row r lives in block block_table[r * max_blocks + p / block_size], at offset
+ * p % block_size:  k_pool[block, g, p % block_size, :] is key head g of that position.
+ */
+typedef struct {
+    void*          k_pool;        /* device [n_blocks, Hkv, block_size, d], 16-byte aligned                 */
+    void*          v_pool;        /* device [n_blocks, Hkv, block_size, d], 16-byte aligned                 */
+    int            n_blocks;      /* blocks in each pool, >= 1 (n_blocks * Hkv * block_size < 2^31)         */
+    int            block_size;    /* positions per block, >= 1; the bf16 tensor-core paths need a multiple  */
+                                  /*   of 64 (other sizes run the CUDA-core kernel)                         */
+    const int32_t* block_table;   /* device int32 [num_rows, max_blocks]; an entry outside [0, n_blocks)    */
+                                  /*   (e.g. -1 for a recycled block) maps nothing                          */
+    int            num_rows;      /* cache rows (requests), >= 1                                            */
+    int            max_blocks;    /* entries per row: a row holds positions < max_blocks * block_size       */
+} da_paged_kv;
+
+/*
+ * da_kv_cache_update_paged -- da_kv_cache_update into a paged pool: token t's k_rot and v go to the slot of
+ * (rows[t], positions[t]) that kv->block_table names. A token whose row or position is out of range, or
+ * whose block is unmapped, writes nothing and sets the device error word (DA_ERR_DEVICE_INDEX).
+ */
+int da_kv_cache_update_paged(const da_layer* layer, const void* q, const void* k, const void* v, int n,
+                             const int32_t* rows, const int32_t* positions, const float* cos, const float* sin,
+                             void* q_rot, const da_paged_kv* kv, cudaStream_t stream);
+
+/*
+ * da_attn_prefill_paged -- da_attn_prefill over a paged pool (same arithmetic, sinks included). A chunk reads
+ * positions from its oldest query's first visible key (first_pos - w + 1 with a window w, else 0) to its
+ * last token; blocks wholly before that may be unmapped. A visible position without a block sets the device
+ * error word (its keys are then not the caller's).
+ */
+int da_attn_prefill_paged(const da_layer* layer, const void* q_rot, int n_tokens, const da_paged_kv* kv, int n_seqs,
+                          const int32_t* q_start, const int32_t* rows, const int32_t* first_pos, int max_q_len,
+                          void* out, cudaStream_t stream);
+
+/*
+ * da_attn_decode_paged -- da_attn_decode over a paged pool. On the split-K path the chunks of a sequence
+ * start at its first visible key rounded down to a 64-key tile (a tile never straddles two blocks), so the
+ * workspace is sized by da_decode_workspace_bytes_paged.
+ */
+int da_attn_decode_paged(const da_layer* layer, const void* q_rot, const da_paged_kv* kv, int n_seqs,
+                         const int32_t* rows, const int32_t* positions, void* out, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* Scratch bytes da_attn_decode_paged needs for n_seqs sequences of a pool whose rows hold max_positions
+ * (= max_blocks * block_size) positions (0 when the layer is invalid or decode needs none). Host arithmetic. */
+size_t da_decode_workspace_bytes_paged(const da_layer* layer, int n_seqs, int max_positions);
+
 /* Waits for `stream`, then reads and clears the device error word that kernels set on an out-of-range
  * index (DA_ERR_DEVICE_INDEX) or a bounded wait that gave up (DA_ERR_TIMEOUT). Returns DA_OK when clear,
  * DA_ERR_CUDA if the wait itself failed. */

@@ -90,3 +90,25 @@ def rotate_tokens(call, token_ids):
         k = A.rms_norm(k, layer.k_norm_w, layer.eps)
     c, s = cos[:, None, :], sin[:, None, :]
     return A.apply_rope(q, c, s), A.apply_rope(k, c, s)
+
+
+def run_layer_call_paged(call, k_pool, v_pool, block_table, block_size):
+    """run_layer_call over a paged pool (k_pool/v_pool [n_blocks, Hkv, block_size, d], block_table [R,
+    max_blocks]): the cache update writes through the table, and attention reads through it."""
+    layer = layer_of(call)
+    cos, sin = rope_tables(call)
+    kp = _np64(k_pool).copy()
+    vp = _np64(v_pool).copy()
+    table = _np_int(block_table)
+    rows, pos = _np_int(call.tok_rows), _np_int(call.tok_pos)
+    q_rot = A.kv_cache_update_paged(layer, _np64(call.q), _np64(call.k), _np64(call.v), rows, pos, cos, sin, kp, vp,
+                                    table, block_size)
+    out = np.zeros_like(q_rot)
+    npf = call.n_prefill
+    if npf:
+        out[:npf] = A.attn_prefill_paged(layer, q_rot[:npf], kp, vp, table, block_size, _np_int(call.q_start),
+                                         _np_int(call.pf_rows), _np_int(call.pf_first_pos))
+    if call.n_tokens > npf:
+        out[npf:] = A.attn_decode_paged(layer, q_rot[npf:], kp, vp, table, block_size, _np_int(call.dec_rows),
+                                        _np_int(call.dec_pos))
+    return {"cos": cos, "sin": sin, "q_rot": q_rot, "k_pool": kp, "v_pool": vp, "out": out}
