@@ -21,6 +21,7 @@ DA_ERR_UNSUPPORTED = -2
 DA_ERR_CUDA = -3
 DA_ERR_DEVICE_INDEX = -4
 DA_ERR_TIMEOUT = -5
+DA_ERR_OUT_OF_BLOCKS = -6
 
 DA_ROPE_DEFAULT, DA_ROPE_LINEAR, DA_ROPE_LLAMA3, DA_ROPE_LONGROPE, DA_ROPE_YARN = range(5)
 DA_BF16, DA_FP32 = 0, 1
@@ -78,6 +79,13 @@ def _load():
                                       P]),
         "da_attn_decode_paged": (I, [ctypes.POINTER(DaLayer), P, ctypes.POINTER(DaPagedKv), I, P, P, P, P, Z, P]),
         "da_decode_workspace_bytes_paged": (Z, [ctypes.POINTER(DaLayer), I, I]),
+        "da_block_pool_create": (P, [I, I, I, I, I]),
+        "da_block_pool_destroy": (None, [P]),
+        "da_block_pool_reserve": (I, [P, I, I, I]),
+        "da_block_pool_release": (I, [P, I]),
+        "da_block_pool_free_blocks": (I, [P]),
+        "da_block_pool_blocks_needed": (I, [P, I, I]),
+        "da_block_pool_table": (ctypes.POINTER(ctypes.c_int32), [P]),
         "da_check_device_error": (I, [P]),
         "da_last_error": (ctypes.c_char_p, []),
         "da_version": (I, []),
@@ -271,6 +279,47 @@ def attn_decode_paged(L, q_rot, kv, n_seqs, rows, positions, out, workspace, ws_
 
 def decode_workspace_bytes_paged(L, n_seqs, max_positions) -> int:
     return int(LIB.da_decode_workspace_bytes_paged(ctypes.byref(L), int(n_seqs), int(max_positions)))
+
+
+class BlockPool:
+    """da_block_pool: host block manager of one layer group's paged pool (see include/decattn.h)."""
+
+    def __init__(self, n_blocks, block_size, num_rows, max_blocks, window=0):
+        self._p = LIB.da_block_pool_create(int(n_blocks), int(block_size), int(num_rows), int(max_blocks),
+                                           int(window))
+        if not self._p:
+            raise DecAttnError(DA_ERR_INVALID_ARG, "da_block_pool_create failed")
+        self.n_blocks, self.block_size = int(n_blocks), int(block_size)
+        self.num_rows, self.max_blocks, self.window = int(num_rows), int(max_blocks), int(window)
+
+    def __del__(self):
+        if getattr(self, "_p", None):
+            LIB.da_block_pool_destroy(self._p)
+            self._p = None
+
+    def reserve(self, row, first_pos, length):
+        rc = LIB.da_block_pool_reserve(self._p, int(row), int(first_pos), int(length))
+        if rc != DA_OK:
+            what = "not enough free blocks" if rc == DA_ERR_OUT_OF_BLOCKS else "invalid row or positions"
+            raise DecAttnError(rc, f"reserve(row={row}, first_pos={first_pos}, length={length}): {what}")
+
+    def release(self, row):
+        if LIB.da_block_pool_release(self._p, int(row)) != DA_OK:
+            raise DecAttnError(DA_ERR_INVALID_ARG, f"release(row={row}): invalid row")
+
+    @property
+    def free_blocks(self):
+        return int(LIB.da_block_pool_free_blocks(self._p))
+
+    def blocks_needed(self, first_pos, length):
+        return int(LIB.da_block_pool_blocks_needed(self._p, int(first_pos), int(length)))
+
+    def table(self):
+        """A copy of the host block table, int32 [num_rows, max_blocks]."""
+        import numpy as np
+        ptr = LIB.da_block_pool_table(self._p)
+        arr = np.ctypeslib.as_array(ptr, shape=(self.num_rows * self.max_blocks,)).copy()
+        return torch.from_numpy(arr).reshape(self.num_rows, self.max_blocks)
 
 
 def check_device_error(stream=None):

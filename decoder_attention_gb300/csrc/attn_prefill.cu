@@ -336,11 +336,12 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     return s < 0 ? -1 : static_cast<int>(s + static_cast<long long>(g) * prm.block_size);
   };
   // One 128-key K or V tile (two 64-column halves, 128-byte swizzled) from boxes of kbox key rows, armed on
-  // `bar` for the bytes it copies. A box wholly before the item's first visible key whose block is gone (a
-  // pool that recycles out-of-window blocks) is skipped: its keys are masked for every query of the item
-  // and the softmax warps zero its V rows. Any other missing block is reported and read from row 0, so
-  // that the copy still delivers the bytes its barrier expects.
-  auto load_kv_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int plane, int key, int first_vis) {
+  // `bar` for the bytes it copies. A box without a block that lies wholly before the item's first visible
+  // key (a pool that recycles out-of-window blocks) or wholly past the row's last key is skipped: its keys
+  // are masked for every query of the item and the softmax warps zero its V rows. Any other missing block
+  // is reported and read from row 0, so that the copy still delivers the bytes its barrier expects.
+  auto load_kv_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int plane, int key, int first_vis,
+                          int kv_len) {
     if constexpr (!PAGED) {
       const int r = plane + key;
       mbar_arrive_expect_tx(bar, TILE);
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       uint32_t bytes = 0;
       for (int j = 0, b = 0; j < BN; j += prm.kbox, ++b) {
         rows[b] = key_row(plane, key + j);
-        if (rows[b] < 0 && key + j + prm.kbox > first_vis) {
+        if (rows[b] < 0 && key + j + prm.kbox > first_vis && key + j < kv_len) {
           set_error(prm.err, kErrIndex);
           rows[b] = 0;
         }
@@ -514,11 +515,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         ++qn;
         return true;
       };
-      auto fill_k = [&](int plane, int key, int first_vis) -> bool {   // plane < 0: the slot has no K tile
+      auto fill_k = [&](int plane, int key, int first_vis, int kv_len) -> bool {   // plane < 0: no K tile
         const int st = kj % NS;
         if (kj >= NS && !mbar_wait(B(B_EM + st), ((kj / NS) - 1) & 1, prm.err)) return false;
         if (plane >= 0) {
-          load_kv_tile(sbase + OFF_R + st * 2 * TILE, &tmk, B(B_FU + st), plane, key, first_vis);
+          load_kv_tile(sbase + OFF_R + st * 2 * TILE, &tmk, B(B_FU + st), plane, key, first_vis, kv_len);
         } else {
           mbar_arrive(B(B_FU + st));
         }
@@ -556,12 +557,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const Tiles T = tiles_of(it, window, hpair);
         if (!load_q(it, 0)) { ok = false; break; }
         for (int i = 0; ok && i < T.n; ++i) {
-          if (*vabort || (i == 1 && T.valid1 && !load_q(it, 1)) || !fill_k(it.plane, (T.tb0 + i) * BN, first_visible(it)))
+          if (*vabort || (i == 1 && T.valid1 && !load_q(it, 1)) ||
+              !fill_k(it.plane, (T.tb0 + i) * BN, first_visible(it), it.fp + it.n_b))
             ok = false;
         }
         if (ok && T.n == 1 && T.valid1 && !load_q(it, 1)) ok = false;
       }
-      if (ok && !fill_k(-1, 0, 0)) ok = false;
+      if (ok && !fill_k(-1, 0, 0, 0)) ok = false;
       if (!ok) abort_flag = 1;
       // every issued copy must land before the CTA's shared memory is released
       for (int j = max(0, qn - NQB); j < qn; ++j) mbar_wait(B(B_QF + j % NQB), (j / NQB) & 1, prm.err);
@@ -572,18 +574,18 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       prefetch_tmap(&tmv);
       int vj = 0;
       bool ok = true;
-      auto fill_v = [&](int plane, int key, int first_vis) -> bool {   // plane < 0: the slot has no V tile
+      auto fill_v = [&](int plane, int key, int first_vis, int kv_len) -> bool {   // plane < 0: no V tile
         const int st = vj % NS;
         if (vj >= NS && !mbar_wait(B(B_EM + st), ((vj / NS) - 1) & 1, prm.err)) return false;
         if (plane >= 0) {
-          load_kv_tile(sbase + OFF_R + st * 2 * TILE + TILE, &tmv, B(B_FU + st), plane, key, first_vis);
+          load_kv_tile(sbase + OFF_R + st * 2 * TILE + TILE, &tmv, B(B_FU + st), plane, key, first_vis, kv_len);
         } else {
           mbar_arrive(B(B_FU + st));
         }
         ++vj;
         return true;
       };
-      ok = fill_v(-1, 0, 0);
+      ok = fill_v(-1, 0, 0, 0);
       for (int e = 0; ok; ++e) {
         Item it;
         if (!get_item(e, it)) { ok = false; break; }
@@ -591,7 +593,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         if (it.kind != kLive) continue;
         const Tiles T = tiles_of(it, window, hpair);
         for (int i = 0; ok && i < T.n; ++i) {
-          if (*vabort || !fill_v(it.plane, (T.tb0 + i) * BN, first_visible(it))) ok = false;
+          if (*vabort || !fill_v(it.plane, (T.tb0 + i) * BN, first_visible(it), it.fp + it.n_b)) ok = false;
         }
       }
       if (!ok) abort_flag = 1;

@@ -109,13 +109,15 @@ class LayerCall:
 
 
 
-def paged_from_contiguous(k_cache, v_cache, block_size, seed=0, spare_blocks=0, unmap_before=None):
+def paged_from_contiguous(k_cache, v_cache, block_size, seed=0, spare_blocks=0, unmap_before=None, unmap_from=None):
     """A paged pool holding the blocks of contiguous caches [R, Hkv, M, d] in a seeded random order.
 
     Returns (k_pool, v_pool, block_table): pools [n_blocks, Hkv, block_size, d] (n_blocks = R * ceil(M /
     block_size) + spare_blocks; spare blocks and the tail of a row's last block hold NaN) and an int32 table
     [R, ceil(M / block_size)]. unmap_before[r], if given, unmaps (-1, contents NaN) every block of row r that
-    lies wholly before that position, as a pool that recycles out-of-window blocks leaves them."""
+    lies wholly before that position, as a pool that recycles out-of-window blocks leaves them; unmap_from[r]
+    unmaps every block that starts at or after that position, as a pool that maps blocks only as a row
+    grows leaves them."""
     R, hkv, M, d = k_cache.shape
     nb = (M + block_size - 1) // block_size
     n_blocks = R * nb + spare_blocks
@@ -130,10 +132,12 @@ def paged_from_contiguous(k_cache, v_cache, block_size, seed=0, spare_blocks=0, 
     kp[idx] = kc.reshape(R, hkv, nb, block_size, d).transpose(1, 2).reshape(R * nb, hkv, block_size, d)
     vp[idx] = vc.reshape(R, hkv, nb, block_size, d).transpose(1, 2).reshape(R * nb, hkv, block_size, d)
     table = perm.clone().to(torch.int32)
-    if unmap_before is not None:
+    if unmap_before is not None or unmap_from is not None:
         for r in range(R):
             for b in range(nb):
-                if (b + 1) * block_size <= int(unmap_before[r]):
+                gone = unmap_before is not None and (b + 1) * block_size <= int(unmap_before[r])
+                gone = gone or (unmap_from is not None and b * block_size >= int(unmap_from[r]))
+                if gone:
                     kp[perm[r, b]] = float("nan")
                     vp[perm[r, b]] = float("nan")
                     table[r, b] = -1

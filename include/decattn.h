@@ -52,6 +52,7 @@ extern "C" {
 #define DA_ERR_CUDA          (-3)   /* a CUDA runtime call failed (message names it)              */
 #define DA_ERR_DEVICE_INDEX  (-4)   /* da_check_device_error: a kernel met an out-of-range index   */
 #define DA_ERR_TIMEOUT       (-5)   /* da_check_device_error: a kernel gave up a bounded wait      */
+#define DA_ERR_OUT_OF_BLOCKS (-6)   /* da_block_pool_reserve: not enough free blocks (nothing done) */
 
 /* RoPE frequency scaling kinds (page 1, "Scaled RoPE", rope_inv_freq; "Model resolution", Overview,
  * for longrope). */
@@ -283,6 +284,44 @@ int da_attn_decode_paged(const da_layer* layer, const void* q_rot, const da_page
 /* Scratch bytes da_attn_decode_paged needs for n_seqs sequences of a pool whose rows hold max_positions
  * (= max_blocks * block_size) positions (0 when the layer is invalid or decode needs none). Host arithmetic. */
 size_t da_decode_workspace_bytes_paged(const da_layer* layer, int n_seqs, int max_positions);
+
+/*
+ * Block manager of a paged pool (host bookkeeping only; page 1, "Sliding windows": each request maps pool
+ * blocks through its own block table, and a group of windowed layers keeps its own table so that the blocks
+ * every query has moved past are recycled: a windowed-only request holds at most ceil(w / block_size) + 1
+ * blocks however long its context). One pool serves one layer group (one window w, 0 = full attention) and
+ * owns the host copy of that group's table [num_rows, max_blocks] (-1 = no block); the device pools and the
+ * device copy of the table belong to the caller, who copies the table after the calls that change it. Free
+ * blocks are handed out last-freed first. A pool is not thread-safe.
+ */
+typedef struct da_block_pool da_block_pool;
+
+/* A pool of n_blocks blocks of block_size positions for num_rows rows of max_blocks table entries each,
+ * for layers with window `window` (0 = full). NULL on invalid arguments or allocation failure. */
+da_block_pool* da_block_pool_create(int n_blocks, int block_size, int num_rows, int max_blocks, int window);
+void da_block_pool_destroy(da_block_pool* pool);
+
+/*
+ * Before a step that attends from position first_pos (the row's oldest query in the step) up to position
+ * length - 1 (its newest token): maps every block of positions [lo, length) that is not yet mapped, with
+ * lo = max(0, first_pos - w + 1) for a windowed pool and 0 otherwise, and (windowed pools) releases the
+ * row's blocks that lie wholly before lo. All or nothing: DA_ERR_OUT_OF_BLOCKS leaves the pool unchanged.
+ * first_pos must not decrease for a row until the row is released. DA_ERR_INVALID_ARG for a bad row,
+ * first_pos < 0, length < first_pos, or length beyond max_blocks * block_size.
+ */
+int da_block_pool_reserve(da_block_pool* pool, int row, int first_pos, int length);
+
+/* Releases every block of a row (its request has finished); the row can then serve a new request. */
+int da_block_pool_release(da_block_pool* pool, int row);
+
+/* Free blocks (-1 for a NULL pool). */
+int da_block_pool_free_blocks(const da_block_pool* pool);
+
+/* Blocks a row holds after da_block_pool_reserve(pool, row, first_pos, length) (-1 on bad arguments). */
+int da_block_pool_blocks_needed(const da_block_pool* pool, int first_pos, int length);
+
+/* The host block table [num_rows, max_blocks], owned by the pool; valid until the pool is destroyed. */
+const int32_t* da_block_pool_table(const da_block_pool* pool);
 
 /* Waits for `stream`, then reads and clears the device error word that kernels set on an out-of-range
  * index (DA_ERR_DEVICE_INDEX) or a bounded wait that gave up (DA_ERR_TIMEOUT). Returns DA_OK when clear,
