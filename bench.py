@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--scale", choices=["full", "profile"], default="full",
                     help="profile: the same head shapes with bounded caches (a few GB), for profiler captures")
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--kv-block", type=int, default=0,
+                    help="0: contiguous caches; N > 0: a paged pool of N-position blocks in shuffled order "
+                         "(da_*_paged entry points)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)   # internal: child process
@@ -265,7 +268,18 @@ def main_native(args):
     torch.cuda.set_device(dev)
     num = inputs.NUMBERS[args.workload]
     wl = inputs.make(num, scale=args.scale if num in (3, 4, 5) else "full", device=dev)
-    steps = [S.AttentionStep(c) for c in wl.layers]
+    pools = []
+    if args.kv_block > 0:
+        for li, c in enumerate(wl.layers):
+            pools.append(inputs.paged_from_contiguous(c.k_cache, c.v_cache, args.kv_block, seed=1000 + li))
+
+    def make_step(c, li):
+        if not pools:
+            return S.AttentionStep(c)
+        kp, vp, table = pools[li]
+        return S.PagedAttentionStep(c, kp, vp, table, args.kv_block)
+
+    steps = [make_step(c, li) for li, c in enumerate(wl.layers)]
     work = W.workload_work(wl)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -326,7 +340,7 @@ def main_native(args):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                 "peak_kind": f"bf16 dense burst, of {peak_kind}", "launch_ms": kms,
                 "algorithmic_flops_per_launch": work["prefill_flops"] / n_layers,
-                "traffic": load_traffic("prefill_kernel", args.workload)}
+                "traffic": None if pools else load_traffic("prefill_kernel", args.workload)}
     else:
         kms = statistics.mean(dec_ms)
         achieved = work["decode_bytes"] / (kms / 1e3) / 1e9
@@ -334,7 +348,7 @@ def main_native(args):
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "peak_kind": f"HBM copy, of {peak_kind}", "launch_ms": kms,
                 "algorithmic_bytes_per_launch": work["decode_bytes"] / n_layers,
-                "traffic": load_traffic("decode_kernel", args.workload)}
+                "traffic": None if pools else load_traffic("decode_kernel", args.workload)}
 
     # ------------------------------------------------------------------ end to end (host buffers)
     # Each step uploads its inputs (new tokens' q/k/v, rows, positions, chunk offsets) from pinned host
@@ -349,7 +363,7 @@ def main_native(args):
         sets = []
         for b in range(2):
             layer_steps = []
-            for st in steps:
+            for li, st in enumerate(steps):
                 c = st.call
                 if b == 0:
                     layer_steps.append(st)
@@ -357,7 +371,7 @@ def main_native(args):
                 fields = {k: getattr(c, k) for k in c.__dataclass_fields__}
                 for n in names:
                     fields[n] = getattr(c, n).clone()
-                layer_steps.append(S.AttentionStep(type(c)(**fields)))
+                layer_steps.append(make_step(type(c)(**fields), li))
             sets.append(layer_steps)
         host_in = [[[getattr(st.call, n).cpu().pin_memory() for n in names] for st in layer_steps]
                    for layer_steps in sets]
@@ -433,6 +447,8 @@ def main_native(args):
             "data": "synthetic",
             "config": {"workload": args.workload, "number": num, "scale": args.scale, "description": wl.description,
                        "l2": "flushed (256 MB write) before every timed step, outside the step's events",
+                       "kv": (f"paged pool, {args.kv_block}-position blocks in shuffled order" if pools
+                              else "contiguous caches"),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "tokens_per_s": tokens_per_s,
             "breakdown_ms": {"rope_and_cache_update": statistics.mean(pre_ms), "prefill": statistics.mean(pf_ms),
