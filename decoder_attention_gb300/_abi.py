@@ -60,6 +60,11 @@ class DaPagedKv(ctypes.Structure):
                 ("max_blocks", ctypes.c_int)]
 
 
+class DaMlaLayer(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int), ("kv_lora_rank", ctypes.c_int), ("qk_rope_dim", ctypes.c_int),
+                ("scale", ctypes.c_float), ("window", ctypes.c_int)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
@@ -79,6 +84,14 @@ def _load():
                                       P]),
         "da_attn_decode_paged": (I, [ctypes.POINTER(DaLayer), P, ctypes.POINTER(DaPagedKv), I, P, P, P, P, Z, P]),
         "da_decode_workspace_bytes_paged": (Z, [ctypes.POINTER(DaLayer), I, I]),
+        "da_mla_cache_update": (I, [ctypes.POINTER(DaMlaLayer), P, P, I, P, P, P, P, P, P, I, I, P]),
+        "da_mla_decode": (I, [ctypes.POINTER(DaMlaLayer), P, P, I, I, I, P, P, P, P, Z, P]),
+        "da_mla_workspace_bytes": (Z, [ctypes.POINTER(DaMlaLayer), I, I]),
+        "da_mla_cache_update_paged": (I, [ctypes.POINTER(DaMlaLayer), P, P, I, P, P, P, P, P,
+                                          ctypes.POINTER(DaPagedKv), P]),
+        "da_mla_decode_paged": (I, [ctypes.POINTER(DaMlaLayer), P, ctypes.POINTER(DaPagedKv), I, P, P, P, P, Z, P]),
+        "da_mla_workspace_bytes_paged": (Z, [ctypes.POINTER(DaMlaLayer), I, I]),
+        "da_mla_softmax_scale": (ctypes.c_double, [I, I, ctypes.c_double, ctypes.c_double]),
         "da_block_pool_create": (P, [I, I, I, I, I]),
         "da_block_pool_destroy": (None, [P]),
         "da_block_pool_reserve": (I, [P, I, I, I]),
@@ -279,6 +292,49 @@ def attn_decode_paged(L, q_rot, kv, n_seqs, rows, positions, out, workspace, ws_
 
 def decode_workspace_bytes_paged(L, n_seqs, max_positions) -> int:
     return int(LIB.da_decode_workspace_bytes_paged(ctypes.byref(L), int(n_seqs), int(max_positions)))
+
+
+def mla_softmax_scale(qk_nope_head_dim, qk_rope_head_dim, rope_scaling=None) -> float:
+    s = rope_scaling or {}
+    return float(LIB.da_mla_softmax_scale(int(qk_nope_head_dim), int(qk_rope_head_dim), float(s.get("factor") or 0.0),
+                                          float(s.get("mscale_all_dim") or 0.0)))
+
+
+def mla_layer(num_heads, scale, kv_lora_rank=512, qk_rope_dim=64, window=0):
+    L = DaMlaLayer()
+    L.num_heads, L.kv_lora_rank, L.qk_rope_dim = int(num_heads), int(kv_lora_rank), int(qk_rope_dim)
+    L.scale, L.window = float(scale), int(window)
+    return L
+
+
+def mla_cache_update(L, latent, k_rope, n, rows, positions, cos, sin, q, cache, num_rows, max_len, stream=None):
+    _check(LIB.da_mla_cache_update(ctypes.byref(L), _ptr(latent), _ptr(k_rope), int(n), _ptr(rows), _ptr(positions),
+                                   _ptr(cos), _ptr(sin), _ptr(q), _ptr(cache), int(num_rows), int(max_len),
+                                   _stream(stream)))
+
+
+def mla_decode(L, q, cache, num_rows, max_len, n_seqs, rows, positions, out, workspace, ws_bytes, stream=None):
+    _check(LIB.da_mla_decode(ctypes.byref(L), _ptr(q), _ptr(cache), int(num_rows), int(max_len), int(n_seqs),
+                             _ptr(rows), _ptr(positions), _ptr(out), _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def mla_workspace_bytes(L, n_seqs, max_len) -> int:
+    return int(LIB.da_mla_workspace_bytes(ctypes.byref(L), int(n_seqs), int(max_len)))
+
+
+def mla_cache_update_paged(L, latent, k_rope, n, rows, positions, cos, sin, q, kv, stream=None):
+    _check(LIB.da_mla_cache_update_paged(ctypes.byref(L), _ptr(latent), _ptr(k_rope), int(n), _ptr(rows),
+                                         _ptr(positions), _ptr(cos), _ptr(sin), _ptr(q), ctypes.byref(kv),
+                                         _stream(stream)))
+
+
+def mla_decode_paged(L, q, kv, n_seqs, rows, positions, out, workspace, ws_bytes, stream=None):
+    _check(LIB.da_mla_decode_paged(ctypes.byref(L), _ptr(q), ctypes.byref(kv), int(n_seqs), _ptr(rows),
+                                   _ptr(positions), _ptr(out), _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def mla_workspace_bytes_paged(L, n_seqs, max_positions) -> int:
+    return int(LIB.da_mla_workspace_bytes_paged(ctypes.byref(L), int(n_seqs), int(max_positions)))
 
 
 class BlockPool:

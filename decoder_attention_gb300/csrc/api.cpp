@@ -533,4 +533,168 @@ int da_check_device_error(cudaStream_t stream) {
   return ok();
 }
 
+// ---------------------------------------------------------------------------------------------- MLA
+
+static int check_mla_layer(const da_mla_layer* L) {
+  if (!L) return fail(DA_ERR_INVALID_ARG, "layer is NULL");
+  if (L->kv_lora_rank != 512 || L->qk_rope_dim != 64)
+    return fail(DA_ERR_UNSUPPORTED, "MLA supports kv_lora_rank 512 and qk_rope_dim 64 (got %d, %d)", L->kv_lora_rank,
+                L->qk_rope_dim);
+  if (L->num_heads < 8 || L->num_heads % 8 != 0 || L->num_heads > 4096)
+    return fail(DA_ERR_UNSUPPORTED, "MLA num_heads must be a positive multiple of 8 (got %d)", L->num_heads);
+  if (!(L->scale > 0.f) || !std::isfinite(L->scale)) return fail(DA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (L->window < 0) return fail(DA_ERR_INVALID_ARG, "window = %d < 0", L->window);
+  return DA_OK;
+}
+
+static int mla_update_impl(const da_mla_layer* L, const void* latent, const void* k_rope, int n, const int32_t* rows,
+                           const int32_t* positions, const float* cos, const float* sin, void* q, void* cache,
+                           int num_rows, int max_len, const da_paged_kv* kv, cudaStream_t stream) {
+  int rc = check_mla_layer(L);
+  if (rc) return rc;
+  if (n < 0) return fail(DA_ERR_INVALID_ARG, "n = %d < 0", n);
+  if (n == 0) return ok();
+  if (!latent || !k_rope || !rows || !positions || !cos || !sin || !cache)
+    return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
+  if (!aligned16(latent) || !aligned16(cache) || !aligned16(q) || (reinterpret_cast<uintptr_t>(k_rope) & 3))
+    return fail(DA_ERR_INVALID_ARG, "latent, q and the cache must be 16-byte aligned, k_rope 4-byte aligned");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  da::MlaUpdateArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.latent = latent;
+  a.k_rope = k_rope;
+  a.rows = rows;
+  a.positions = positions;
+  a.cos = cos;
+  a.sin = sin;
+  a.q = q;
+  a.cache = cache;
+  a.n = n;
+  a.hq = L->num_heads;
+  a.num_rows = num_rows;
+  a.max_len = max_len;
+  set_paged(a, kv);
+  a.err = err;
+  cudaError_t e = da::launch_mla_update(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "MLA cache update launch");
+  return ok();
+}
+
+int da_mla_cache_update(const da_mla_layer* L, const void* latent, const void* k_rope, int n, const int32_t* rows,
+                        const int32_t* positions, const float* cos, const float* sin, void* q, void* cache,
+                        int num_rows, int max_len, cudaStream_t stream) {
+  return mla_update_impl(L, latent, k_rope, n, rows, positions, cos, sin, q, cache, num_rows, max_len, nullptr,
+                         stream);
+}
+
+static int check_mla_paged(const da_mla_layer* L, const da_paged_kv* kv) {
+  if (!kv) return fail(DA_ERR_INVALID_ARG, "the paged pool description is NULL");
+  if (!kv->k_pool || !kv->block_table) return fail(DA_ERR_INVALID_ARG, "a pool pointer is NULL");
+  if (kv->n_blocks < 1 || kv->block_size < 1 || kv->num_rows < 1 || kv->max_blocks < 1)
+    return fail(DA_ERR_INVALID_ARG, "n_blocks, block_size, num_rows and max_blocks must be >= 1");
+  if (static_cast<long long>(kv->max_blocks) * kv->block_size > 0x7fffffffLL ||
+      static_cast<long long>(kv->n_blocks) * kv->block_size > 0x7fffffffLL)
+    return fail(DA_ERR_UNSUPPORTED, "the pool or a row exceeds 2^31 positions");
+  if (!aligned16(kv->k_pool)) return fail(DA_ERR_INVALID_ARG, "the pool must be 16-byte aligned");
+  (void)L;
+  return DA_OK;
+}
+
+int da_mla_cache_update_paged(const da_mla_layer* L, const void* latent, const void* k_rope, int n,
+                              const int32_t* rows, const int32_t* positions, const float* cos, const float* sin,
+                              void* q, const da_paged_kv* kv, cudaStream_t stream) {
+  int rc = check_mla_layer(L);
+  if (rc) return rc;
+  if (n == 0) return ok();
+  rc = check_mla_paged(L, kv);
+  if (rc) return rc;
+  return mla_update_impl(L, latent, k_rope, n, rows, positions, cos, sin, q, kv->k_pool, kv->num_rows,
+                         kv->max_blocks * kv->block_size, kv, stream);
+}
+
+double da_mla_softmax_scale(int qk_nope_head_dim, int qk_rope_head_dim, double factor, double mscale_all_dim) {
+  if (qk_nope_head_dim < 0 || qk_rope_head_dim < 0 || qk_nope_head_dim + qk_rope_head_dim <= 0)
+    return std::nan("");
+  double scale = 1.0 / std::sqrt(static_cast<double>(qk_nope_head_dim + qk_rope_head_dim));
+  if (mscale_all_dim > 0.0 && factor > 1.0) {
+    const double m = 0.1 * mscale_all_dim * std::log(factor) + 1.0;
+    scale *= m * m;
+  }
+  return scale;
+}
+
+size_t da_mla_workspace_bytes(const da_mla_layer* L, int n_seqs, int max_len) {
+  if (check_mla_layer(L) != DA_OK || n_seqs <= 0 || max_len <= 0) return 0;
+  return da::mla_workspace_bytes(L->num_heads, n_seqs, da::mla_plan(L->num_heads, n_seqs, max_len, L->window, false));
+}
+
+size_t da_mla_workspace_bytes_paged(const da_mla_layer* L, int n_seqs, int max_positions) {
+  if (check_mla_layer(L) != DA_OK || n_seqs <= 0 || max_positions <= 0) return 0;
+  return da::mla_workspace_bytes(L->num_heads, n_seqs,
+                                 da::mla_plan(L->num_heads, n_seqs, max_positions, L->window, true));
+}
+
+static int mla_decode_impl(const da_mla_layer* L, const void* q, const void* cache, int num_rows, int max_len,
+                           int n_seqs, const int32_t* rows, const int32_t* positions, void* out, void* workspace,
+                           size_t ws_bytes, const da_paged_kv* kv, cudaStream_t stream) {
+  int rc = check_mla_layer(L);
+  if (rc) return rc;
+  if (n_seqs < 0) return fail(DA_ERR_INVALID_ARG, "n_seqs = %d < 0", n_seqs);
+  if (n_seqs > 65535) return fail(DA_ERR_UNSUPPORTED, "n_seqs = %d > 65535 per call", n_seqs);
+  if (n_seqs == 0) return ok();
+  if (!q || !cache || !rows || !positions || !out) return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
+  if (!kv && static_cast<long long>(num_rows) * max_len > 0x7fffffffLL)
+    return fail(DA_ERR_UNSUPPORTED, "num_rows * max_len exceeds 2^31 rows");
+  if (kv && kv->block_size % 64 != 0)
+    return fail(DA_ERR_UNSUPPORTED, "MLA decode over a pool needs a block size that is a multiple of 64");
+  if (!aligned16(q) || !aligned16(cache) || !aligned16(out))
+    return fail(DA_ERR_INVALID_ARG, "q, the cache and out must be 16-byte aligned");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  const da::MlaPlan p = da::mla_plan(L->num_heads, n_seqs, max_len, L->window, kv != nullptr);
+  const size_t need = da::mla_workspace_bytes(L->num_heads, n_seqs, p);
+  if (!workspace || ws_bytes < need)
+    return fail(DA_ERR_INVALID_ARG, "MLA workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
+  if (!aligned16(workspace)) return fail(DA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  da::MlaArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.cache = cache;
+  a.out = out;
+  a.hq = L->num_heads;
+  a.num_rows = num_rows;
+  a.max_len = max_len;
+  a.n_seqs = n_seqs;
+  a.window = L->window;
+  a.scale = L->scale;
+  a.rows = rows;
+  a.positions = positions;
+  set_paged(a, kv);
+  a.err = err;
+  cudaError_t e = da::launch_mla_decode(a, p, workspace, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
+  return ok();
+}
+
+int da_mla_decode(const da_mla_layer* L, const void* q, const void* cache, int num_rows, int max_len, int n_seqs,
+                  const int32_t* rows, const int32_t* positions, void* out, void* workspace, size_t ws_bytes,
+                  cudaStream_t stream) {
+  return mla_decode_impl(L, q, cache, num_rows, max_len, n_seqs, rows, positions, out, workspace, ws_bytes, nullptr,
+                         stream);
+}
+
+int da_mla_decode_paged(const da_mla_layer* L, const void* q, const da_paged_kv* kv, int n_seqs, const int32_t* rows,
+                        const int32_t* positions, void* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_mla_layer(L);
+  if (rc) return rc;
+  if (n_seqs == 0) return ok();
+  rc = check_mla_paged(L, kv);
+  if (rc) return rc;
+  return mla_decode_impl(L, q, kv->k_pool, kv->num_rows, kv->max_blocks * kv->block_size, n_seqs, rows, positions,
+                         out, workspace, ws_bytes, kv, stream);
+}
+
 }  // extern "C"

@@ -119,6 +119,42 @@ void* static_scratch();   // its device address on the current device; NULL if t
 // tcgen05 prefill (bf16, d = 128, no key_positions).
 cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream);
 
+// MLA (latent rank 512, rotary 64, bf16): cache rows [num_rows, max_len, 576] or a paged pool of such rows.
+struct MlaUpdateArgs {
+  const void* latent;             // [n, 512]
+  const void* k_rope;             // [n, 64], adjacent pairs
+  const int32_t* rows;
+  const int32_t* positions;
+  const float* cos;               // [n, 32]
+  const float* sin;
+  void* q;                        // [n, Hq, 576] or NULL (rotary part rotated in place)
+  void* cache;
+  int n, hq, num_rows, max_len;
+  const int32_t* block_table;     // paged pool or NULL
+  int block_size, max_blocks, n_blocks;
+  int* err;
+};
+struct MlaArgs {
+  const void* q;                  // [S, Hq, 576]
+  const void* cache;
+  void* out;                      // [S, Hq, 512]
+  int hq, num_rows, max_len, n_seqs, window;
+  float scale;
+  const int32_t* rows;
+  const int32_t* positions;
+  const int32_t* block_table;
+  int block_size, max_blocks, n_blocks;
+  int* err;
+};
+struct MlaPlan {
+  int chunk;      // keys per split (multiple of 64)
+  int n_splits;
+};
+MlaPlan mla_plan(int hq, int n_seqs, int max_len, int window, bool aligned);
+size_t mla_workspace_bytes(int hq, int n_seqs, const MlaPlan& p);
+cudaError_t launch_mla_update(const MlaUpdateArgs& a, cudaStream_t stream);
+cudaError_t launch_mla_decode(const MlaArgs& a, const MlaPlan& plan, void* workspace, cudaStream_t stream);
+
 // Tensor maps (driver entry point resolved at run time; no link-time dependency on libcuda).
 bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                          uint32_t box_inner, uint32_t box_outer);

@@ -109,6 +109,82 @@ class LayerCall:
 
 
 
+# ------------------------------------------------------------------------------------------ MLA decode
+
+DEEPSEEK_V3_YARN = {"type": "yarn", "factor": 40.0, "original_max_position_embeddings": 4096, "beta_fast": 32.0,
+                    "beta_slow": 1.0, "mscale": 1.0, "mscale_all_dim": 1.0}
+
+
+@dataclass
+class MlaCall:
+    """One MLA decode step: S sequences, one new token each (DeepSeek-V3 shapes: latent 512, rotary 64)."""
+    num_heads: int
+    qk_nope_head_dim: int            # the scale is (qk_nope + qk_rope)^-0.5 with YaRN's temperature
+    qk_rope_head_dim: int
+    rope_theta: float
+    rope_scaling: dict | None
+    max_position_embeddings: int
+    q: torch.Tensor = None           # [S, H, 576] bf16: W_uk^T q_nope (512), then q_rope (64, adjacent pairs)
+    latent: torch.Tensor = None      # [S, 512] bf16: the new token's latent c
+    k_rope: torch.Tensor = None      # [S, 64] bf16: its rotary key (adjacent pairs)
+    rows: torch.Tensor = None        # int32 [S]
+    positions: torch.Tensor = None   # int32 [S]: the new token's position (it sees 0..p)
+    seq_len: torch.Tensor = None     # int32 [S]: positions + 1
+    cache: torch.Tensor = None       # [R, M, 576] bf16: rows [c, rotated k_rope] of earlier positions
+    window: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def n_seqs(self):
+        return int(self.q.shape[0])
+
+    @property
+    def num_rows(self):
+        return int(self.cache.shape[0])
+
+    @property
+    def max_len(self):
+        return int(self.cache.shape[1])
+
+    def to(self, device):
+        out = MlaCall(**{k: getattr(self, k) for k in self.__dataclass_fields__})
+        for k in self.__dataclass_fields__:
+            val = getattr(self, k)
+            if isinstance(val, torch.Tensor):
+                setattr(out, k, val.to(device))
+        out.meta = dict(self.meta)
+        return out
+
+
+def deepseek_v3_mla_decode(scale="full", device="cpu", heads=128):
+    """MLA decode with DeepSeek-V3's attention shapes: 128 query heads per latent row, rows of 512 + 64,
+    YaRN (factor 40 over 4096), one new token for each of 64 sequences at contexts uniform in [2048, 32768]
+    (rows permuted). Latents and rotary keys N(0,1); absorbed queries N(0, 0.5^2). Small: 5 sequences at
+    contexts up to 700 (one first token, one at the 64-key tile boundary), 16 heads."""
+    g = _gen(1006)
+    g_len = _gen(2006)
+    if scale == "full":
+        S, lo, hi, M, H = 64, 2048, 32768, 32768, heads
+        lens = torch.randint(lo, hi + 1, (S,), generator=g_len).tolist()
+    else:
+        S, M, H = 5, 700, 16
+        lens = [1, 64, 65, 700, 333]
+    rows = torch.randperm(S, generator=g_len).tolist()
+    cache = torch.empty((S, M, 576), dtype=torch.bfloat16, device=device)
+    gd = g if str(device) == "cpu" else _gen(1006 + 7919, device)
+    for r in range(S):
+        cache[r].copy_(torch.randn((M, 576), generator=gd, dtype=torch.float32, device=device))
+    q = _randn(g, (S, H, 576), 0.5, torch.bfloat16)
+    latent = _randn(g, (S, 512), 1.0, torch.bfloat16)
+    k_rope = _randn(g, (S, 64), 1.0, torch.bfloat16)
+    pos = [L - 1 for L in lens]
+    return MlaCall(num_heads=H, qk_nope_head_dim=128, qk_rope_head_dim=64, rope_theta=1e4, rope_scaling=DEEPSEEK_V3_YARN,
+                   max_position_embeddings=163840, q=q, latent=latent, k_rope=k_rope, rows=_i32(rows),
+                   positions=_i32(pos), seq_len=_i32(lens), cache=cache,
+                   meta={"description": f"DeepSeek-V3 MLA decode: {S} sequences, {H} heads per 576-wide latent row, "
+                                        f"contexts {min(lens)}..{max(lens)}"}).to(device)
+
+
 def paged_from_contiguous(k_cache, v_cache, block_size, seed=0, spare_blocks=0, unmap_before=None, unmap_from=None):
     """A paged pool holding the blocks of contiguous caches [R, Hkv, M, d] in a seeded random order.
 

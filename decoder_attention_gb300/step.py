@@ -124,3 +124,62 @@ class PagedAttentionStep(AttentionStep):
             _abi.attn_decode_paged(self.L, self.q_rot[c.n_prefill:], self.kv, c.n_decode, c.dec_rows, c.dec_pos,
                                    self.out[c.n_prefill:], self.workspace, self.ws_bytes, stream)
 
+
+
+class MlaDecodeStep:
+    """Buffers and C structs for one MLA decode step (see decoder_attention_gb300.inputs.MlaCall): rope tables
+    for the 64 rotary features, the cache update (rows written, queries' rotary part rotated in place) and the
+    absorbed decode. Over a paged pool when k_pool and block_table are given."""
+
+    def __init__(self, call, k_pool=None, block_table=None, block_size=0):
+        c = self.call = call
+        dev = c.q.device
+        self.rs, self._keep = _abi.rope_scaling(c.rope_theta, c.qk_rope_head_dim, c.rope_scaling,
+                                                c.max_position_embeddings)
+        self.scale = _abi.mla_softmax_scale(c.qk_nope_head_dim, c.qk_rope_head_dim, c.rope_scaling)
+        self.L = _abi.mla_layer(c.num_heads, self.scale, window=c.window)
+        S = c.n_seqs
+        self.cos = torch.empty((max(S, 1), c.qk_rope_head_dim // 2), dtype=torch.float32, device=dev)
+        self.sin = torch.empty_like(self.cos)
+        self.q_rot = c.q.clone()
+        self.out = torch.empty((S, c.num_heads, 512), dtype=c.q.dtype, device=dev)
+        self.kv = None
+        if k_pool is not None:
+            self.k_pool, self.block_table = k_pool, block_table
+            self.kv = _abi.paged_kv(k_pool, k_pool, block_table, block_size)
+            self.ws_bytes = _abi.mla_workspace_bytes_paged(self.L, S, int(block_table.shape[1]) * int(block_size))
+        else:
+            self.ws_bytes = _abi.mla_workspace_bytes(self.L, S, c.max_len)
+        self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def rope(self, stream=None):
+        c = self.call
+        _abi.rope_tables_build(self.rs, c.positions, c.seq_len, c.n_seqs, self.cos, self.sin, stream)
+
+    def cache_update(self, stream=None):
+        c = self.call
+        self.q_rot.copy_(c.q)
+        if self.kv is not None:
+            _abi.mla_cache_update_paged(self.L, c.latent, c.k_rope, c.n_seqs, c.rows, c.positions, self.cos, self.sin,
+                                        self.q_rot, self.kv, stream)
+        else:
+            _abi.mla_cache_update(self.L, c.latent, c.k_rope, c.n_seqs, c.rows, c.positions, self.cos, self.sin,
+                                  self.q_rot, c.cache, c.num_rows, c.max_len, stream)
+
+    def decode(self, stream=None):
+        c = self.call
+        if self.kv is not None:
+            _abi.mla_decode_paged(self.L, self.q_rot, self.kv, c.n_seqs, c.rows, c.positions, self.out,
+                                  self.workspace, self.ws_bytes, stream)
+        else:
+            _abi.mla_decode(self.L, self.q_rot, c.cache, c.num_rows, c.max_len, c.n_seqs, c.rows, c.positions,
+                            self.out, self.workspace, self.ws_bytes, stream)
+
+    def run(self, stream=None):
+        self.rope(stream)
+        self.cache_update(stream)
+        self.decode(stream)
+        return self.out
+
+    def kernel_launches(self):
+        return 4 if self.call.n_seqs else 0     # rope tables, cache update, decode, merge

@@ -286,6 +286,63 @@ int da_attn_decode_paged(const da_layer* layer, const void* q_rot, const da_page
 size_t da_decode_workspace_bytes_paged(const da_layer* layer, int n_seqs, int max_positions);
 
 /*
+ * Multi-head latent attention, absorbed form (page 1, "Multi-head latent attention" and "Serving it:
+ * absorbing the up-projections"). Each token caches one row [c, k_rope] of kv_lora_rank + qk_rope_dim bf16
+ * numbers; each query head arrives mapped into latent space, q = [W_uk^T q_nope, q_rope], and decode is
+ * multi-query attention of all heads over the rows, whose first kv_lora_rank features are the values. The
+ * output is each head's latent (kv_lora_rank wide); W_uv and o_proj are applied by the caller.
+ * Supported: bf16, kv_lora_rank 512, qk_rope_dim 64 (DeepSeek-V2/V3, Kimi K2), num_heads a multiple of 8.
+ */
+typedef struct {
+    int   num_heads;       /* query heads sharing each latent row                                       */
+    int   kv_lora_rank;    /* latent (= value) width: 512                                              */
+    int   qk_rope_dim;     /* rotary width: 64                                                         */
+    float scale;           /* softmax scale: (qk_nope_head_dim + qk_rope_dim)^-0.5, times YaRN's squared */
+                           /*   temperature (0.1 mscale_all_dim ln s + 1)^2 when rope_scaling sets it  */
+    int   window;          /* 0 = full attention                                                       */
+} da_mla_layer;
+
+/*
+ * da_mla_cache_update -- writes token t's row [latent[t], rope(k_rope[t])] at (rows[t], positions[t]) and,
+ * when q is not NULL, rotates the last qk_rope_dim features of every head of q[t] in place. The rotary
+ * inputs are in DeepSeek's adjacent-pair order (x[2i], x[2i+1]); they are deinterleaved (evens, then odds)
+ * and rotated by the split-half rotation with cos/sin [n, qk_rope_dim / 2] from da_rope_tables_build:
+ * y'[i] = x[2i] c_i - x[2i+1] s_i, y'[i + r/2] = x[2i+1] c_i + x[2i] s_i.
+ *   latent [n, 512], k_rope [n, 64], q [n, H, 576] or NULL, cache [num_rows, max_len, 576] (device, bf16,
+ *   16-byte aligned). A token whose slot is out of range writes nothing and sets DA_ERR_DEVICE_INDEX.
+ */
+int da_mla_cache_update(const da_mla_layer* layer, const void* latent, const void* k_rope, int n, const int32_t* rows,
+                        const int32_t* positions, const float* cos, const float* sin, void* q, void* cache, int num_rows,
+                        int max_len, cudaStream_t stream);
+
+/*
+ * da_mla_decode -- one query token per sequence: out[s, h] = sum_j softmax_j(scale q[s,h] . row_j) row_j[:512]
+ * over rows 0 .. positions[s] of cache row rows[s] (the last w with a window). Split-K with a fixed-order
+ * merge (deterministic); the workspace is sized by da_mla_workspace_bytes.
+ *   q [S, H, 576], cache [num_rows, max_len, 576], out [S, H, 512] (device, bf16, 16-byte aligned).
+ */
+int da_mla_decode(const da_mla_layer* layer, const void* q, const void* cache, int num_rows, int max_len, int n_seqs,
+                  const int32_t* rows, const int32_t* positions, void* out, void* workspace, size_t ws_bytes,
+                  cudaStream_t stream);
+size_t da_mla_workspace_bytes(const da_mla_layer* layer, int n_seqs, int max_len);
+
+/* The same over a paged pool of latent rows: kv->k_pool [n_blocks, 1, block_size, 576] (v_pool unused; the
+ * page's pool passes one tensor as both); block_size a multiple of 64 for da_mla_decode_paged. The
+ * workspace is sized by da_mla_workspace_bytes_paged(layer, n_seqs, max_blocks * block_size). */
+int da_mla_cache_update_paged(const da_mla_layer* layer, const void* latent, const void* k_rope, int n,
+                              const int32_t* rows, const int32_t* positions, const float* cos, const float* sin,
+                              void* q, const da_paged_kv* kv, cudaStream_t stream);
+int da_mla_decode_paged(const da_mla_layer* layer, const void* q, const da_paged_kv* kv, int n_seqs,
+                        const int32_t* rows, const int32_t* positions, void* out, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream);
+size_t da_mla_workspace_bytes_paged(const da_mla_layer* layer, int n_seqs, int max_positions);
+
+/* MLAAttention's softmax scale (page 1, MLAAttention.__init__): (qk_nope_head_dim + qk_rope_head_dim)^-0.5,
+ * times (0.1 mscale_all_dim ln factor + 1)^2 when mscale_all_dim > 0 and factor > 1 (YaRN's temperature);
+ * pass 0 for either to leave it out. Host arithmetic; NaN for non-positive head dims. */
+double da_mla_softmax_scale(int qk_nope_head_dim, int qk_rope_head_dim, double factor, double mscale_all_dim);
+
+/*
  * Block manager of a paged pool (host bookkeeping only; page 1, "Sliding windows": each request maps pool
  * blocks through its own block table, and a group of windowed layers keeps its own table so that the blocks
  * every query has moved past are recycled: a windowed-only request holds at most ceil(w / block_size) + 1

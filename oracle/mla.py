@@ -86,3 +86,22 @@ def mla_decode(q, cache, rows, positions, scale, rank, window=0):
         w = e / e.sum(axis=1, keepdims=True)
         out[s] = w @ kv[:, :rank]
     return out
+
+
+def run_mla_call(call):
+    """The oracle over one MLA decode step (the call object of the workload generator, read by attribute):
+    tables for the rotary features, the cache update, the absorbed queries and the decode (float64)."""
+    from .attention import rope_inv_freq, rope_tables
+    pos = call.positions.detach().cpu().numpy().astype(np.int64)
+    rows = call.rows.detach().cpu().numpy().astype(np.int64)
+    inv, af = rope_inv_freq(call.qk_rope_head_dim, call.rope_theta, call.rope_scaling, call.max_position_embeddings)
+    cos, sin = rope_tables(pos, inv, af)
+    cache = call.cache.detach().cpu().double().numpy().copy()
+    q = call.q.detach().cpu().double().numpy()
+    mla_cache_update(call.latent.detach().cpu().double().numpy(), call.k_rope.detach().cpu().double().numpy(), rows,
+                     pos, cos, sin, cache)
+    rank = q.shape[-1] - call.qk_rope_head_dim
+    q_rot = mla_query(q[..., :rank], q[..., rank:], cos, sin)
+    scale = mla_scale(call.qk_nope_head_dim, call.qk_rope_head_dim, call.rope_scaling)
+    out = mla_decode(q_rot, cache, rows, pos, scale, rank, call.window)
+    return {"cos": cos, "sin": sin, "cache": cache, "q_rot": q_rot, "out": out}

@@ -149,7 +149,8 @@ def test_struct_layouts_match_the_header(tmp_path):
     import shutil
     if shutil.which("gcc") is None:
         pytest.skip("no C compiler")
-    structs = {"da_layer": _abi.DaLayer, "da_rope_scaling": _abi.DaRopeScaling}
+    structs = {"da_layer": _abi.DaLayer, "da_rope_scaling": _abi.DaRopeScaling, "da_paged_kv": _abi.DaPagedKv,
+               "da_mla_layer": _abi.DaMlaLayer}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "decattn.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -170,3 +171,21 @@ def test_struct_layouts_match_the_header(tmp_path):
         assert got[(cname, "size")] == ctypes.sizeof(py), cname
         for fname, _ in py._fields_:
             assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)
+
+
+def test_mla_host_checks_and_scale():
+    """MLA entry points refuse unsupported shapes before any launch; the library's softmax scale equals the
+    closed form of MLAAttention (DeepSeek-V3: 192^-0.5 times (0.1 ln 40 + 1)^2)."""
+    import math
+    L = _abi.mla_layer(16, 0.1)
+    assert _abi.LIB.da_mla_decode(ctypes.byref(L), None, None, 1, 1, 0, None, None, None, None, 0, None) == _abi.DA_OK
+    bad = _abi.mla_layer(16, 0.1, kv_lora_rank=256)
+    assert _abi.LIB.da_mla_decode(ctypes.byref(bad), None, None, 1, 1, 1, None, None, None, None, 0, None) == \
+        _abi.DA_ERR_UNSUPPORTED
+    bad = _abi.mla_layer(12, 0.1)
+    assert _abi.LIB.da_mla_decode(ctypes.byref(bad), None, None, 1, 1, 1, None, None, None, None, 0, None) == \
+        _abi.DA_ERR_UNSUPPORTED
+    assert _abi.mla_workspace_bytes(L, 4, 1000) == 4 * 16 * 4 * (512 * 4 + 8) + 256    # 256-key chunks: 4 splits
+    sc = _abi.mla_softmax_scale(128, 64, {"type": "yarn", "factor": 40, "mscale_all_dim": 1.0})
+    assert abs(sc - 192 ** -0.5 * (0.1 * math.log(40) + 1) ** 2) < 1e-15
+    assert math.isclose(_abi.mla_softmax_scale(128, 64), 192 ** -0.5, rel_tol=1e-15)
