@@ -468,11 +468,173 @@ def main_native(args):
     return 0
 
 
+# ---------------------------------------------------------------------------------------------- MLA decode
+
+MLA_WORKLOAD = "deepseek_v3_mla_decode"
+
+
+def mla_work(call):
+    """Latent rows read (one 1152-byte row per visible key) and tensor FLOPs of one MLA decode step."""
+    pos = call.positions.cpu().tolist()
+    keys = sum(min(p + 1, call.window) if call.window else p + 1 for p in pos)
+    h = call.num_heads
+    return {"decode_keys": keys, "decode_bytes": keys * 576 * 2, "decode_flops": keys * h * (576 + 512) * 2,
+            "tokens": len(pos), "prefill_flops": 0}
+
+
+def mla_oracle_sample(call, seqs):
+    """The oracle on the listed sequences of an MLA call (each against its own cache row only)."""
+    from decoder_attention_gb300 import inputs
+    from oracle import mla as OM
+    cpu = call.to("cpu") if call.q.is_cuda else call
+    t0 = time.perf_counter()
+    keys = 0
+    for s in seqs:
+        sub = inputs.MlaCall(**{k: getattr(cpu, k) for k in cpu.__dataclass_fields__})
+        r, p = int(cpu.rows[s]), int(cpu.positions[s])
+        sub.q, sub.latent, sub.k_rope = cpu.q[s:s + 1], cpu.latent[s:s + 1], cpu.k_rope[s:s + 1]
+        sub.rows = cpu.rows.new_zeros(1)
+        sub.positions, sub.seq_len = cpu.positions[s:s + 1], cpu.seq_len[s:s + 1]
+        sub.cache = cpu.cache[r:r + 1, :p + 1]
+        OM.run_mla_call(sub)
+        keys += p + 1
+    sec = time.perf_counter() - t0
+    return keys * 576 * 2 / sec / 1e9, sec, f"{len(seqs)} of {call.n_seqs} sequences, all heads; single-threaded fp64 numpy"
+
+
+def main_native_mla(args):
+    import torch
+
+    from decoder_attention_gb300 import _abi, inputs, step as S
+
+    rank, world, local = dist_init(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    call = inputs.deepseek_v3_mla_decode("full", device=dev)
+    pool = None
+    if args.kv_block > 0:
+        kp, _, table = inputs.paged_from_contiguous(call.cache[:, None], call.cache[:, None], args.kv_block, seed=1006)
+        pool = (kp, table)
+    st = S.MlaDecodeStep(call, *(pool or ()), args.kv_block) if pool else S.MlaDecodeStep(call)
+    work = mla_work(call)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    clocks.mark_start()
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        st.run()
+    torch.cuda.synchronize()
+    _abi.check_device_error()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        st.rope()
+        st.cache_update()
+        ev[i][1].record(stream)
+        st.decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.mark_end()
+    _abi.check_device_error()
+    ms = reduce_max(statistics.mean(e[0].elapsed_time(e[2]) for e in ev), world)
+    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    clock_info = clocks.stop()
+    value = work["decode_bytes"] / (ms / 1e3) / 1e9 * world
+    peaks, peak_kind = load_peaks()
+    achieved = work["decode_bytes"] / (dec_ms / 1e3) / 1e9
+    roof = {"kernel": "mla_decode_kernel + mla_merge_kernel (one da_mla_decode call)", "bound": "hbm",
+            "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "peak_kind": f"HBM copy, of {peak_kind}", "launch_ms": dec_ms,
+            "algorithmic_bytes_per_launch": work["decode_bytes"],
+            "tensor_tflops": work["decode_flops"] / (dec_ms / 1e3) / 1e12, "traffic": None}
+    e2e = None
+    if not args.no_e2e:
+        names = ["q", "latent", "k_rope", "rows", "positions", "seq_len"]
+        host_in = [getattr(call, n).cpu().pin_memory() for n in names]
+        host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+
+        def e2e_step():
+            for n, h in zip(names, host_in):
+                getattr(call, n).copy_(h, non_blocking=True)
+            st.run()
+            host_out.copy_(st.out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, world)
+        e2e = {"value": work["decode_bytes"] / (e2e_ms / 1e3) / 1e9 * world, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
+               "via": "MlaDecodeStep.run (C ABI) with pinned host inputs/outputs, one stream, L2 not flushed"}
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sec, desc = mla_oracle_sample(call, [0, 1])
+        cpu_base = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc, "seconds": sec,
+                    "host_cores": os.cpu_count()}
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": MLA_WORKLOAD, "description": call.meta["description"],
+                       "l2": "flushed (256 MB write) before every timed step, outside the step's events",
+                       "kv": (f"paged pool, {args.kv_block}-position blocks in shuffled order" if pool
+                              else "contiguous latent rows"),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tokens_per_s": work["tokens"] * world / (ms / 1e3),
+            "breakdown_ms": {"rope_and_cache_update": ms - dec_ms, "decode": dec_ms},
+            "work": work, "roofline": roof, "e2e": e2e, "gpu_launches": st.kernel_launches() * args.steps,
+            "clocks": clock_info, "cpu_baseline": cpu_base, "peaks": dict(peaks, kind=peak_kind)}))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main_reference_mla(args):
+    rank, world, _ = dist_init(args)
+    if rank != 0:
+        return 0
+    from decoder_attention_gb300 import inputs
+    call = inputs.deepseek_v3_mla_decode("full", device="cpu")
+    secs = []
+    for _ in range(args.warmup + args.steps):
+        v, sec, desc = mla_oracle_sample(call, [0])
+        secs.append(sec)
+    sec = statistics.mean(secs[args.warmup:])
+    keys = int(call.positions[0]) + 1
+    value = keys * 576 * 2 / sec / 1e9
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": {"workload": MLA_WORKLOAD, "sample": desc},
+                      "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+                      "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.oracle_sample:
         oracle_sample_child(args.workload, args.sample_kind, args.steps)
         return 0
+    if args.workload == MLA_WORKLOAD:
+        return main_reference_mla(args) if args.impl == "reference" else main_native_mla(args)
     if args.impl == "reference":
         return main_reference(args)
     return main_native(args)

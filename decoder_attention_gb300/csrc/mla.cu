@@ -11,14 +11,16 @@
 //
 // mla_decode_kernel: work unit = (key chunk, group of 32 query heads, sequence). One producer warp streams the
 // chunk's rows through a 3-stage ring of TMA-filled tiles (64 keys x 576, nine 128-byte-swizzled boxes of 64
-// features); four compute warps each serve 8 heads over every key of a tile with m16n8k16 bf16 MMAs: scores
-// S^T = K Q^T with keys on M and heads on N (the 8 heads' queries held in registers), O^T += V^T P^T with the
-// 512 value features on M (32 MMAs per 16 keys, O^T in registers). Each warp writes its heads' partial (max,
-// sum, unnormalised output); mla_merge_kernel combines the chunks in a fixed order.
+// features); four compute warps share each 16-key slab with m16n8k16 bf16 MMAs: warp w computes partial scores
+// S^T = K Q^T over features [144w, 144w + 144) for all 32 heads (its queries in registers), warp w sums the
+// partials of heads 8w .. 8w + 7 and runs their online softmax, and warp w updates O^T for value features
+// [128w, 128w + 128) of all 32 heads (O^T in registers), so every tile byte is read from shared memory once.
+// The running max moves only when it grows by more than 2^8, so O is rescaled on few slabs. Each warp writes
+// its partials (max, sum, unnormalised output); mla_merge_kernel combines the chunks in a fixed order.
 //
 // Roofline: a key costs 1152 bytes and H * (576 + 512) * 2 FLOP (278.5 KFLOP at H = 128, 242 FLOP per byte).
-// At that intensity the step needs tensor-core rates; this kernel's legacy MMAs reach ~1600 FLOP per clock
-// per SM, and each warp re-reads the tile from shared memory, so it runs well below the HBM bound at H = 128.
+// At that intensity the step needs tensor-core rates well above what the legacy MMAs give (about 1600 FLOP
+// per clock per SM, a fifth of tcgen05): this kernel is bound by MMA issue and latency, not by HBM.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -44,6 +46,11 @@ constexpr int HPW = 8;                    // heads per warp
 constexpr int HPC = CWARPS * HPW;         // heads per CTA
 constexpr int THREADS = (CWARPS + 1) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
+#ifndef DA_MLA_SACC
+#define DA_MLA_SACC 4
+#endif
+constexpr int SACC = DA_MLA_SACC;   // independent partial sums of the 36-MMA score chain
+constexpr float kGrow = 8.0f;       // log2 units: the running max may lag the true max by up to x256
 
 struct Params {
   const __nv_bfloat16* q;     // [S, H, 576]
@@ -135,9 +142,10 @@ __global__ void __launch_bounds__(256) mla_update_kernel(const UpdateParams a) {
 
 __global__ void __launch_bounds__(THREADS, 1) mla_decode_kernel(const __grid_constant__ CUtensorMap tmc,
                                                                  const Params prm) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * STAGE_BYTES);   // full[NST], empty[NST]
+  volatile int* give_up = reinterpret_cast<volatile int*>(smem + NST * STAGE_BYTES + 64);
 
   const int c = blockIdx.x, hg = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,123 +205,195 @@ __global__ void __launch_bounds__(THREADS, 1) mla_decode_kernel(const __grid_con
     return;
   }
 
-  // -------------------------------------------------------------------- consumers: 8 heads per warp
-  const int h0 = hg * HPC + warp * HPW;
-  const bool active = h0 < prm.hq;
+  // -------------------------------------------------------------------- consumers
+  // Per 16-key slab: (1) warp w computes partial scores over features [144w, 144w + 144) for all 32 heads
+  // (one A fragment feeds 4 MMAs) and stores them; (2) warp w sums the four partials of heads 8w .. 8w + 7,
+  // runs their online softmax and stores P^T fragments and rescale factors; (3) warp w updates O^T for value
+  // features [128w, 128w + 128) and all 32 heads (one A fragment feeds 4 MMAs). Every tile byte is read from
+  // shared memory once per CTA.
+  float* part = reinterpret_cast<float*>(smem + NST * STAGE_BYTES + 128);    // [4 warps][4 n-tiles][32][4]
+  uint32_t* pfrag = reinterpret_cast<uint32_t*>(part + CWARPS * 4 * 32 * 4);  // [4 n-tiles][32][2]
+  float* alpha_s = reinterpret_cast<float*>(pfrag + 4 * 32 * 2);             // [32 heads]
+  volatile int* grow_s = reinterpret_cast<volatile int*>(alpha_s + 32);       // [4]: a head's max grew
+  const int hbase = hg * HPC;
   const int gq = lane >> 2, cq = lane & 3;
-  // B operand of S^T (k = feature, n = head): b0 = Q[h0+gq][16kk + 2cq .. +1], b1 = the same at +8
-  uint32_t qb[DR / 16][2];
-  {
-    const __nv_bfloat16* qrow = prm.q + (static_cast<long long>(s) * prm.hq + (active ? h0 + gq : 0)) * DR;
+  auto sync_compute = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(CWARPS * 32) : "memory"); };
+  // B operands of the partial scores: heads hbase + 8nt + gq, features 144 warp + 16kk + 2cq (+8)
+  uint32_t qb[4][9][2];
 #pragma unroll
-    for (int kk = 0; kk < DR / 16; ++kk) {
-      qb[kk][0] = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * cq);
-      qb[kk][1] = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * cq);
+  for (int nt = 0; nt < 4; ++nt) {
+    const int h = min(hbase + nt * 8 + gq, prm.hq - 1);
+    const __nv_bfloat16* qrow = prm.q + (static_cast<long long>(s) * prm.hq + h) * DR + warp * 144;
+#pragma unroll
+    for (int kk = 0; kk < 9; ++kk) {
+      qb[nt][kk][0] = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * cq);
+      qb[nt][kk][1] = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * cq);
     }
   }
   const float zmul = prm.scale * kLog2e;
-  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
+  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};   // heads hbase + 8 warp + 2cq (+1)
   float l_run[2] = {0.f, 0.f};
-  float o[RANK / 16][4];
+  float o[8][4][4];                                   // O^T: features 128 warp + 16mt (+gq, +8), heads 8nt + 2cq (+1)
 #pragma unroll
-  for (int mt = 0; mt < RANK / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
 
   bool ok = true;
   const int mi = lane >> 3, r8 = lane & 7;
   for (int i = 0; i < n_tiles; ++i) {
     const int st = i % NST;
-    if (!mbar_wait(full_bar(st), (i / NST) & 1, prm.err)) { ok = false; break; }
+    if (!__all_sync(0xffffffffu, mbar_wait(full_bar(st), (i / NST) & 1, prm.err))) ok = false;
+    // the four warps agree on giving up, so that none waits at a barrier the others skip
+    if (threadIdx.x == 0) *give_up = 0;
+    sync_compute();
+    if (!ok && lane == 0) *give_up = 1;
+    sync_compute();
+    if (*give_up) { ok = false; break; }
     const uint32_t sT = sbase + st * STAGE_BYTES;
-    for (int slab = 0; slab < BK / 16 && active; ++slab) {
-      const int kb = k0 + i * BK + slab * 16;        // first key of the slab
-      const int n_valid = k1 - kb;                   // keys of the 16 inside the chunk (may be <= 0)
+    for (int slab = 0; slab < BK / 16; ++slab) {
+      const int kb = k0 + i * BK + slab * 16;
+      const int n_valid = k1 - kb;                   // uniform over the CTA
       if (n_valid <= 0) break;
-      const int n_lo = lo - kb;                      // keys of the 16 below the window (paged tiles only)
-      // S^T[16 keys x 8 heads]
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int n_lo = lo - kb;
+      // (1) partial scores
+      float sp[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) sp[nt][0] = sp[nt][1] = sp[nt][2] = sp[nt][3] = 0.f;
       const int kr = slab * 16 + (mi & 1) * 8 + r8;
 #pragma unroll
-      for (int kk = 0; kk < DR / 16; ++kk) {
+      for (int kk = 0; kk < 9; ++kk) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(sT + sw_off(kr, kk * 2 + (mi >> 1)), a0, a1, a2, a3);
-        mma_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-      }
-      const bool v0 = gq >= n_lo && gq < n_valid, v1 = gq + 8 >= n_lo && gq + 8 < n_valid;
-      float z[4];
+        ldsm_x4(sT + sw_off(kr, warp * 18 + kk * 2 + (mi >> 1)), a0, a1, a2, a3);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) z[e] = ((e < 2) ? v0 : v1) ? sc[e] * zmul : -CUDART_INF_F;
-      float tmax[2] = {fmaxf(z[0], z[2]), fmaxf(z[1], z[3])};
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(0xffffffffu, tmax[j], 4));
-        tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(0xffffffffu, tmax[j], 8));
-        tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(0xffffffffu, tmax[j], 16));
+        for (int nt = 0; nt < 4; ++nt) mma_16816(sp[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
       }
-      float alpha[2], muse[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float mn = fmaxf(m_run[j], tmax[j]);
-        muse[j] = (mn == -CUDART_INF_F) ? 0.f : mn;
-        alpha[j] = ex2(m_run[j] - muse[j]);
-        m_run[j] = mn;
-      }
-      const float p0 = ex2(z[0] - muse[0]), p1 = ex2(z[1] - muse[1]);
-      const float p2 = ex2(z[2] - muse[0]), p3 = ex2(z[3] - muse[1]);
-      l_run[0] = l_run[0] * alpha[0] + p0 + p2;
-      l_run[1] = l_run[1] * alpha[1] + p1 + p3;
+      for (int nt = 0; nt < 4; ++nt)
+        reinterpret_cast<float4*>(part)[(warp * 4 + nt) * 32 + lane] = make_float4(sp[nt][0], sp[nt][1], sp[nt][2], sp[nt][3]);
+      sync_compute();
+      // (2) softmax of heads 8 warp .. 8 warp + 7
+      {
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int mt = 0; mt < RANK / 16; ++mt) {
-        o[mt][0] *= alpha[0];
-        o[mt][1] *= alpha[1];
-        o[mt][2] *= alpha[0];
-        o[mt][3] *= alpha[1];
+        for (int w = 0; w < CWARPS; ++w) {
+          const float4 v = reinterpret_cast<const float4*>(part)[(w * 4 + warp) * 32 + lane];
+          sc[0] += v.x;
+          sc[1] += v.y;
+          sc[2] += v.z;
+          sc[3] += v.w;
+        }
+        const bool v0 = gq >= n_lo && gq < n_valid, v1 = gq + 8 >= n_lo && gq + 8 < n_valid;
+        float z[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) z[e] = ((e < 2) ? v0 : v1) ? sc[e] * zmul : -CUDART_INF_F;
+        float tmax[2] = {fmaxf(z[0], z[2]), fmaxf(z[1], z[3])};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(0xffffffffu, tmax[j], 4));
+          tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(0xffffffffu, tmax[j], 8));
+          tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(0xffffffffu, tmax[j], 16));
+        }
+        // the running max moves only when it grows by more than kGrow (log2 units): P then stays below
+        // 2^kGrow and O is rescaled on few slabs
+        float alpha[2] = {1.f, 1.f}, muse[2];
+        bool grow = false;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (tmax[j] > m_run[j] + kGrow) {
+            alpha[j] = ex2(m_run[j] - tmax[j]);   // 0 while m_run is -inf
+            m_run[j] = tmax[j];
+            grow = true;
+          }
+          muse[j] = (m_run[j] == -CUDART_INF_F) ? 0.f : m_run[j];
+        }
+        const float p0 = ex2(z[0] - muse[0]), p1 = ex2(z[1] - muse[1]);
+        const float p2 = ex2(z[2] - muse[0]), p3 = ex2(z[3] - muse[1]);
+        l_run[0] = l_run[0] * alpha[0] + p0 + p2;
+        l_run[1] = l_run[1] * alpha[1] + p1 + p3;
+        reinterpret_cast<uint2*>(pfrag)[warp * 32 + lane] = make_uint2(movmatrix_t(pack2(p0, p1)), movmatrix_t(pack2(p2, p3)));
+        if (gq == 0) {
+          alpha_s[warp * 8 + 2 * cq] = alpha[0];
+          alpha_s[warp * 8 + 2 * cq + 1] = alpha[1];
+        }
+        const bool any_grow = __any_sync(0xffffffffu, grow);   // written every slab, read after the barrier
+        if (lane == 0) grow_s[warp] = any_grow ? 1 : 0;
       }
-      // P^T as the B operand (k = key, n = head)
-      const uint32_t b0 = movmatrix_t(pack2(p0, p1));
-      const uint32_t b1 = movmatrix_t(pack2(p2, p3));
-      // O^T[512 x 8 heads] += V^T[512 x 16 keys] P^T
+      sync_compute();
+      // (3) O^T[128 features x 32 heads] += V^T P^T
+      uint32_t pb[4][2];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const uint2 f = reinterpret_cast<const uint2*>(pfrag)[nt * 32 + lane];
+        pb[nt][0] = f.x;
+        pb[nt][1] = f.y;
+      }
+      if (grow_s[0] | grow_s[1] | grow_s[2] | grow_s[3]) {   // some head's max grew: rescale O (uniform)
+        float al[4][2];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          al[nt][0] = alpha_s[nt * 8 + 2 * cq];
+          al[nt][1] = alpha_s[nt * 8 + 2 * cq + 1];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            o[mt][nt][0] *= al[nt][0];
+            o[mt][nt][1] *= al[nt][1];
+            o[mt][nt][2] *= al[nt][0];
+            o[mt][nt][3] *= al[nt][1];
+          }
+      }
       const int vr = slab * 16 + (mi >> 1) * 8 + r8;
       const bool partial = n_valid < 16 || n_lo > 0;
       auto in = [&](int k) { return k >= n_lo && k < n_valid; };
       const uint32_t keep01 = (in(2 * cq) ? 0x0000ffffu : 0u) | (in(2 * cq + 1) ? 0xffff0000u : 0u);
       const uint32_t keep23 = (in(2 * cq + 8) ? 0x0000ffffu : 0u) | (in(2 * cq + 9) ? 0xffff0000u : 0u);
 #pragma unroll
-      for (int mt = 0; mt < RANK / 16; ++mt) {
+      for (int mt = 0; mt < 8; ++mt) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(sT + sw_off(vr, mt * 2 + (mi & 1)), a0, a1, a2, a3);
+        ldsm_x4_t(sT + sw_off(vr, warp * 16 + mt * 2 + (mi & 1)), a0, a1, a2, a3);
         if (partial) {   // slots outside the chunk may hold anything (even NaN): 0 * NaN must not reach O
           a0 &= keep01;
           a1 &= keep01;
           a2 &= keep23;
           a3 &= keep23;
         }
-        mma_16816(o[mt], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) mma_16816(o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_bar(st));
   }
-  if (!ok || !active) return;
-  // row sums: the 8 lanes sharing cq hold disjoint keys
+  if (!ok) return;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
     l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
     l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
   }
-  // o[mt][0..1]: feature mt*16 + gq, heads 2cq, 2cq+1; o[mt][2..3]: feature + 8
+  // (max, sum) of heads 8 warp + 2cq (+1); O^T features 128 warp + 16mt + gq (+8) of heads 8nt + 2cq (+1)
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const int h = h0 + 2 * cq + j;
-    const long long slot = (static_cast<long long>(s) * prm.hq + h) * prm.n_splits + c;
-    float* wo = prm.ws_o + slot * RANK;
-#pragma unroll
-    for (int mt = 0; mt < RANK / 16; ++mt) {
-      wo[mt * 16 + gq] = o[mt][j];
-      wo[mt * 16 + gq + 8] = o[mt][2 + j];
-    }
-    if (gq == 0) prm.ws_ml[slot] = make_float2(m_run[j], l_run[j]);
+    const int h = hbase + warp * 8 + 2 * cq + j;
+    if (gq == 0 && h < prm.hq)
+      prm.ws_ml[(static_cast<long long>(s) * prm.hq + h) * prm.n_splits + c] = make_float2(m_run[j], l_run[j]);
   }
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = hbase + nt * 8 + 2 * cq + j;
+      if (h >= prm.hq) continue;
+      float* wo = prm.ws_o + ((static_cast<long long>(s) * prm.hq + h) * prm.n_splits + c) * RANK + warp * 128;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        wo[mt * 16 + gq] = o[mt][nt][j];
+        wo[mt * 16 + gq + 8] = o[mt][nt][2 + j];
+      }
+    }
 }
 
 // One block of 128 threads per (query head, sequence): combine the chunks in order, 4 features a thread.
@@ -427,7 +507,11 @@ cudaError_t launch_mla_decode(const MlaArgs& a, const MlaPlan& plan, void* works
   prm.n_blocks = a.n_blocks;
   prm.hkv = 1;
   prm.err = a.err;
-  const int smem = NST * STAGE_BYTES + 2 * NST * 8 + 1024;
+  // ring, barriers and the give-up word (128 B), exchange buffers: partial scores (8 KB), P^T fragments
+  // (1 KB), rescale factors (128 B); 1 KB of alignment slack
+  const int smem = NST * STAGE_BYTES + 128 + CWARPS * 4 * 32 * 16 + 4 * 32 * 8 + 32 * 4 + 16 + 1024;
+  static_assert(NST * STAGE_BYTES + 128 + CWARPS * 4 * 32 * 16 + 4 * 32 * 8 + 32 * 4 + 16 + 1024 <= 227 * 1024,
+                "shared memory budget");
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
