@@ -92,6 +92,10 @@ def _load():
         "da_mla_decode_paged": (I, [ctypes.POINTER(DaMlaLayer), P, ctypes.POINTER(DaPagedKv), I, P, P, P, P, Z, P]),
         "da_mla_workspace_bytes_paged": (Z, [ctypes.POINTER(DaMlaLayer), I, I]),
         "da_mla_softmax_scale": (ctypes.c_double, [I, I, ctypes.c_double, ctypes.c_double]),
+        "da_qkv_project_update": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, P, P, P, P, P, P, P, I, I, P]),
+        "da_qkv_project_update_paged": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, P, P, P, P, P,
+                                            ctypes.POINTER(DaPagedKv), P]),
+        "da_linear": (I, [P, P, P, I, I, I, P, P]),
         "da_block_pool_create": (P, [I, I, I, I, I]),
         "da_block_pool_destroy": (None, [P]),
         "da_block_pool_reserve": (I, [P, I, I, I]),
@@ -335,6 +339,23 @@ def mla_decode_paged(L, q, kv, n_seqs, rows, positions, out, workspace, ws_bytes
 
 def mla_workspace_bytes_paged(L, n_seqs, max_positions) -> int:
     return int(LIB.da_mla_workspace_bytes_paged(ctypes.byref(L), int(n_seqs), int(max_positions)))
+
+
+def qkv_project_update(L, x, w_qkv, bias, n, hidden, rows, positions, cos, sin, q_rot, k_cache, v_cache, num_rows,
+                       max_len, stream=None):
+    _check(LIB.da_qkv_project_update(ctypes.byref(L), _ptr(x), _ptr(w_qkv), _ptr(bias), int(n), int(hidden), _ptr(rows),
+                                     _ptr(positions), _ptr(cos), _ptr(sin), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache),
+                                     int(num_rows), int(max_len), _stream(stream)))
+
+
+def qkv_project_update_paged(L, x, w_qkv, bias, n, hidden, rows, positions, cos, sin, q_rot, kv, stream=None):
+    _check(LIB.da_qkv_project_update_paged(ctypes.byref(L), _ptr(x), _ptr(w_qkv), _ptr(bias), int(n), int(hidden),
+                                           _ptr(rows), _ptr(positions), _ptr(cos), _ptr(sin), _ptr(q_rot),
+                                           ctypes.byref(kv), _stream(stream)))
+
+
+def linear(x, w, bias, m, n, k, y, stream=None):
+    _check(LIB.da_linear(_ptr(x), _ptr(w), _ptr(bias), int(m), int(n), int(k), _ptr(y), _stream(stream)))
 
 
 class BlockPool:

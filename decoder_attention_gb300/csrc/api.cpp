@@ -697,4 +697,98 @@ int da_mla_decode_paged(const da_mla_layer* L, const void* q, const da_paged_kv*
                          out, workspace, ws_bytes, kv, stream);
 }
 
+// ---------------------------------------------------------------------------------------------- projections
+
+static int qkv_proj_impl(const da_layer* L, const void* x, const void* w, const float* bias, int n, int hidden,
+                         const int32_t* rows, const int32_t* positions, const float* cos, const float* sin, void* q_rot,
+                         void* k_cache, void* v_cache, int num_rows, int max_len, const da_paged_kv* kv,
+                         cudaStream_t stream) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n < 0 || hidden < 0) return fail(DA_ERR_INVALID_ARG, "n and hidden must be >= 0");
+  if (n == 0) return ok();
+  if (L->dtype != DA_BF16 || L->head_dim != 128 || L->rotary_dim != 128)
+    return fail(DA_ERR_UNSUPPORTED, "the fused projection needs bf16, head_dim 128 and all 128 dims rotated");
+  const int heads = L->num_attention_heads + 2 * L->num_key_value_heads;
+  if (heads % 2 != 0) return fail(DA_ERR_UNSUPPORTED, "Hq + 2 Hkv must be even (256-wide output tiles)");
+  if (hidden < 64 || hidden % 64 != 0) return fail(DA_ERR_UNSUPPORTED, "hidden must be a positive multiple of 64");
+  if (!x || !w || !rows || !positions || !cos || !sin || !q_rot || !k_cache || !v_cache)
+    return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(DA_ERR_INVALID_ARG, "x, w, q_rot and the caches must be 16-byte aligned");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  da::ProjArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.x = x;
+  a.w = w;
+  a.bias = bias;
+  a.m = n;
+  a.n = heads * 128;
+  a.k = hidden;
+  a.hq = L->num_attention_heads;
+  a.hkv = L->num_key_value_heads;
+  a.q_norm_w = L->q_norm_w;
+  a.k_norm_w = L->k_norm_w;
+  a.eps = static_cast<float>(L->eps);
+  a.cos = cos;
+  a.sin = sin;
+  a.rows = rows;
+  a.positions = positions;
+  a.q_rot = q_rot;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_rows = num_rows;
+  a.max_len = max_len;
+  set_paged(a, kv);
+  a.err = err;
+  cudaError_t e = da::launch_proj(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fused QKV projection launch");
+  return ok();
+}
+
+int da_qkv_project_update(const da_layer* L, const void* x, const void* w_qkv, const float* bias, int n, int hidden,
+                          const int32_t* rows, const int32_t* positions, const float* cos, const float* sin,
+                          void* q_rot, void* k_cache, void* v_cache, int num_rows, int max_len, cudaStream_t stream) {
+  return qkv_proj_impl(L, x, w_qkv, bias, n, hidden, rows, positions, cos, sin, q_rot, k_cache, v_cache, num_rows,
+                       max_len, nullptr, stream);
+}
+
+int da_qkv_project_update_paged(const da_layer* L, const void* x, const void* w_qkv, const float* bias, int n,
+                                int hidden, const int32_t* rows, const int32_t* positions, const float* cos,
+                                const float* sin, void* q_rot, const da_paged_kv* kv, cudaStream_t stream) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n == 0) return ok();
+  rc = check_paged(L, kv);
+  if (rc) return rc;
+  return qkv_proj_impl(L, x, w_qkv, bias, n, hidden, rows, positions, cos, sin, q_rot, kv->k_pool, kv->v_pool,
+                       kv->num_rows, kv->max_blocks * kv->block_size, kv, stream);
+}
+
+int da_linear(const void* x, const void* w, const float* bias, int m, int n, int k, void* y, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0) return fail(DA_ERR_INVALID_ARG, "m, n and k must be >= 0");
+  if (m == 0) return ok();
+  if (n < 256 || n % 256 != 0) return fail(DA_ERR_UNSUPPORTED, "n must be a positive multiple of 256");
+  if (k < 64 || k % 64 != 0) return fail(DA_ERR_UNSUPPORTED, "k must be a positive multiple of 64");
+  if (!x || !w || !y) return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return fail(DA_ERR_INVALID_ARG, "x, w and y must be 16-byte aligned");
+  int* err = da::error_word_ptr();
+  if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
+  da::ProjArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.x = x;
+  a.w = w;
+  a.bias = bias;
+  a.m = m;
+  a.n = n;
+  a.k = k;
+  a.y = y;
+  a.err = err;
+  cudaError_t e = da::launch_proj(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "linear (tcgen05 GEMM) launch");
+  return ok();
+}
+
 }  // extern "C"

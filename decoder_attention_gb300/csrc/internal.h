@@ -155,6 +155,33 @@ size_t mla_workspace_bytes(int hq, int n_seqs, const MlaPlan& p);
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, cudaStream_t stream);
 cudaError_t launch_mla_decode(const MlaArgs& a, const MlaPlan& plan, void* workspace, cudaStream_t stream);
 
+// Projections (tcgen05 GEMM, bf16, K a multiple of 64, N a multiple of 256): y = x w^T (+ bias), or with
+// q_rot set, the stacked q/k/v projection with norm, RoPE (head_dim 128, all dims rotated) and cache write
+// fused into the epilogue.
+struct ProjArgs {
+  const void* x;                  // [m, k]
+  const void* w;                  // [n, k]
+  const float* bias;              // [n] or NULL
+  int m, n, k;
+  void* y;                        // [m, n] (plain)
+  int hq, hkv;
+  const float* q_norm_w;
+  const float* k_norm_w;
+  float eps;
+  const float* cos;               // [m, 64]
+  const float* sin;
+  const int32_t* rows;
+  const int32_t* positions;
+  void* q_rot;                    // NULL: plain projection
+  void* k_cache;
+  void* v_cache;
+  int num_rows, max_len;
+  const int32_t* block_table;
+  int block_size, max_blocks, n_blocks;
+  int* err;
+};
+cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream);
+
 // Tensor maps (driver entry point resolved at run time; no link-time dependency on libcuda).
 bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                          uint32_t box_inner, uint32_t box_outer);

@@ -343,6 +343,31 @@ size_t da_mla_workspace_bytes_paged(const da_mla_layer* layer, int n_seqs, int m
 double da_mla_softmax_scale(int qk_nope_head_dim, int qk_rope_head_dim, double factor, double mscale_all_dim);
 
 /*
+ * da_qkv_project_update -- the projection before the step fused with the step's first half (page 1,
+ * DecoderAttention.forward: q_proj/k_proj/v_proj, q_norm/k_norm, apply_rope, cache.update): for token t,
+ *     y = x[t] W_qkv^T (+ bias),  W_qkv = [q_proj; k_proj; v_proj] stacked by rows ([(Hq + 2 Hkv) d, hidden])
+ * then for each q and k head the layer's RMSNorm (when it has norm weights) and RoPE with cos/sin[t] (from
+ * da_rope_tables_build), written to q_rot[t] and to the token's cache slot, and each v head to its slot; the
+ * q/k/v intermediate never reaches memory. One tcgen05 GEMM whose epilogue does the rest (fp32 until the
+ * bf16 stores). Supported: bf16, head_dim 128, rotary_dim 128, Hq + 2 Hkv even, hidden a multiple of 64.
+ *   x [n, hidden], w_qkv as above (device bf16, 16-byte aligned), bias [(Hq + 2 Hkv) d] fp32 or NULL; the other
+ *   arguments as for da_kv_cache_update (same slot rules and device error reporting).
+ */
+int da_qkv_project_update(const da_layer* layer, const void* x, const void* w_qkv, const float* bias, int n, int hidden,
+                          const int32_t* rows, const int32_t* positions, const float* cos, const float* sin,
+                          void* q_rot, void* k_cache, void* v_cache, int num_rows, int max_len, cudaStream_t stream);
+int da_qkv_project_update_paged(const da_layer* layer, const void* x, const void* w_qkv, const float* bias, int n,
+                                int hidden, const int32_t* rows, const int32_t* positions, const float* cos,
+                                const float* sin, void* q_rot, const da_paged_kv* kv, cudaStream_t stream);
+
+/*
+ * da_linear -- y = x w^T (+ bias) with x [m, k], w [n, k], y [m, n] bf16 (fp32 accumulation, bias fp32 [n] or
+ * NULL): the o_proj after the step (page 1, DecoderAttention.forward), on the same tcgen05 GEMM. n a multiple
+ * of 256, k a multiple of 64; pointers 16-byte aligned.
+ */
+int da_linear(const void* x, const void* w, const float* bias, int m, int n, int k, void* y, cudaStream_t stream);
+
+/*
  * Block manager of a paged pool (host bookkeeping only; page 1, "Sliding windows": each request maps pool
  * blocks through its own block table, and a group of windowed layers keeps its own table so that the blocks
  * every query has moved past are recycled: a windowed-only request holds at most ceil(w / block_size) + 1
