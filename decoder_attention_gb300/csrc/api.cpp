@@ -715,8 +715,9 @@ static int qkv_proj_impl(const da_layer* L, const void* x, const void* w, const 
   if (!x || !w || !rows || !positions || !cos || !sin || !q_rot || !k_cache || !v_cache)
     return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
-  if (!aligned16(x) || !aligned16(w) || !aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache))
-    return fail(DA_ERR_INVALID_ARG, "x, w, q_rot and the caches must be 16-byte aligned");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(bias) || !aligned16(cos) || !aligned16(sin) || !aligned16(L->q_norm_w) || !aligned16(L->k_norm_w))
+    return fail(DA_ERR_INVALID_ARG, "x, w, q_rot, the caches, bias, cos/sin and the norm weights must be 16-byte aligned");
   int* err = da::error_word_ptr();
   if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
   da::ProjArgs a;
@@ -773,7 +774,8 @@ int da_linear(const void* x, const void* w, const float* bias, int m, int n, int
   if (n < 256 || n % 256 != 0) return fail(DA_ERR_UNSUPPORTED, "n must be a positive multiple of 256");
   if (k < 64 || k % 64 != 0) return fail(DA_ERR_UNSUPPORTED, "k must be a positive multiple of 64");
   if (!x || !w || !y) return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return fail(DA_ERR_INVALID_ARG, "x, w and y must be 16-byte aligned");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(bias))
+    return fail(DA_ERR_INVALID_ARG, "x, w, y and bias must be 16-byte aligned");
   int* err = da::error_word_ptr();
   if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
   da::ProjArgs a;

@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     int it = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
-      const int mt = w % m_tiles, nt = w / m_tiles;
+      const int nt = w % n_tiles, mt = w / n_tiles;   // W (all n-tiles) stays in L2; X is read once
       for (int kb = 0; kb < kb_n; ++kb, ++it) {
         const int s = it % NS;
         if (it >= NS && !mbar_wait(B(B_EM + s), ((it / NS) - 1) & 1, prm.err)) { ok = false; break; }
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       const int buf = tcount & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(B(B_AF + buf), (tcount >> 1) & 1, prm.err))) break;
       tc_fence_after();
-      const int mt = w % m_tiles, nt = w / m_tiles;
+      const int nt = w % n_tiles, mt = w / n_tiles;   // W (all n-tiles) stays in L2; X is read once
       const int row = mt * BM + r;           // output row (token)
       const bool live = row < prm.m;
 #pragma unroll 1
@@ -165,8 +165,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         }
         if (!live) continue;
         if (prm.bias) {
+          const float4* b4 = reinterpret_cast<const float4*>(prm.bias + col0);
 #pragma unroll
-          for (int e = 0; e < 128; ++e) x[e] += prm.bias[col0 + e];
+          for (int e = 0; e < 32; ++e) {
+            const float4 b = b4[e];
+            x[4 * e] += b.x;
+            x[4 * e + 1] += b.y;
+            x[4 * e + 2] += b.z;
+            x[4 * e + 3] += b.w;
+          }
         }
         __nv_bfloat16* dst;
         if constexpr (EPI == EPI_PLAIN) {
@@ -181,17 +188,29 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
 #pragma unroll
               for (int e = 0; e < 128; ++e) ss += x[e] * x[e];
               const float inv = rsqrtf(ss * (1.f / 128.f) + prm.eps);
+              const float4* w4 = reinterpret_cast<const float4*>(nw);
 #pragma unroll
-              for (int e = 0; e < 128; ++e) x[e] = x[e] * inv * nw[e];
+              for (int e = 0; e < 32; ++e) {
+                const float4 wv = w4[e];
+                x[4 * e] *= inv * wv.x;
+                x[4 * e + 1] *= inv * wv.y;
+                x[4 * e + 2] *= inv * wv.z;
+                x[4 * e + 3] *= inv * wv.w;
+              }
             }
-            const float* cs = prm.cos + static_cast<long long>(row) * 64;
-            const float* sn = prm.sin + static_cast<long long>(row) * 64;
+            const float4* cs = reinterpret_cast<const float4*>(prm.cos + static_cast<long long>(row) * 64);
+            const float4* sn = reinterpret_cast<const float4*>(prm.sin + static_cast<long long>(row) * 64);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {   // split-half pairs (i, i + 64)
-              const float c = cs[i], s = sn[i];
-              const float a = x[i], b = x[i + 64];
-              x[i] = a * c - b * s;
-              x[i + 64] = b * c + a * s;
+            for (int i4 = 0; i4 < 16; ++i4) {   // split-half pairs (i, i + 64), four at a time
+              const float4 c4 = cs[i4], s4 = sn[i4];
+              const float cv[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int i = 4 * i4 + j;
+                const float a = x[i], b = x[i + 64];
+                x[i] = a * cv[j] - b * sv[j];
+                x[i + 64] = b * cv[j] + a * sv[j];
+              }
             }
           }
           if (is_q) {
