@@ -628,11 +628,120 @@ def main_reference_mla(args):
     return 0
 
 
+# ---------------------------------------------------------------------------------------------- attention block
+
+BLOCK_WORKLOAD = "qwen3_8b_attn_block"
+
+
+def main_native_block(args):
+    """The Qwen3-8B-shaped attention block: the fused q/k/v projection (norm, RoPE and cache write in the GEMM
+    epilogue), the prefill attention and o_proj, all through the C ABI; the unfused form (a cuBLAS GEMM for
+    q/k/v, then da_kv_cache_update; cuBLAS for o_proj) is timed beside it for comparison."""
+    import math
+
+    import torch
+
+    from decoder_attention_gb300 import _abi, inputs, step as S, work as W
+
+    rank, world, local = dist_init(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    call = inputs.make(2, scale="full", device=dev).layers[0]          # 4 x 2048 tokens, Hq 32, Hkv 8
+    n, hq, hkv, hidden = call.n_tokens, call.num_attention_heads, call.num_key_value_heads, 4096
+    g = torch.Generator(device=dev).manual_seed(3002)
+    x = torch.randn((n, hidden), generator=g, device=dev).to(torch.bfloat16)
+    w_qkv = (torch.randn(((hq + 2 * hkv) * 128, hidden), generator=g, device=dev) / math.sqrt(hidden)).to(torch.bfloat16)
+    w_o = (torch.randn((hidden, hq * 128), generator=g, device=dev) / math.sqrt(hq * 128)).to(torch.bfloat16)
+    st = S.AttentionStep(call)
+    y = torch.empty((n, hidden), dtype=torch.bfloat16, device=dev)
+    qkv = torch.empty((n, (hq + 2 * hkv) * 128), dtype=torch.bfloat16, device=dev)
+    proj_flops = 2 * n * (hq + 2 * hkv) * 128 * hidden
+    o_flops = 2 * n * hidden * hq * 128
+    attn_flops = W.layer_call_work(call)["prefill_flops"]
+
+    def fused():
+        st.rope()
+        _abi.qkv_project_update(st.L, x, w_qkv, None, n, hidden, call.tok_rows, call.tok_pos, st.cos, st.sin,
+                                st.q_rot, call.k_cache, call.v_cache, call.num_rows, call.max_len)
+
+    def unfused():
+        st.rope()
+        torch.matmul(x, w_qkv.t(), out=qkv)
+        q = qkv[:, :hq * 128].view(n, hq, 128)
+        k = qkv[:, hq * 128:(hq + hkv) * 128].view(n, hkv, 128)
+        v = qkv[:, (hq + hkv) * 128:].view(n, hkv, 128)
+        _abi.kv_cache_update(st.L, q.contiguous(), k.contiguous(), v.contiguous(), n, call.tok_rows, call.tok_pos,
+                             st.cos, st.sin, st.q_rot, call.k_cache, call.v_cache, call.num_rows, call.max_len)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    clocks.mark_start()
+
+    def timed(fn_parts, steps):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fn_parts) + 1)] for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            for j, fn in enumerate(fn_parts):
+                fn()
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize()
+        return [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(len(fn_parts))]
+
+    parts = [fused, st.prefill, lambda: _abi.linear(st.out.view(n, hq * 128), w_o, None, n, hidden, hq * 128, y)]
+    timed(parts, max(args.warmup, 3))
+    _abi.check_device_error()
+    barrier(world)
+    ms_parts = timed(parts, args.steps)
+    barrier(world)
+    clocks.mark_end()
+    _abi.check_device_error()
+    cmp_parts = [unfused, st.prefill, lambda: torch.matmul(st.out.view(n, hq * 128), w_o.t(), out=y)]
+    timed(cmp_parts, 3)
+    ms_cmp = timed(cmp_parts, max(3, min(args.steps, 20)))
+    clock_info = clocks.stop()
+    ms = reduce_max(sum(ms_parts), world)
+    total = proj_flops + attn_flops + o_flops
+    peaks, peak_kind = load_peaks()
+    achieved = proj_flops / (ms_parts[0] / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": total / (ms / 1e3) / 1e12 * world, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init projection weights)",
+            "config": {"workload": BLOCK_WORKLOAD, "description": "Qwen3-8B-shaped attention block: 4 x 2048 tokens, "
+                       "hidden 4096, fused q/k/v projection + norm + RoPE + cache write, prefill attention, o_proj",
+                       "l2": "flushed (256 MB write) before every timed step, outside the step's events",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "breakdown_ms": {"rope_tables_and_fused_qkv_projection": ms_parts[0], "prefill": ms_parts[1],
+                             "o_proj": ms_parts[2]},
+            "work": {"qkv_projection_flops": proj_flops, "attention_flops": attn_flops, "o_proj_flops": o_flops},
+            "roofline": {"kernel": "gemm_kernel<EPI_QKV> (one da_qkv_project_update call)", "bound": "tensor",
+                         "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"], "peak_kind": f"bf16 dense burst, of {peak_kind}",
+                         "launch_ms": ms_parts[0], "traffic": None},
+            "unfused_comparison_ms": {"rope_tables_cublas_qkv_and_cache_update": ms_cmp[0], "prefill": ms_cmp[1],
+                                      "cublas_o_proj": ms_cmp[2]},
+            "e2e": None, "gpu_launches": 5 * args.steps, "clocks": clock_info, "cpu_baseline": None,
+            "peaks": dict(peaks, kind=peak_kind)}))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.oracle_sample:
         oracle_sample_child(args.workload, args.sample_kind, args.steps)
         return 0
+    if args.workload == BLOCK_WORKLOAD:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the attention-block workload has no oracle arm"}))
+            return 0
+        return main_native_block(args)
     if args.workload == MLA_WORKLOAD:
         return main_reference_mla(args) if args.impl == "reference" else main_native_mla(args)
     if args.impl == "reference":
