@@ -4,10 +4,14 @@
 // q = q_proj(x), k = k_proj(x), v = v_proj(x), then q_norm/k_norm, apply_rope and cache.update; after
 // attention, o_proj. Both are a GEMM Y = X W^T (+ b) with X [M, K] and W [N, K] bf16, fp32 accumulation.
 //
-// gemm_kernel<EPI> is persistent (one CTA per SM) over 128 x 256 output tiles: a TMA producer warp streams
-// 64-wide K slices of X (128 rows) and W (256 rows) through a 4-stage ring (128-byte swizzle), one thread
-// issues tcgen05.mma (M 128, N 256, K 16) into one of two TMEM accumulators (256 columns each), and a
-// warpgroup of 128 epilogue threads (one output row each) drains the other accumulator meanwhile:
+// gemm_kernel<EPI> runs persistent clusters of two CTAs (one per SM) over 256 x 256 output tiles. CTA r of a
+// pair stages, per 64-wide K slice, X rows r*128.. of the tile and W rows r*128.. (its half of the tile's
+// columns) through a 6-stage ring (128-byte swizzle); one thread of CTA 0 issues tcgen05.mma with
+// cta_group::2 (M 256, N 256, K 16), which reads both CTAs' slices and leaves rows r*128.. of the tile in CTA
+// r's TMEM, in one of two 256-column accumulators. Per SM this moves half the operand bytes of a one-CTA
+// 128 x 256 tile through shared memory (each W column slice is staged once per pair, not per CTA), which is
+// what keeps the tensor pipe fed. A warpgroup of 128 epilogue threads per CTA (one output row each) drains
+// the other accumulator meanwhile:
 //   EPI_QKV   the tile is two 128-wide heads of the stacked q/k/v projection. Per token and head: bias, then
 //             for q and k the per-head RMSNorm (when the layer has norm weights) and the split-half RoPE with
 //             the token's cos/sin, rounded to bf16 and written to q_rot or the token's cache slot (k); v heads
@@ -25,16 +29,95 @@
 namespace da {
 namespace proj {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int NS = 4;                          // ring stages
-constexpr int A_BYTES = BM * BK * 2;           // 16 KB
-constexpr int B_BYTES = BN * BK * 2;           // 32 KB
-constexpr int STAGE = A_BYTES + B_BYTES;       // 48 KB
-constexpr int THREADS = 256;                   // warp 0 TMA, warp 1 MMA, warp 2 TMEM owner, warps 4-7 epilogue
+constexpr int BM = 128, BN = 256, BK = 64;     // per CTA: 128 rows of the pair's 256-row tile, all 256 columns
+constexpr int CLUSTER = 2;
+constexpr int NS = 6;                          // ring stages
+constexpr int A_BYTES = BM * BK * 2;           // 16 KB: this CTA's X rows
+constexpr int B_BYTES = (BN / 2) * BK * 2;     // 16 KB: this CTA's half of the W rows
+constexpr int STAGE = A_BYTES + B_BYTES;       // 32 KB
+constexpr int THREADS = 256;                   // warp 0 TMA, warp 1 MMA (CTA 0), warp 2 TMEM owner, warps 4-7 epilogue
 constexpr int EPI_QKV = 0, EPI_PLAIN = 1;
-// barriers: full[NS], empty[NS], acc_full[2], acc_empty[2]
+// barriers: full[NS] (CTA 0's count the pair's bytes), empty[NS], acc_full[2], acc_empty[2] (CTA 0's count the
+// pair's eight epilogue warps)
 constexpr int B_FU = 0, B_EM = NS, B_AF = 2 * NS, B_AE = 2 * NS + 2, N_BARS = 2 * NS + 4;
 constexpr int SMEM_BYTES = NS * STAGE + 256 + 1024;
+constexpr uint16_t PAIR = (1u << CLUSTER) - 1;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the variable at shared::cta address `a` in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a barrier that the peer CTA's threads arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer() - t0 > DA_WAIT_NS) {
+      set_error(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+// TMA tile load into this CTA's shared memory whose bytes complete on a barrier of either CTA of the pair
+// (`bar` a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D (both CTAs' TMEM) (+)= A (both CTAs' shared memory) * B (both CTAs' shared memory), M 256.
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at shared::cta offset `bar` of both CTAs when this thread's prior MMAs are done.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(PAIR)
+      : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -64,8 +147,8 @@ struct Params {
 };
 
 template <int EPI>
-__global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ CUtensorMap tma,
-                                                          const __grid_constant__ CUtensorMap tmb, const Params prm) {
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb, const Params prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -73,8 +156,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + NS * STAGE + N_BARS * 8);
   auto B = [&](int i) { return bar + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a work item is one n-tile of a pair of m-tiles; CTA `rank` of the cluster takes m-tile 2 * pair + rank
+  // (past the last m-tile it computes on the zeros TMA fills in and stores nothing)
+  const int rank = static_cast<int>(cluster_rank());
   const int m_tiles = (prm.m + BM - 1) / BM, n_tiles = prm.n / BN;
-  const int n_work = m_tiles * n_tiles;
+  const int cid = blockIdx.x / CLUSTER, n_clusters = gridDim.x / CLUSTER;
+  const int n_work = ((m_tiles + 1) / 2) * n_tiles;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -83,46 +170,49 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(B(B_AF + i), 1);
-      mbar_init(B(B_AE + i), 4);   // one arrival per epilogue warp
+      mbar_init(B(B_AE + i), 4 * CLUSTER);   // one arrival per epilogue warp of the pair
     }
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();   // both CTAs' barriers are initialised before any copy, commit or arrival reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int kb_n = prm.k / BK;
 
   if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- TMA producer (both CTAs)
     prefetch_tmap(&tma);
     prefetch_tmap(&tmb);
+    const uint32_t full0 = map_to_rank(B(B_FU), 0);   // the pair's full barriers live in CTA 0
     int it = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
-      const int nt = w % n_tiles, mt = w / n_tiles;   // W (all n-tiles) stays in L2; X is read once
+    for (int w = cid; ok && w < n_work; w += n_clusters) {
+      const int nt = w % n_tiles, mt = 2 * (w / n_tiles) + rank;   // W (all n-tiles) stays in L2; X read once
       for (int kb = 0; kb < kb_n; ++kb, ++it) {
         const int s = it % NS;
         if (it >= NS && !mbar_wait(B(B_EM + s), ((it / NS) - 1) & 1, prm.err)) { ok = false; break; }
         const uint32_t dst = sbase + s * STAGE;
-        mbar_arrive_expect_tx(B(B_FU + s), STAGE);
-        tma_load_2d(dst, &tma, B(B_FU + s), kb * BK, mt * BM);
-        tma_load_2d(dst + A_BYTES, &tmb, B(B_FU + s), kb * BK, nt * BN);
+        if (rank == 0) mbar_arrive_expect_tx(B(B_FU + s), CLUSTER * STAGE);   // both CTAs' slices
+        tma_load_2d_pair(dst, &tma, full0 + 8u * s, kb * BK, mt * BM);
+        tma_load_2d_pair(dst + A_BYTES, &tmb, full0 + 8u * s, kb * BK, nt * BN + rank * (BN / 2));
       }
     }
-    for (int j = max(0, it - NS); j < it; ++j) mbar_wait(B(B_FU + j % NS), (j / NS) & 1, prm.err);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, false);
+    // the last stages are released: the pair's MMAs have read every slice this CTA staged
+    for (int j = max(0, it - NS); j < it; ++j) mbar_wait(B(B_EM + j % NS), (j / NS) & 1, prm.err);
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------------------------------------------------------- MMA issuer (CTA 0 for the pair)
+    constexpr uint32_t idesc = idesc_bf16_f32(CLUSTER * BM, BN, false, false);
     int it = 0, tcount = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++tcount) {
+    for (int w = cid; ok && w < n_work; w += n_clusters, ++tcount) {
       const int buf = tcount & 1;
-      if (tcount >= 2 && !mbar_wait(B(B_AE + buf), ((tcount >> 1) - 1) & 1, prm.err)) break;   // buffer drained
+      if (tcount >= 2 && !mbar_wait_cluster(B(B_AE + buf), ((tcount >> 1) - 1) & 1, prm.err)) break;   // drained
       tc_fence_after();
       const uint32_t d = tmem + buf * BN;
       for (int kb = 0; kb < kb_n; ++kb, ++it) {
@@ -132,10 +222,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         const uint32_t a = sbase + s * STAGE, b = a + A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          mma_ss(d, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(b + kk * 32, 16, 1024), idesc, (kb | kk) != 0);
-        tc_commit(B(B_EM + s));   // the stage is free once these MMAs have read it
+          mma_ss_pair(d, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(b + kk * 32, 16, 1024), idesc,
+                      (kb | kk) != 0);
+        tc_commit_pair(B(B_EM + s));   // the stage is free in both CTAs once these MMAs have read it
       }
-      if (ok) tc_commit(B(B_AF + buf));
+      if (ok) tc_commit_pair(B(B_AF + buf));
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue: one output row per thread
@@ -143,12 +234,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     const int r = q4 * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     const KvLayout kvl = kv_layout(prm);
+    const uint32_t acc_empty0 = map_to_rank(B(B_AE), 0);
     int tcount = 0;
-    for (int w = blockIdx.x; w < n_work; w += gridDim.x, ++tcount) {
+    for (int w = cid; w < n_work; w += n_clusters, ++tcount) {
       const int buf = tcount & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(B(B_AF + buf), (tcount >> 1) & 1, prm.err))) break;
       tc_fence_after();
-      const int nt = w % n_tiles, mt = w / n_tiles;   // W (all n-tiles) stays in L2; X is read once
+      const int nt = w % n_tiles, mt = 2 * (w / n_tiles) + rank;
       const int row = mt * BM + r;           // output row (token)
       const bool live = row < prm.m;
 #pragma unroll 1
@@ -238,13 +330,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(B(B_AE + buf));   // this warp's lanes of the accumulator are drained
+      if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * buf);   // this warp's accumulator lanes are drained
     }
   }
   tc_fence_before();
   __syncthreads();
+  // neither CTA leaves while a copy, commit or arrival of the pair may still target its shared memory or TMEM:
+  // both epilogues have seen the last accumulators, so every MMA and copy of the pair has completed
+  cluster_sync();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, 512);
+  if (warp == 2) tmem_dealloc_pair(tmem, 512);
 }
 
 }  // namespace proj
@@ -254,7 +349,7 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream) {
   if (a.m == 0) return cudaSuccess;
   CUtensorMap tma, tmb;
   if (!encode_tmap_2d_bf16(&tma, a.x, a.k, a.m, static_cast<uint64_t>(a.k) * 2, BK, BM) ||
-      !encode_tmap_2d_bf16(&tmb, a.w, a.k, a.n, static_cast<uint64_t>(a.k) * 2, BK, BN))
+      !encode_tmap_2d_bf16(&tmb, a.w, a.k, a.n, static_cast<uint64_t>(a.k) * 2, BK, BN / 2))
     return cudaErrorInvalidValue;
   Params p;
   p.m = a.m;
@@ -289,13 +384,20 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream) {
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const long long work = static_cast<long long>((a.m + BM - 1) / BM) * (a.n / BN);
-  const int grid = static_cast<int>(std::min<long long>(work, n_sm));
-  if (qkv)
-    gemm_kernel<EPI_QKV><<<grid, THREADS, SMEM_BYTES, stream>>>(tma, tmb, p);
-  else
-    gemm_kernel<EPI_PLAIN><<<grid, THREADS, SMEM_BYTES, stream>>>(tma, tmb, p);
-  return cudaGetLastError();
+  // persistent clusters: as many as can be resident at once (a GPC with an odd number of free SMs leaves one idle)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_sm / CLUSTER * CLUSTER);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  int resident = 0;
+  e = cudaOccupancyMaxActiveClusters(&resident, qkv ? gemm_kernel<EPI_QKV> : gemm_kernel<EPI_PLAIN>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  const long long work = static_cast<long long>(((a.m + BM - 1) / BM + 1) / 2) * (a.n / BN);   // tile pairs
+  cfg.gridDim = dim3(CLUSTER * static_cast<unsigned>(std::min<long long>(work, resident)));
+  return qkv ? cudaLaunchKernelEx(&cfg, gemm_kernel<EPI_QKV>, tma, tmb, p)
+             : cudaLaunchKernelEx(&cfg, gemm_kernel<EPI_PLAIN>, tma, tmb, p);
 }
 
 }  // namespace da
