@@ -23,7 +23,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdecattn.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cpp", "block_pool.cpp", "errors.cu", "rope_kv.cu", "attn_generic.cu", "attn_decode.cu", "attn_prefill.cu", "mla.cu", "proj.cu"]
+SOURCES = ["api.cpp", "block_pool.cpp", "errors.cu", "rope_kv.cu", "attn_generic.cu", "attn_decode.cu", "attn_prefill.cu", "mla.cu", "mla_pair.cu", "proj.cu"]
 
 
 def nvcc_path():

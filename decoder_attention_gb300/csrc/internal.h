@@ -104,7 +104,7 @@ cudaError_t launch_attn_generic(const AttnArgs& a, bool bf16, cudaStream_t strea
 
 // Split-K decode (bf16, d = 128, Hq/Hkv <= 8, no key_positions).
 struct DecodePlan {
-  int chunk;      // keys per split (multiple of 64)
+  int chunk;      // keys per split (multiple of 64; of 256 for 128 heads)
   int n_splits;   // splits per (sequence, KV head) at most
 };
 // aligned: chunks start at the window start rounded down to a 64-key tile (paged pools)
@@ -147,13 +147,17 @@ struct MlaArgs {
   int* err;
 };
 struct MlaPlan {
-  int chunk;      // keys per split (multiple of 64)
+  int chunk;      // keys per split (multiple of 64; of 256 for 128 heads)
   int n_splits;
 };
 MlaPlan mla_plan(int hq, int n_seqs, int max_len, int window, bool aligned);
 size_t mla_workspace_bytes(int hq, int n_seqs, const MlaPlan& p);
 cudaError_t launch_mla_update(const MlaUpdateArgs& a, cudaStream_t stream);
 cudaError_t launch_mla_decode(const MlaArgs& a, const MlaPlan& plan, void* workspace, cudaStream_t stream);
+// 128-head layers: the tcgen05 CTA-pair kernel (chunks a multiple of 256 keys); partials in the same layout
+int mla_pair_chunk(int n_seqs, int max_keys);
+cudaError_t launch_mla_pair_decode(const MlaArgs& a, const MlaPlan& plan, float* ws_o, float2* ws_ml,
+                                   cudaStream_t stream);
 
 // Projections (tcgen05 GEMM, bf16, K a multiple of 64, N a multiple of 256): y = x w^T (+ bias), or with
 // q_rot set, the stacked q/k/v projection with norm, RoPE (head_dim 128, all dims rotated) and cache write

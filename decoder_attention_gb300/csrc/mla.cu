@@ -436,6 +436,11 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const Params prm) {
 MlaPlan mla_plan(int hq, int n_seqs, int max_len, int window, bool aligned) {
   MlaPlan p;
   const int max_keys = (window > 0 ? std::min(window, max_len) : max_len) + (aligned ? mla::BK - 1 : 0);
+  if (hq == 128) {   // CTA-pair tcgen05 kernel
+    p.chunk = mla_pair_chunk(n_seqs, max_keys);
+    p.n_splits = std::max(1, (max_keys + p.chunk - 1) / p.chunk);
+    return p;
+  }
   const long long groups = static_cast<long long>(n_seqs) * ((hq + mla::HPC - 1) / mla::HPC);
   int chunk = 256;
   // grow the chunk (fewer partials) while the grid keeps >= 2 CTAs per SM of a 152-SM part
@@ -512,15 +517,20 @@ cudaError_t launch_mla_decode(const MlaArgs& a, const MlaPlan& plan, void* works
   const int smem = NST * STAGE_BYTES + 128 + CWARPS * 4 * 32 * 16 + 4 * 32 * 8 + 32 * 4 + 16 + 1024;
   static_assert(NST * STAGE_BYTES + 128 + CWARPS * 4 * 32 * 16 + 4 * 32 * 8 + 32 * 4 + 16 + 1024 <= 227 * 1024,
                 "shared memory budget");
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+  cudaError_t e;
+  if (a.hq == 128) {
+    e = launch_mla_pair_decode(a, plan, prm.ws_o, prm.ws_ml, stream);
+  } else {
+    static bool attr_set = false;
+    if (!attr_set) {
+      e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    dim3 grid(plan.n_splits, (a.hq + HPC - 1) / HPC, a.n_seqs);
+    mla_decode_kernel<<<grid, THREADS, smem, stream>>>(tmc, prm);
+    e = cudaGetLastError();
   }
-  dim3 grid(plan.n_splits, (a.hq + HPC - 1) / HPC, a.n_seqs);
-  mla_decode_kernel<<<grid, THREADS, smem, stream>>>(tmc, prm);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mla_merge_kernel<<<dim3(a.hq, a.n_seqs), 128, 0, stream>>>(prm);
   return cudaGetLastError();
