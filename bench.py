@@ -548,7 +548,8 @@ def main_native_mla(args):
     value = work["decode_bytes"] / (ms / 1e3) / 1e9 * world
     peaks, peak_kind = load_peaks()
     achieved = work["decode_bytes"] / (dec_ms / 1e3) / 1e9
-    roof = {"kernel": "mla_decode_kernel + mla_merge_kernel (one da_mla_decode call)", "bound": "hbm",
+    kname = "mla_pair_kernel" if call.num_heads == 128 else "mla_decode_kernel"
+    roof = {"kernel": f"{kname} + mla_merge_kernel (one da_mla_decode call)", "bound": "hbm",
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "peak_kind": f"HBM copy, of {peak_kind}", "launch_ms": dec_ms,
             "algorithmic_bytes_per_launch": work["decode_bytes"],

@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "kvmap.cuh"
@@ -51,10 +53,11 @@ constexpr int M_OFF = WM_OFF + 4 * H * 4;         // running max per head (log2 
 constexpr int AL_OFF = M_OFF + H * 4;             // rescale factor per head
 constexpr int LP_OFF = AL_OFF + H * 4;            // CTA 1's sums per head (received by CTA 0)
 constexpr int BAR_OFF = LP_OFF + H * 4;
-// barriers: full[3] (CTA 0's count the pair's bytes), empty[3], s_full[2], s_free[2], p_full, o_done,
+// barriers: full[NSLOT] (CTA 0's count the pair's bytes), empty[NSLOT], s_full[2], s_free[2], p_full, o_done,
 // mx_full[2], q_full
-constexpr int B_FULL = 0, B_EMPTY = 3, B_SFULL = 6, B_SFREE = 8, B_PFULL = 10, B_ODONE = 11, B_MXFULL = 12,
-              B_QFULL = 14, N_BARS = 15;
+constexpr int B_FULL = 0, B_EMPTY = B_FULL + NSLOT, B_SFULL = B_EMPTY + NSLOT, B_SFREE = B_SFULL + 2,
+              B_PFULL = B_SFREE + 2, B_ODONE = B_PFULL + 1, B_MXFULL = B_ODONE + 1, B_QFULL = B_MXFULL + 2,
+              N_BARS = B_QFULL + 1;
 constexpr int SMEM_BYTES = BAR_OFF + N_BARS * 8 + 8 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr int THREADS = 256;   // warp 0 TMA, warp 1 MMA (CTA 0), warp 2 TMEM owner, warps 4-7 softmax
@@ -240,13 +243,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         ok = mbar_wait(bar(B_FULL + st), (q / NSLOT) & 1, prm.err);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a0 = sb + RING_OFF + st * SLOT;
-        const int nk = j < 4 ? 8 : 4;
-#pragma unroll 1
-        for (int kk = 0; kk < nk; ++kk) {
-          const uint32_t a = a0 + (kk >> 2) * ATOM + (kk & 3) * 32;
-          const uint32_t bq = sb + Q_OFF + (2 * j + (kk >> 2)) * BOX + (kk & 3) * 32;
-          mma_ss_pair(d, sdesc_sw128(a, 16, 1024), sdesc_sw128(bq, 16, 1024), id_s, (j | kk) != 0);
+        // descriptors advance by the operand's byte offset / 16 (shared memory < 256 KB: no carry out of the
+        // address field)
+        const uint64_t da = sdesc_sw128(sb + RING_OFF + st * SLOT, 16, 1024);
+        const uint64_t db = sdesc_sw128(sb + Q_OFF + 2 * j * BOX, 16, 1024);
+        if (j < 4) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss_pair(d, da + (((kk >> 2) * ATOM + (kk & 3) * 32) >> 4), db + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4),
+                        id_s, (j | kk) != 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_ss_pair(d, da + ((kk * 32) >> 4), db + ((kk * 32) >> 4), id_s, 1u);
         }
         tc_commit_pair(bar(B_EMPTY + st));
         ++q;
@@ -262,15 +270,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         ok = mbar_wait(bar(B_FULL + st), (q / NSLOT) & 1, prm.err);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a0 = sb + RING_OFF + st * SLOT;
         const uint32_t d = tmem + 256 + (v >> 1) * 128;
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk) {   // 16 keys per step: V^T and P^T are MN-major (features, heads contiguous)
-          const uint32_t a = a0 + kk * 16 * 128;
-          const uint32_t bp = sb + PT_OFF + ((v & 1) * TK + kk * 16) * 128;
-          mma_ss_pair(d, sdesc_sw128(a, ATOM, 1024), sdesc_sw128(bp, ATOM, 1024), id_o,
-                      (t > 0 || (v & 1) || kk > 0) ? 1u : 0u);
-        }
+        const uint64_t da = sdesc_sw128(sb + RING_OFF + st * SLOT, ATOM, 1024);
+        const uint64_t db = sdesc_sw128(sb + PT_OFF + (v & 1) * TK * 128, ATOM, 1024);
+        const uint32_t acc0 = (t > 0 || (v & 1)) ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)   // 16 keys per step: V^T and P^T are MN-major (features, heads contiguous)
+          mma_ss_pair(d, da + kk * 128, db + kk * 128, id_o, kk > 0 ? 1u : acc0);
         tc_commit_pair(bar(B_EMPTY + st));
         ++q;
       }
@@ -321,11 +327,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       bar_sync_softmax();
       const float cm = fmaxf(fmaxf(wm[hd], wm[H + hd]), fmaxf(wm[2 * H + hd], wm[3 * H + hd]));
       st_cluster_f32(mx_peer + (b * H + hd) * 4, cm);
-      __syncwarp();
-      if (lane == 0) {
-        fence_acq_rel_cluster();
-        mbar_arrive_cluster(mxfull_peer + 8u * b);
-      }
+      __syncwarp();   // the warp's stores precede lane 0's release-arrive
+      if (lane == 0) mbar_arrive_cluster(mxfull_peer + 8u * b);
       if (ok) ok = mbar_wait_cluster(bar(B_MXFULL + b), (t >> 1) & 1, prm.err);
       const float gm = fmaxf(cm, mx[b * H + hd]);
       const float gz = gm == -CUDART_INF_F ? -CUDART_INF_F : gm * zmul;
@@ -335,7 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         alpha = m_reg == -CUDART_INF_F ? 0.f : ex2(m_reg - gz);
         m_reg = gz;
       }
-      m_s[hd] = m_reg;
+      m_s[hd] = m_reg == -CUDART_INF_F ? 0.f : m_reg;   // -inf only while every key so far was masked
       al_s[hd] = alpha;
       const bool any_grow = bar_or_softmax(grow);
       // (2) the previous tile's O^T MMAs are done: P^T may be overwritten and O^T rescaled
@@ -359,20 +362,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tmem_wait_st();
         }
       }
-      // (3) probabilities: P^T rows of this CTA's keys; heads [0, 64) live in CTA 0, [64, 128) in CTA 1
+      // (3) probabilities: P^T rows of this CTA's keys; heads [0, 64) live in CTA 0, [64, 128) in CTA 1. The
+      // other CTA's heads go first, so that its remote stores have drained by the fence below.
       const int prow = r * TK + kr;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      auto chunk = [&](auto jc) {
+        constexpr int j = decltype(jc)::value;
         uint32_t v[32];
         tmem_ld32(s_t + j * 32, v);
         tmem_wait_ld();
+        const float4* m4 = reinterpret_cast<const float4*>(m_s + j * 32);
         float x[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float m = m_s[j * 32 + e];
-          x[e] = valid ? ex2(fmaf(__uint_as_float(v[e]), zmul, -(m == -CUDART_INF_F ? 0.f : m))) : 0.f;
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 m = m4[e4];
+          const float mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            x[4 * e4 + k] = valid ? ex2(fmaf(__uint_as_float(v[4 * e4 + k]), zmul, -mm[k])) : 0.f;
         }
-        const uint32_t dst = ((j >> 1) == r ? pt_own : pt_peer) + prow * 128;
+        const bool own = (j >> 1) == r;
+        const uint32_t dst = (own ? pt_own : pt_peer) + prow * 128;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 pk;
@@ -381,18 +390,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           pk.z = pack2(x[8 * i + 4], x[8 * i + 5]);
           pk.w = pack2(x[8 * i + 6], x[8 * i + 7]);
           const uint32_t a = dst + ((((j & 1) * 4 + i) ^ (prow & 7)) << 4);
-          if ((j >> 1) == r)
+          if (own)
             st_shared_v4(a, pk);
           else
             st_cluster_v4(a, pk);
         }
         l_acc[j] += warp_colreduce32<false>(x, lane);
+      };
+      using I0 = std::integral_constant<int, 0>;
+      using I1 = std::integral_constant<int, 1>;
+      using I2 = std::integral_constant<int, 2>;
+      using I3 = std::integral_constant<int, 3>;
+      if (r == 0) {
+        chunk(I2{});
+        chunk(I3{});
+        chunk(I0{});
+        chunk(I1{});
+      } else {
+        chunk(I0{});
+        chunk(I1{});
+        chunk(I2{});
+        chunk(I3{});
       }
       tc_fence_before();
       fence_proxy_async_cluster();   // this thread's P^T stores, both CTAs, before the tensor core reads them
       __syncwarp();
       if (lane == 0) {
-        fence_acq_rel_cluster();
         mbar_arrive_cluster(sfree0 + 8u * b);   // this S^T buffer may be overwritten
         mbar_arrive_cluster(pfull0);
       }
