@@ -60,7 +60,7 @@ constexpr int B_FULL = 0, B_EMPTY = B_FULL + NSLOT, B_SFULL = B_EMPTY + NSLOT, B
               N_BARS = B_QFULL + 1;
 constexpr int SMEM_BYTES = BAR_OFF + N_BARS * 8 + 8 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-constexpr int THREADS = 256;   // warp 0 TMA, warp 1 MMA (CTA 0), warp 2 TMEM owner, warps 4-7 softmax
+constexpr int THREADS = 384;   // warp 0 TMA, warp 1 MMA (CTA 0), warp 2 TMEM owner, warps 4-11 softmax
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kGrow = 8.0f;  // log2 units: the running max may lag the true max by up to x256
 
@@ -78,12 +78,12 @@ struct Params {
   int* err;
 };
 
-__device__ __forceinline__ void bar_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void bar_sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ bool bar_or_softmax(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "bar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(v ? 1u : 0u)
       : "memory");
@@ -152,10 +152,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 8);    // four softmax warps in each CTA
+      mbar_init(bar(B_SFREE + i), 16);   // eight softmax warps in each CTA
       mbar_init(bar(B_MXFULL + i), 4);   // the peer's four softmax warps
     }
-    mbar_init(bar(B_PFULL), 8);
+    mbar_init(bar(B_PFULL), 16);
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_QFULL), 1);
     fence_mbar_init();
@@ -290,20 +290,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (ok) o_tile(n_tiles - 1);
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax and epilogue (both CTAs)
-    const int q4 = warp - 4;                // TMEM lane quarter
+    // eight warps: warp w reads TMEM lane quarter w % 4 (its 32 keys of S^T, its 32 features of O^T) and handles
+    // heads [64 hh, +64), hh = (w - 4) / 4; threads 0..127 of the group keep the running max of one head each
+    const int q4 = warp & 3;
+    const int hh = (warp - 4) >> 2;
     const int kr = q4 * 32 + lane;          // key row of S^T, feature row of O^T
-    const int hd = threadIdx.x - 128;       // head this thread keeps the running max of
+    const int tid = threadIdx.x - 128;
+    const bool head_owner = tid < H;
+    const int hd = tid & (H - 1);
     const uint32_t lane_addr = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t peer = static_cast<uint32_t>(r ^ 1);
     const uint32_t sfree0 = map_to_rank(bar(B_SFREE), 0), pfull0 = map_to_rank(bar(B_PFULL), 0);
     const uint32_t mx_peer = map_to_rank(sb + MX_OFF, peer), mxfull_peer = map_to_rank(bar(B_MXFULL), peer);
-    const uint32_t pt_own = sb + PT_OFF, pt_peer = map_to_rank(sb + PT_OFF, peer);
+    // P^T of heads [64 r, +64) lives in CTA r: this warp's probabilities go to the other CTA when hh != r
+    const bool remote = hh != r;
+    const uint32_t pt_dst = remote ? map_to_rank(sb + PT_OFF, peer) : sb + PT_OFF;
     float* mx = reinterpret_cast<float*>(smem + MX_OFF);
     float* wm = reinterpret_cast<float*>(smem + WM_OFF);
     float* m_s = reinterpret_cast<float*>(smem + M_OFF);
     float* al_s = reinterpret_cast<float*>(smem + AL_OFF);
     const float zmul = prm.scale * kLog2e;
-    float l_acc[4] = {0.f, 0.f, 0.f, 0.f};   // this warp's keys, heads 32 j + lane
+    float l_acc[2] = {0.f, 0.f};   // this warp's keys, heads 64 hh + 32 jj + lane
     bool ok = true;
 #pragma unroll 1
     for (int t = 0; t < n_tiles; ++t) {
@@ -312,46 +319,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const bool valid = key >= lo && key < k1;
       if (ok) ok = mbar_wait_cluster(bar(B_SFULL + b), (t >> 1) & 1, prm.err);
       tc_fence_after();
-      const uint32_t s_t = tmem + lane_addr + b * 128;
+      const uint32_t s_t = tmem + lane_addr + b * 128 + hh * 64;
       // (1) per-head maximum over this CTA's 128 keys, then over the pair
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int jj = 0; jj < 2; ++jj) {
         uint32_t v[32];
-        tmem_ld32(s_t + j * 32, v);
+        tmem_ld32(s_t + jj * 32, v);
         tmem_wait_ld();
         float x[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = valid ? __uint_as_float(v[e]) : -CUDART_INF_F;
-        wm[q4 * H + j * 32 + lane] = warp_colreduce32<true>(x, lane);
+        wm[q4 * H + hh * 64 + jj * 32 + lane] = warp_colreduce32<true>(x, lane);
       }
       bar_sync_softmax();
-      const float cm = fmaxf(fmaxf(wm[hd], wm[H + hd]), fmaxf(wm[2 * H + hd], wm[3 * H + hd]));
-      st_cluster_f32(mx_peer + (b * H + hd) * 4, cm);
-      __syncwarp();   // the warp's stores precede lane 0's release-arrive
-      if (lane == 0) mbar_arrive_cluster(mxfull_peer + 8u * b);
-      if (ok) ok = mbar_wait_cluster(bar(B_MXFULL + b), (t >> 1) & 1, prm.err);
-      const float gm = fmaxf(cm, mx[b * H + hd]);
-      const float gz = gm == -CUDART_INF_F ? -CUDART_INF_F : gm * zmul;
-      const bool grow = gz > m_reg + kGrow;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = m_reg == -CUDART_INF_F ? 0.f : ex2(m_reg - gz);
-        m_reg = gz;
+      bool grow = false;
+      if (head_owner) {
+        const float cm = fmaxf(fmaxf(wm[hd], wm[H + hd]), fmaxf(wm[2 * H + hd], wm[3 * H + hd]));
+        st_cluster_f32(mx_peer + (b * H + hd) * 4, cm);
+        __syncwarp();   // the warp's stores precede lane 0's release-arrive
+        if (lane == 0) mbar_arrive_cluster(mxfull_peer + 8u * b);
+        if (ok) ok = mbar_wait_cluster(bar(B_MXFULL + b), (t >> 1) & 1, prm.err);
+        const float gm = fmaxf(cm, mx[b * H + hd]);
+        const float gz = gm == -CUDART_INF_F ? -CUDART_INF_F : gm * zmul;
+        grow = gz > m_reg + kGrow;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = m_reg == -CUDART_INF_F ? 0.f : ex2(m_reg - gz);
+          m_reg = gz;
+        }
+        m_s[hd] = m_reg == -CUDART_INF_F ? 0.f : m_reg;   // -inf only while every key so far was masked
+        al_s[hd] = alpha;
       }
-      m_s[hd] = m_reg == -CUDART_INF_F ? 0.f : m_reg;   // -inf only while every key so far was masked
-      al_s[hd] = alpha;
       const bool any_grow = bar_or_softmax(grow);
       // (2) the previous tile's O^T MMAs are done: P^T may be overwritten and O^T rescaled
       if (t >= 1 && ok) ok = mbar_wait(bar(B_ODONE), (t - 1) & 1, prm.err);
       tc_fence_after();
       if (any_grow) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) l_acc[j] *= al_s[j * 32 + lane];
+        for (int jj = 0; jj < 2; ++jj) l_acc[jj] *= al_s[hh * 64 + jj * 32 + lane];
         if (t >= 1) {
 #pragma unroll 1
-          for (int cb = 0; cb < 8; ++cb) {   // 2 feature blocks x 4 column groups of 32 heads
-            const uint32_t o_t = tmem + lane_addr + 256 + cb * 32;
-            const int h0 = (cb & 3) * 32;
+          for (int cb = 0; cb < 4; ++cb) {   // 2 feature blocks x this warp's 2 column groups of 32 heads
+            const int h0 = hh * 64 + (cb & 1) * 32;
+            const uint32_t o_t = tmem + lane_addr + 256 + (cb >> 1) * 128 + h0;
             uint32_t v[32];
             tmem_ld32(o_t, v);
             tmem_wait_ld();
@@ -362,15 +372,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tmem_wait_st();
         }
       }
-      // (3) probabilities: P^T rows of this CTA's keys; heads [0, 64) live in CTA 0, [64, 128) in CTA 1. The
-      // other CTA's heads go first, so that its remote stores have drained by the fence below.
+      // (3) probabilities of this warp's heads for this CTA's keys: P^T rows r * 128 + key
       const int prow = r * TK + kr;
-      auto chunk = [&](auto jc) {
-        constexpr int j = decltype(jc)::value;
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
         uint32_t v[32];
-        tmem_ld32(s_t + j * 32, v);
+        tmem_ld32(s_t + jj * 32, v);
         tmem_wait_ld();
-        const float4* m4 = reinterpret_cast<const float4*>(m_s + j * 32);
+        const float4* m4 = reinterpret_cast<const float4*>(m_s + hh * 64 + jj * 32);
         float x[32];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
@@ -380,8 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           for (int k = 0; k < 4; ++k)
             x[4 * e4 + k] = valid ? ex2(fmaf(__uint_as_float(v[4 * e4 + k]), zmul, -mm[k])) : 0.f;
         }
-        const bool own = (j >> 1) == r;
-        const uint32_t dst = (own ? pt_own : pt_peer) + prow * 128;
+        const uint32_t dst = pt_dst + prow * 128;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 pk;
@@ -389,31 +397,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           pk.y = pack2(x[8 * i + 2], x[8 * i + 3]);
           pk.z = pack2(x[8 * i + 4], x[8 * i + 5]);
           pk.w = pack2(x[8 * i + 6], x[8 * i + 7]);
-          const uint32_t a = dst + ((((j & 1) * 4 + i) ^ (prow & 7)) << 4);
-          if (own)
-            st_shared_v4(a, pk);
-          else
+          const uint32_t a = dst + (((jj * 4 + i) ^ (prow & 7)) << 4);
+          if (remote)
             st_cluster_v4(a, pk);
+          else
+            st_shared_v4(a, pk);
         }
-        l_acc[j] += warp_colreduce32<false>(x, lane);
-      };
-      using I0 = std::integral_constant<int, 0>;
-      using I1 = std::integral_constant<int, 1>;
-      using I2 = std::integral_constant<int, 2>;
-      using I3 = std::integral_constant<int, 3>;
-      if (r == 0) {
-        chunk(I2{});
-        chunk(I3{});
-        chunk(I0{});
-        chunk(I1{});
-      } else {
-        chunk(I0{});
-        chunk(I1{});
-        chunk(I2{});
-        chunk(I3{});
+        l_acc[jj] += warp_colreduce32<false>(x, lane);
       }
       tc_fence_before();
-      fence_proxy_async_cluster();   // this thread's P^T stores, both CTAs, before the tensor core reads them
+      // this thread's P^T stores before the tensor core reads them (the other CTA's memory: cluster scope)
+      if (remote)
+        fence_proxy_async_cluster();
+      else
+        fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_cluster(sfree0 + 8u * b);   // this S^T buffer may be overwritten
@@ -425,28 +422,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_after();
     float* ws = prm.ws_o + (static_cast<long long>(s) * H * prm.n_splits + c) * 512;
 #pragma unroll 1
-    for (int cb = 0; cb < 8; ++cb) {
-      const int f = (cb >> 2) * 256 + r * 128 + kr;
-      const int h0 = (cb & 3) * 32;
+    for (int cb = 0; cb < 4; ++cb) {
+      const int f = (cb >> 1) * 256 + r * 128 + kr;
+      const int h0 = hh * 64 + (cb & 1) * 32;
       uint32_t v[32];
-      tmem_ld32(tmem + lane_addr + 256 + cb * 32, v);
+      tmem_ld32(tmem + lane_addr + 256 + (cb >> 1) * 128 + h0, v);
       tmem_wait_ld();
 #pragma unroll
       for (int e = 0; e < 32; ++e)
         ws[static_cast<long long>(h0 + e) * prm.n_splits * 512 + f] = __uint_as_float(v[e]);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) wm[q4 * H + j * 32 + lane] = l_acc[j];
+    for (int jj = 0; jj < 2; ++jj) wm[q4 * H + hh * 64 + jj * 32 + lane] = l_acc[jj];
     bar_sync_softmax();
-    l_cta = wm[hd] + wm[H + hd] + wm[2 * H + hd] + wm[3 * H + hd];
-    if (r == 1) st_cluster_f32(map_to_rank(sb + LP_OFF + hd * 4, 0), l_cta);
+    if (head_owner) {
+      l_cta = wm[hd] + wm[H + hd] + wm[2 * H + hd] + wm[3 * H + hd];
+      if (r == 1) st_cluster_f32(map_to_rank(sb + LP_OFF + hd * 4, 0), l_cta);
+    }
   }
   tc_fence_before();
   __syncthreads();
   // every MMA, copy, commit and remote store of the pair has landed before either CTA passes this point
   cluster_sync();
   tc_fence_after();
-  if (r == 0 && warp >= 4) {
+  if (r == 0 && warp >= 4 && warp < 8) {
     const int hd = threadIdx.x - 128;
     const float l_peer = reinterpret_cast<const float*>(smem + LP_OFF)[hd];
     prm.ws_ml[(static_cast<long long>(s) * H + hd) * prm.n_splits + c] = make_float2(m_reg, l_cta + l_peer);
