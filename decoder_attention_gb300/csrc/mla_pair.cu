@@ -52,12 +52,15 @@ constexpr int WM_OFF = MX_OFF + 2 * H * 4;        // per-warp column maxima / su
 constexpr int M_OFF = WM_OFF + 4 * H * 4;         // running max per head (log2 units)
 constexpr int AL_OFF = M_OFF + H * 4;             // rescale factor per head
 constexpr int LP_OFF = AL_OFF + H * 4;            // CTA 1's sums per head (received by CTA 0)
-constexpr int BAR_OFF = LP_OFF + H * 4;
+constexpr int FILL_OFF = LP_OFF + H * 4;           // boundary group: [2][4] int (destination, first key)
+constexpr int BAR_OFF = FILL_OFF + 2 * 4 * 4;
 // barriers: full[NSLOT] (CTA 0's count the pair's bytes), empty[NSLOT], s_full[2], s_free[2], p_full, o_done,
-// mx_full[2], q_full
+// mx_full[2], q_full, split[2] (CTA 0's: the hand-filled value rows of the group holding the last visible key
+// are in place in both CTAs, one barrier for each of the two value slots that carry it), fill[2] (the producer
+// hands such a slot to the filling warp)
 constexpr int B_FULL = 0, B_EMPTY = B_FULL + NSLOT, B_SFULL = B_EMPTY + NSLOT, B_SFREE = B_SFULL + 2,
               B_PFULL = B_SFREE + 2, B_ODONE = B_PFULL + 1, B_MXFULL = B_ODONE + 1, B_QFULL = B_MXFULL + 2,
-              N_BARS = B_QFULL + 1;
+              B_SPLIT = B_QFULL + 1, B_FILL = B_SPLIT + 2, N_BARS = B_FILL + 2;
 constexpr int SMEM_BYTES = BAR_OFF + N_BARS * 8 + 8 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr int THREADS = 384;   // warp 0 TMA, warp 1 MMA (CTA 0), warp 2 TMEM owner, warps 4-11 softmax
@@ -75,6 +78,7 @@ struct Params {
   const int32_t* block_table;
   int block_size, max_blocks, n_blocks;
   int hkv;
+  int oob_row;                      // first row past the cache (TMA reads zeros there)
   int* err;
 };
 
@@ -118,6 +122,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The 64-key group starting at key g holds the last visible key p and keys past it, which were never written.
+__device__ __forceinline__ bool holds_last(int g, int p) { return g <= p && g + 63 > p; }
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mla_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmc,
                     const Params prm) {
@@ -158,6 +165,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(bar(B_PFULL), 16);
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_SPLIT), 2);        // both CTAs' producer warps
+    mbar_init(bar(B_SPLIT + 1), 2);
+    mbar_init(bar(B_FILL), 1);
+    mbar_init(bar(B_FILL + 1), 1);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -172,8 +183,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   float m_reg = -CUDART_INF_F, l_cta = 0.f;   // softmax threads: head (threadIdx.x - 128)
 
+  // the 64-key group holding the last visible key p, when it lies in this chunk and holds keys past p (whose
+  // value rows were never written): warp 3 fills its two value slots by hand
+  const bool has_split = k1 == p + 1 && ((p - k0) & 63) != 63;
+  int* fill = reinterpret_cast<int*>(smem + FILL_OFF);
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
+    // Groups with no visible key, value groups past p and missing blocks are read from past the end of the
+    // cache, where TMA fills zeros: no unwritten slot reaches O through 0 * NaN. The value rows of the group
+    // holding p go to warp 3 instead (rows up to p copied, the rest zero).
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmc);
     const uint32_t full0 = map_to_rank(bar(B_FULL), 0);
@@ -183,14 +201,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tma_load_2d_pair(sb + Q_OFF + b * BOX, &tmq, map_to_rank(bar(B_QFULL), 0), b * 64, s * H + r * HH);
     const KvLayout kvl = kv_layout(prm);
     const long long plane = static_cast<long long>(row) * prm.max_len;
-    // first cache row of the 64-key group starting at key g (a group past the visible keys may be unmapped:
-    // it is read from row 0 and masked)
-    auto group_row = [&](int g) -> int {
-      if (!paged) return static_cast<int>(plane + g);
-      long long sl = kv_slot(kvl, row, g);
+    // cache rows of the four 64-key groups of tile t (-1: outside the cache or a missing block), looked up once
+    // per tile with independent loads and kept for the tile's value slots, which come a tile later
+    long long ge[4], go[4];   // even and odd tiles, in registers (selected, never indexed at run time)
+    auto lookup = [&](int t) {
+      long long v[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int g = k0 + t * PT + m * 64;
+        v[m] = paged ? kv_slot(kvl, row, g) : plane + g;
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        if (t & 1) go[m] = v[m];
+        else ge[m] = v[m];
+      }
+    };
+    auto group_row = [&](int t, int m, bool is_v) -> int {
+      const int g = k0 + t * PT + m * 64;
+      if (g + 63 < lo || (is_v && g > p)) return prm.oob_row;
+      const long long* gs = (t & 1) ? go : ge;
+      const long long sl = m == 0 ? gs[0] : m == 1 ? gs[1] : m == 2 ? gs[2] : gs[3];
       if (sl < 0) {
-        if (g <= p && g + 63 >= lo) set_error(prm.err, kErrIndex);
-        sl = 0;
+        if (g <= p) set_error(prm.err, kErrIndex);
+        return prm.oob_row;
       }
       return static_cast<int>(sl);
     };
@@ -204,18 +238,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (q >= NSLOT && !(ok = mbar_wait(bar(B_EMPTY + st), ((q / NSLOT) - 1) & 1, prm.err))) return;
       const uint32_t dst = sb + RING_OFF + st * SLOT;
       const int nblk = (!is_v && j == 4) ? 1 : 2;
-      if (r == 0) mbar_arrive_expect_tx(bar(B_FULL + st), 2 * nblk * ATOM);
       const int key0 = k0 + t * PT + (is_v ? (j & 1) : r) * TK;
       const int f0 = is_v ? ((j >> 1) * 4 + r * 2) : 2 * j;   // first 64-feature block
-      const int g0 = group_row(key0), g1 = group_row(key0 + 64);
+      const bool sp0 = is_v && holds_last(key0, p), sp1 = is_v && holds_last(key0 + 64, p);
+      // both CTAs skip the same groups (the tile and p are common), so CTA 0 can count the pair's bytes
+      if (r == 0) mbar_arrive_expect_tx(bar(B_FULL + st), 2 * nblk * (2 - sp0 - sp1) * BOX);
+      const int m0 = (is_v ? (j & 1) : r) * 2;   // the slot's first group within the tile
+      const int g0 = group_row(t, m0, is_v), g1 = group_row(t, m0 + 1, is_v);
       for (int blk = 0; blk < nblk; ++blk) {
-        tma_load_2d_pair(dst + blk * ATOM, &tmc, full0 + 8u * st, (f0 + blk) * 64, g0);
-        tma_load_2d_pair(dst + blk * ATOM + BOX, &tmc, full0 + 8u * st, (f0 + blk) * 64, g1);
+        if (!sp0) tma_load_2d_pair(dst + blk * ATOM, &tmc, full0 + 8u * st, (f0 + blk) * 64, g0);
+        if (!sp1) tma_load_2d_pair(dst + blk * ATOM + BOX, &tmc, full0 + 8u * st, (f0 + blk) * 64, g1);
+      }
+      if (sp0 || sp1) {   // this CTA's copy of the group lands on a local barrier; warp 3 then clears rows past p
+        const int fb = j >> 1, hr = sp1 ? 1 : 0;
+        fill[fb * 4 + 0] = static_cast<int>(dst + hr * BOX);
+        fill[fb * 4 + 1] = key0 + hr * 64;
+        mbar_arrive_expect_tx(bar(B_FILL + fb), 2 * BOX);
+        const int gr = group_row(t, m0 + hr, false);
+        for (int blk = 0; blk < 2; ++blk)
+          tma_load_2d(dst + hr * BOX + blk * ATOM, &tmc, bar(B_FILL + fb), (f0 + blk) * 64, gr);
       }
       ++q;
     };
 #pragma unroll 1
     for (int t = 0; t < n_tiles; ++t) {
+      lookup(t);
 #pragma unroll 1
       for (int j = 0; j < 5; ++j) issue(t, false, j);
       if (t >= 1)
@@ -226,6 +273,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int v = 0; v < 4; ++v) issue(n_tiles - 1, true, v);
     // the pair's MMAs have read every slot this CTA filled (so no copy of it is still in flight)
     for (int i = max(0, q - NSLOT); i < q; ++i) mbar_wait(bar(B_EMPTY + i % NSLOT), (i / NSLOT) & 1, prm.err);
+  } else if (warp == 3 && has_split) {
+    // ------------------------------------------------------------------ boundary fill (both CTAs)
+    // the group's value rows have landed (this CTA's copy, local barrier): zero the rows of keys past p
+    const uint32_t split0 = map_to_rank(bar(B_SPLIT), 0);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+    for (int fb = 0; fb < 2; ++fb) {
+      if (!mbar_wait(bar(B_FILL + fb), 0, prm.err)) break;   // the producer gave up before this slot
+      const uint32_t dst = static_cast<uint32_t>(fill[fb * 4 + 0]);
+      const int first = p - fill[fb * 4 + 1] + 1;   // rows [first, 64) hold keys past p (whole 128-byte rows)
+#pragma unroll 1
+      for (int e = first * 8 + lane; e < 64 * 8; e += 32) {
+        st_shared_v4(dst + e * 16, zero);
+        st_shared_v4(dst + ATOM + e * 16, zero);
+      }
+      fence_proxy_async_smem();   // generic stores before the tensor core reads them
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(split0 + 8u * fb);
+    }
   } else if (warp == 1 && lane == 0 && r == 0) {
     // ------------------------------------------------------------------ MMA issuer (CTA 0 for the pair)
     constexpr uint32_t id_s = idesc_bf16_f32(256, 128, false, false);
@@ -269,6 +335,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int st = q % NSLOT;
         ok = mbar_wait(bar(B_FULL + st), (q / NSLOT) & 1, prm.err);
         if (!ok) break;
+        const int key0 = k0 + t * PT + (v & 1) * TK;
+        if (holds_last(key0, p) || holds_last(key0 + 64, p)) {   // used once per CTA pair: phase 0
+          ok = mbar_wait_cluster(bar(B_SPLIT + (v >> 1)), 0, prm.err);
+          if (!ok) break;
+        }
         tc_fence_after();
         const uint32_t d = tmem + 256 + (v >> 1) * 128;
         const uint64_t da = sdesc_sw128(sb + RING_OFF + st * SLOT, ATOM, 1024);
@@ -470,6 +541,7 @@ cudaError_t launch_mla_pair_decode(const MlaArgs& a, const MlaPlan& plan, float*
   CUtensorMap tmq, tmc;
   const uint64_t rows_total = a.block_table ? static_cast<uint64_t>(a.n_blocks) * a.block_size
                                             : static_cast<uint64_t>(a.num_rows) * a.max_len;
+  if (rows_total + 512 > 0x7fffffffULL) return cudaErrorInvalidValue;   // TMA row coordinates are int32
   if (!encode_tmap_2d_bf16(&tmq, a.q, DR, static_cast<uint64_t>(a.n_seqs) * H, DR * 2, 64, HH) ||
       !encode_tmap_2d_bf16(&tmc, a.cache, DR, rows_total, DR * 2, 64, 64))
     return cudaErrorInvalidValue;
@@ -490,6 +562,7 @@ cudaError_t launch_mla_pair_decode(const MlaArgs& a, const MlaPlan& plan, float*
   prm.max_blocks = a.max_blocks;
   prm.n_blocks = a.n_blocks;
   prm.hkv = 1;
+  prm.oob_row = static_cast<int>(rows_total);
   prm.err = a.err;
   static bool attr_set = false;
   if (!attr_set) {
