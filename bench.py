@@ -553,7 +553,8 @@ def main_native_mla(args):
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "peak_kind": f"HBM copy, of {peak_kind}", "launch_ms": dec_ms,
             "algorithmic_bytes_per_launch": work["decode_bytes"],
-            "tensor_tflops": work["decode_flops"] / (dec_ms / 1e3) / 1e12, "traffic": None}
+            "tensor_tflops": work["decode_flops"] / (dec_ms / 1e3) / 1e12,
+            "traffic": load_traffic(kname, MLA_WORKLOAD) if not args.kv_block else None}
     e2e = None
     if not args.no_e2e:
         names = ["q", "latent", "k_rope", "rows", "positions", "seq_len"]
@@ -722,7 +723,7 @@ def main_native_block(args):
             "roofline": {"kernel": "gemm_kernel<EPI_QKV> (one da_qkv_project_update call)", "bound": "tensor",
                          "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"], "peak_kind": f"bf16 dense burst, of {peak_kind}",
-                         "launch_ms": ms_parts[0], "traffic": None},
+                         "launch_ms": ms_parts[0], "traffic": load_traffic("gemm_kernel", BLOCK_WORKLOAD)},
             "unfused_comparison_ms": {"rope_tables_cublas_qkv_and_cache_update": ms_cmp[0], "prefill": ms_cmp[1],
                                       "cublas_o_proj": ms_cmp[2]},
             "e2e": None, "gpu_launches": 5 * args.steps, "clocks": clock_info, "cpu_baseline": None,
