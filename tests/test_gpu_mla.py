@@ -132,3 +132,31 @@ def test_mla_128_heads_multi_tile_rescale(cuda, window, block):
     out = st.out.cpu()
     for s in (0, 1, 2, 5, 7, 9, 10, 11):
         _close_scaled(out[s:s + 1], OM.run_mla_call(_sub_call(call, s))["out"])
+
+
+@pytest.mark.parametrize("heads", [16, 128])
+def test_mla_invalid_sequence(cuda, heads):
+    """A sequence whose cache row is out of range: the device error word says so, its outputs are zero and the
+    other sequences are unaffected (legacy and CTA-pair kernels)."""
+    from decoder_attention_gb300 import _abi, inputs
+    call = inputs.deepseek_v3_mla_decode("small")
+    if heads != call.num_heads:
+        g = torch.Generator().manual_seed(heads)
+        call.q = (torch.randn((call.n_seqs, heads, 576), generator=g) * 0.5).to(torch.bfloat16)
+        call.num_heads = heads
+    good = call.to("cpu")
+    bad = inputs.MlaCall(**{k: getattr(call, k) for k in call.__dataclass_fields__})
+    bad.rows = call.rows.clone()
+    bad.rows[1] = call.num_rows                      # one past the last row
+    from decoder_attention_gb300 import step
+    st = step.MlaDecodeStep(bad.to(cuda))
+    st.run()
+    torch.cuda.synchronize()
+    with pytest.raises(_abi.DecAttnError) as ei:
+        _abi.check_device_error()
+    assert ei.value.code == _abi.DA_ERR_DEVICE_INDEX
+    out = st.out.cpu()
+    assert torch.count_nonzero(out[1]) == 0
+    for s in (0, 2, 3, 4):
+        _close(out[s:s + 1], OM.run_mla_call(_sub_call(good, s))["out"])
+    _abi.check_device_error()                         # the word was cleared
