@@ -150,3 +150,38 @@ def test_qwen3_shape_sampled(cuda):
     np.testing.assert_allclose(vc.double().cpu().numpy()[r_i, :, p_i], vc64[r_i, :, p_i], rtol=2.0 ** -7, atol=4e-3)
     y_ref = P.o_project(q_rot.double().cpu().numpy()[idx], wo.double().cpu().numpy())
     np.testing.assert_allclose(y.double().cpu().numpy()[idx], y_ref, rtol=2.0 ** -7, atol=4e-3)
+
+
+def test_fused_qkv_invalid_token(cuda):
+    """A token whose position is past the cache: the device error word says so and no cache slot is written for
+    it; its q_rot and every other token's outputs are still correct."""
+    from decoder_attention_gb300 import _abi
+    hidden, hq, hkv, R, M, n = 256, 4, 2, 3, 200, 150
+    x, w, b, qn, kn, rows, pos, kc, vc = _setup(n, hidden, hq, hkv, R, M, seed=11)
+    bad_pos = pos.clone()
+    bad_pos[37] = M                                   # one past the last slot
+    cos, sin = _rope_tables(pos.numpy(), 128, 1e6)    # the rotation itself is the valid position's
+    layer = A.Layer(head_dim=128, num_attention_heads=hq, num_key_value_heads=hkv, rotary_dim=128,
+                    q_norm_w=qn.double().numpy(), k_norm_w=kn.double().numpy())
+    kc64, vc64 = kc.double().numpy().copy(), vc.double().numpy().copy()
+    q_ref = P.project_and_update(layer, x.double().numpy(), w.double().numpy(), rows.numpy(), pos.numpy(), cos, sin,
+                                 kc64, vc64, b.double().numpy())
+    L, keep = _layer(hq, hkv, qn, kn, cuda)
+    kcd, vcd = kc.to(cuda), vc.to(cuda)
+    q_rot = torch.empty((n, hq, 128), dtype=torch.bfloat16, device=cuda)
+    _abi.qkv_project_update(L, x.to(cuda), w.to(cuda), b.to(cuda).float(), n, hidden, rows.to(cuda),
+                            bad_pos.to(cuda), torch.from_numpy(cos).float().to(cuda),
+                            torch.from_numpy(sin).float().to(cuda), q_rot, kcd, vcd, R, M)
+    torch.cuda.synchronize()
+    with pytest.raises(_abi.DecAttnError) as ei:
+        _abi.check_device_error()
+    assert ei.value.code == _abi.DA_ERR_DEVICE_INDEX
+    np.testing.assert_allclose(q_rot.double().cpu().numpy(), q_ref, rtol=2.0 ** -7, atol=2e-3)
+    ok = np.arange(n) != 37
+    r_i, p_i = rows.numpy().astype(np.int64)[ok], pos.numpy().astype(np.int64)[ok]
+    kg, vg = kcd.cpu(), vcd.cpu()
+    np.testing.assert_allclose(kg.double().numpy()[r_i, :, p_i], kc64[r_i, :, p_i], rtol=2.0 ** -7, atol=2e-3)
+    np.testing.assert_allclose(vg.double().numpy()[r_i, :, p_i], vc64[r_i, :, p_i], rtol=2.0 ** -7, atol=2e-3)
+    r37, p37 = int(rows[37]), int(pos[37])           # the slot the token would have had is untouched
+    assert torch.equal(kg[r37, :, p37], kc[r37, :, p37]) and torch.equal(vg[r37, :, p37], vc[r37, :, p37])
+    _abi.check_device_error()
