@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <cstdlib>
 #include <type_traits>
 
 #include "common.cuh"
@@ -527,6 +528,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }  // namespace mlap
 
 int mla_pair_chunk(int n_seqs, int max_keys) {
+  const char* env = std::getenv("DA_MLA_CHUNK");   // tuning override (multiple of 256)
+  if (env && std::atoi(env) >= mlap::PT && std::atoi(env) % mlap::PT == 0) return std::atoi(env);
   int chunk = mlap::PT;
   // grow the chunk (fewer partials) while the grid keeps >= 4 waves of the 76 CTA pairs a 152-SM part holds
   while (chunk < 16384 && static_cast<long long>(n_seqs) * ((max_keys + 2 * chunk - 1) / (2 * chunk)) >= 4LL * 76)
