@@ -9,6 +9,8 @@
 #include <algorithm>
 #include <cmath>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "kvmap.cuh"
@@ -284,6 +286,11 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
   }
 }
 
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // Bulk-copy form (SHFL layouts with cos/sin rows a multiple of 16 bytes). A block walks tokens blockIdx.x,
 // blockIdx.x + gridDim.x, ... through KB_STAGES shared-memory stages. Per token one thread copies the
 // token's q, k and v rows and its cos/sin rows into a stage with cp.async.bulk (so the loads in flight do not
@@ -372,87 +379,181 @@ __global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpda
   }
 
   // -------------------------------------------------------------------- normalise and rotate (warps 0-7)
-  const int sub = lane % TPV, slot = lane / TPV, e0 = sub * VEC;
-  const int hc = half / VEC;
-  const bool lower = sub < hc, upper = sub >= hc && sub < 2 * hc;
-  const int psub = lower ? sub + hc : (upper ? sub - hc : sub);
-  const int src_lane = slot * TPV + psub;
-  const int ci = (lower ? sub : sub - hc) * VEC;   // this piece's pairs (lower or upper half)
   const bool norm = a.q_norm_w != nullptr;
-  float wq[VEC], wk[VEC];
-  if (norm) {
+  if constexpr (std::is_same_v<T, __nv_bfloat16> && D == 128) {
+    // Two heads per warp, 16 lanes per head. A lane holds both members of its four rotary pairs, elements
+    // [4 sub, +4) and [half + 4 sub, +4), or, past the rotated features, eight that pass through (two runs of
+    // four at 2 half + 8 (sub - half / 4)); so the rotation needs no exchange between lanes, and the math runs
+    // on packed fp32 pairs. Pass-through lanes rotate by cos 1, sin 0.
+    const int sub = lane & 15, slot = lane >> 4, hp = half / 4;   // hp: lanes that hold rotary pairs
+    const bool pairs = sub < hp;
+    const int off0 = pairs ? 4 * sub : 2 * half + 8 * (sub - hp), off1 = pairs ? half + 4 * sub : off0 + 4;
+    uint64_t wq2[4], wk2[4];   // norm weights of this lane's elements, packed in pairs
 #pragma unroll
-    for (int j = 0; j < VEC; j += 4) {
-      const float4 q4 = *reinterpret_cast<const float4*>(a.q_norm_w + e0 + j);
-      const float4 k4 = *reinterpret_cast<const float4*>(a.k_norm_w + e0 + j);
-      wq[j] = q4.x; wq[j + 1] = q4.y; wq[j + 2] = q4.z; wq[j + 3] = q4.w;
-      wk[j] = k4.x; wk[j + 1] = k4.y; wk[j + 2] = k4.z; wk[j + 3] = k4.w;
+    for (int i = 0; i < 4; ++i) {
+      const int e = (i < 2 ? off0 : off1) + 2 * (i & 1);
+      wq2[i] = norm ? f2_pack(a.q_norm_w[e], a.q_norm_w[e + 1]) : f2_pack(1.f, 1.f);
+      wk2[i] = norm ? f2_pack(a.k_norm_w[e], a.k_norm_w[e + 1]) : f2_pack(1.f, 1.f);
     }
-  }
-  const int steps = (heads + HPW - 1) / HPW;
-  for (int kk = 0; kk < n_mine; ++kk) {
-    const int t = blockIdx.x + kk * gridDim.x;
-    const int s = kk % KB_STAGES;
-    uint8_t* st = kb_smem + s * L.bytes;
-    int row = 0, pos = 0;
-    if (warp == 0 && lane == 0) {
-      row = a.rows[t];
-      pos = a.positions[t];
-    }
-    if (!__all_sync(0xffffffffu, mbar_wait(full(s), (kk / KB_STAGES) & 1, a.err))) break;
-    if (warp == 0 && lane == 0) {
-      // the token's cache slot, for the copy thread (published by this thread's arrival on done[s]); written
-      // only now: the stage's full barrier is armed after the copy thread has read the previous token's slot
-      const long long slot = kv_slot(kv_layout(a), row, pos);
-      if (slot < 0) set_error(a.err, kErrIndex);
-      *reinterpret_cast<long long*>(st + L.hdr) = slot;
-    }
-    float c[VEC], sv[VEC];
-    if (lower || upper) {
-#pragma unroll
-      for (int j = 0; j < VEC; j += 4) {
-        const float4 c4 = *reinterpret_cast<const float4*>(st + L.cos + (ci + j) * 4);
-        const float4 s4 = *reinterpret_cast<const float4*>(st + L.sin + (ci + j) * 4);
-        c[j] = c4.x; c[j + 1] = c4.y; c[j + 2] = c4.z; c[j + 3] = c4.w;
-        sv[j] = s4.x; sv[j + 1] = s4.y; sv[j + 2] = s4.z; sv[j + 3] = s4.w;
+    const int steps = (heads + 1) / 2;
+    for (int kk = 0; kk < n_mine; ++kk) {
+      const int t = blockIdx.x + kk * gridDim.x;
+      const int s = kk % KB_STAGES;
+      uint8_t* st = kb_smem + s * L.bytes;
+      int row = 0, pos = 0;
+      if (warp == 0 && lane == 0) {
+        row = a.rows[t];
+        pos = a.positions[t];
       }
-    }
-    for (int step = warp; step < steps; step += 8) {
-      const int hh = step * HPW + slot;
-      const bool live = hh < heads;
-      const bool is_q = hh < a.hq;
-      T* vec = reinterpret_cast<T*>(st + (is_q ? hh * D * es : L.k + (hh - a.hq) * D * es)) + e0;
-      float x[VEC];
-      if (live) V::load(vec, x);
-      else {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) x[j] = 0.f;
+      if (!__all_sync(0xffffffffu, mbar_wait(full(s), (kk / KB_STAGES) & 1, a.err))) break;
+      if (warp == 0 && lane == 0) {
+        // the token's cache slot, for the copy thread (published by this thread's arrival on done[s]); written
+        // only now: the stage's full barrier is armed after the copy thread has read the previous token's slot
+        const long long slot_ = kv_slot(kv_layout(a), row, pos);
+        if (slot_ < 0) set_error(a.err, kErrIndex);
+        *reinterpret_cast<long long*>(st + L.hdr) = slot_;
       }
-      if (norm) {
-        float ss = 0.f;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) ss = fmaf(x[j], x[j], ss);
-#pragma unroll
-        for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
-        const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * (is_q ? wq[j] : wk[j]);
-      }
-      float px[VEC], y[VEC];
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) px[j] = __shfl_sync(0xffffffffu, x[j], src_lane);
-      if (lower || upper) {
-        const float sgn = lower ? -1.f : 1.f;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) y[j] = fmaf(sgn * px[j], sv[j], x[j] * c[j]);
+      uint64_t c2[2], s2[2];   // cos / sin of this lane's pairs 4 sub .. 4 sub + 3
+      if (pairs) {
+        const float4 c4 = *reinterpret_cast<const float4*>(st + L.cos + 4 * sub * 4);
+        const float4 s4 = *reinterpret_cast<const float4*>(st + L.sin + 4 * sub * 4);
+        c2[0] = f2_pack(c4.x, c4.y); c2[1] = f2_pack(c4.z, c4.w);
+        s2[0] = f2_pack(-s4.x, -s4.y); s2[1] = f2_pack(-s4.z, -s4.w);   // negated: y_lo = x_lo c - x_hi s
       } else {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) y[j] = x[j];
+        c2[0] = c2[1] = f2_pack(1.f, 1.f);
+        s2[0] = s2[1] = f2_pack(0.f, 0.f);
       }
-      if (live) V::store(vec, y);
+      for (int step = warp; step < steps; step += 8) {
+        const int hh = step * 2 + slot;
+        const bool live = hh < heads;
+        const bool is_q = hh < a.hq;
+        uint8_t* vec = st + (is_q ? hh * D * 2 : L.k + (hh - a.hq) * D * 2);
+        uint2 lo = make_uint2(0u, 0u), hi = make_uint2(0u, 0u);
+        if (live) {
+          lo = *reinterpret_cast<const uint2*>(vec + off0 * 2);
+          hi = *reinterpret_cast<const uint2*>(vec + off1 * 2);
+        }
+        // bf16 -> fp32 pairs: a bf16 is the high half of its fp32
+        uint64_t x2[4] = {f2_pack(__uint_as_float(lo.x << 16), __uint_as_float(lo.x & 0xffff0000u)),
+                          f2_pack(__uint_as_float(lo.y << 16), __uint_as_float(lo.y & 0xffff0000u)),
+                          f2_pack(__uint_as_float(hi.x << 16), __uint_as_float(hi.x & 0xffff0000u)),
+                          f2_pack(__uint_as_float(hi.y << 16), __uint_as_float(hi.y & 0xffff0000u))};
+        if (norm) {
+          uint64_t q2 = f2_mul(x2[0], x2[0]);
+#pragma unroll
+          for (int i = 1; i < 4; ++i) q2 = f2_fma(x2[i], x2[i], q2);
+          float q0, q1;
+          f2_unpack(q2, q0, q1);
+          float ss = q0 + q1;
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
+          const uint64_t rs2 = f2_pack(rs, rs);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x2[i] = f2_mul(f2_mul(x2[i], rs2), is_q ? wq2[i] : wk2[i]);
+        }
+        // y_lo = x_lo c - x_hi s, y_hi = x_hi c + x_lo s
+        uint64_t y2[4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          y2[i] = f2_fma(x2[2 + i], s2[i], f2_mul(x2[i], c2[i]));
+          y2[2 + i] = f2_fma(x2[i], f2_mul(s2[i], f2_pack(-1.f, -1.f)), f2_mul(x2[2 + i], c2[i]));
+        }
+        if (live) {
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) f2_unpack(y2[i], f[2 * i], f[2 * i + 1]);
+          *reinterpret_cast<uint2*>(vec + off0 * 2) = make_uint2(bf16x2_bits(f[0], f[1]), bf16x2_bits(f[2], f[3]));
+          *reinterpret_cast<uint2*>(vec + off1 * 2) = make_uint2(bf16x2_bits(f[4], f[5]), bf16x2_bits(f[6], f[7]));
+        }
+      }
+      fence_proxy_async_smem();   // the rotated vectors (generic proxy) -> visible to the bulk stores
+      mbar_arrive(done(s));
     }
-    fence_proxy_async_smem();   // the rotated vectors (generic proxy) -> visible to the bulk stores
-    mbar_arrive(done(s));
+    return;
+  } else {
+    const int sub = lane % TPV, slot = lane / TPV, e0 = sub * VEC;
+    const int hc = half / VEC;
+    const bool lower = sub < hc, upper = sub >= hc && sub < 2 * hc;
+    const int psub = lower ? sub + hc : (upper ? sub - hc : sub);
+    const int src_lane = slot * TPV + psub;
+    const int ci = (lower ? sub : sub - hc) * VEC;   // this piece's pairs (lower or upper half)
+    const bool norm = a.q_norm_w != nullptr;
+    float wq[VEC], wk[VEC];
+    if (norm) {
+  #pragma unroll
+      for (int j = 0; j < VEC; j += 4) {
+        const float4 q4 = *reinterpret_cast<const float4*>(a.q_norm_w + e0 + j);
+        const float4 k4 = *reinterpret_cast<const float4*>(a.k_norm_w + e0 + j);
+        wq[j] = q4.x; wq[j + 1] = q4.y; wq[j + 2] = q4.z; wq[j + 3] = q4.w;
+        wk[j] = k4.x; wk[j + 1] = k4.y; wk[j + 2] = k4.z; wk[j + 3] = k4.w;
+      }
+    }
+    const int steps = (heads + HPW - 1) / HPW;
+    for (int kk = 0; kk < n_mine; ++kk) {
+      const int t = blockIdx.x + kk * gridDim.x;
+      const int s = kk % KB_STAGES;
+      uint8_t* st = kb_smem + s * L.bytes;
+      int row = 0, pos = 0;
+      if (warp == 0 && lane == 0) {
+        row = a.rows[t];
+        pos = a.positions[t];
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(full(s), (kk / KB_STAGES) & 1, a.err))) break;
+      if (warp == 0 && lane == 0) {
+        // the token's cache slot, for the copy thread (published by this thread's arrival on done[s]); written
+        // only now: the stage's full barrier is armed after the copy thread has read the previous token's slot
+        const long long slot = kv_slot(kv_layout(a), row, pos);
+        if (slot < 0) set_error(a.err, kErrIndex);
+        *reinterpret_cast<long long*>(st + L.hdr) = slot;
+      }
+      float c[VEC], sv[VEC];
+      if (lower || upper) {
+  #pragma unroll
+        for (int j = 0; j < VEC; j += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(st + L.cos + (ci + j) * 4);
+          const float4 s4 = *reinterpret_cast<const float4*>(st + L.sin + (ci + j) * 4);
+          c[j] = c4.x; c[j + 1] = c4.y; c[j + 2] = c4.z; c[j + 3] = c4.w;
+          sv[j] = s4.x; sv[j + 1] = s4.y; sv[j + 2] = s4.z; sv[j + 3] = s4.w;
+        }
+      }
+      for (int step = warp; step < steps; step += 8) {
+        const int hh = step * HPW + slot;
+        const bool live = hh < heads;
+        const bool is_q = hh < a.hq;
+        T* vec = reinterpret_cast<T*>(st + (is_q ? hh * D * es : L.k + (hh - a.hq) * D * es)) + e0;
+        float x[VEC];
+        if (live) V::load(vec, x);
+        else {
+  #pragma unroll
+          for (int j = 0; j < VEC; ++j) x[j] = 0.f;
+        }
+        if (norm) {
+          float ss = 0.f;
+  #pragma unroll
+          for (int j = 0; j < VEC; ++j) ss = fmaf(x[j], x[j], ss);
+  #pragma unroll
+          for (int off = TPV / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, TPV);
+          const float rs = rsqrtf(ss * (1.0f / D) + a.eps);
+  #pragma unroll
+          for (int j = 0; j < VEC; ++j) x[j] = x[j] * rs * (is_q ? wq[j] : wk[j]);
+        }
+        float px[VEC], y[VEC];
+  #pragma unroll
+        for (int j = 0; j < VEC; ++j) px[j] = __shfl_sync(0xffffffffu, x[j], src_lane);
+        if (lower || upper) {
+          const float sgn = lower ? -1.f : 1.f;
+  #pragma unroll
+          for (int j = 0; j < VEC; ++j) y[j] = fmaf(sgn * px[j], sv[j], x[j] * c[j]);
+        } else {
+  #pragma unroll
+          for (int j = 0; j < VEC; ++j) y[j] = x[j];
+        }
+        if (live) V::store(vec, y);
+      }
+      fence_proxy_async_smem();   // the rotated vectors (generic proxy) -> visible to the bulk stores
+      mbar_arrive(done(s));
+    }
   }
 }
 
