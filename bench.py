@@ -308,8 +308,7 @@ def main_native(args):
         e = ev[i]
         e[0].record(stream)
         for li, st in enumerate(steps):
-            st.rope()
-            st.cache_update()
+            st.update()
             e[1 + 3 * li].record(stream)
             st.prefill()
             e[2 + 3 * li].record(stream)
@@ -533,8 +532,7 @@ def main_native_mla(args):
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
-        st.rope()
-        st.cache_update()
+        st.update()
         ev[i][1].record(stream)
         st.decode()
         ev[i][2].record(stream)

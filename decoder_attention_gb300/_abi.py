@@ -73,6 +73,10 @@ def _load():
     sig = {
         "da_rope_tables_build": (I, [ctypes.POINTER(DaRopeScaling), P, P, I, P, P, P]),
         "da_kv_cache_update": (I, [ctypes.POINTER(DaLayer), P, P, P, I, P, P, P, P, P, P, P, I, I, P]),
+        "da_kv_cache_update_rope": (I, [ctypes.POINTER(DaLayer), ctypes.POINTER(DaRopeScaling), P, P, P, I, P, P, P, P,
+                                        P, P, I, I, P]),
+        "da_kv_cache_update_rope_paged": (I, [ctypes.POINTER(DaLayer), ctypes.POINTER(DaRopeScaling), P, P, P, I, P, P,
+                                              P, P, ctypes.c_void_p, P]),
         "da_attn_prefill": (I, [ctypes.POINTER(DaLayer), P, I, P, P, I, I, I, P, P, P, I, P, P, P, Z, P]),
         "da_attn_decode": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, I, P, P, P, P, P, Z, P]),
         "da_decode_workspace_bytes": (Z, [ctypes.POINTER(DaLayer), I, I]),
@@ -230,6 +234,24 @@ def kv_cache_update(L, q, k, v, n, rows, positions, cos, sin, q_rot, k_cache, v_
     _check(LIB.da_kv_cache_update(ctypes.byref(L), _ptr(q), _ptr(k), _ptr(v), int(n), _ptr(rows), _ptr(positions),
                                   _ptr(cos), _ptr(sin), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), int(num_rows),
                                   int(max_len), _stream(stream)))
+
+
+def kv_cache_update_rope(L, rs, q, k, v, n, rows, positions, seq_len, q_rot, k_cache, v_cache, num_rows, max_len,
+                         stream=None):
+    _check(LIB.da_kv_cache_update_rope(ctypes.byref(L), ctypes.byref(rs), _ptr(q), _ptr(k), _ptr(v), int(n), _ptr(rows),
+                                       _ptr(positions), _ptr(seq_len), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache),
+                                       int(num_rows), int(max_len), _stream(stream)))
+
+
+def kv_cache_update_rope_paged(L, rs, q, k, v, n, rows, positions, seq_len, q_rot, kv, stream=None):
+    _check(LIB.da_kv_cache_update_rope_paged(ctypes.byref(L), ctypes.byref(rs), _ptr(q), _ptr(k), _ptr(v), int(n),
+                                             _ptr(rows), _ptr(positions), _ptr(seq_len), _ptr(q_rot),
+                                             ctypes.cast(ctypes.pointer(kv), ctypes.c_void_p), _stream(stream)))
+
+
+def kv_rope_fused_supported(L):
+    """Whether da_kv_cache_update_rope takes this layer (bf16, head_dim 128, rotary_dim a multiple of 16)."""
+    return L.dtype == DA_BF16 and L.head_dim == 128 and L.rotary_dim % 16 == 0
 
 
 def attn_prefill(L, q_rot, n_tokens, k_cache, v_cache, num_rows, max_len, n_seqs, q_start, rows, first_pos,

@@ -272,18 +272,31 @@ static void set_paged(Args& a, const da_paged_kv* kv) {
 }
 }
 
+// rs != NULL: cos/sin are formed in the kernel from rs, positions and seq_len (cos/sin unused).
 static int kv_update_impl(const da_layer* L, const void* q, const void* k, const void* v, int n, const int32_t* rows,
                           const int32_t* positions, const float* cos, const float* sin, void* q_rot, void* k_cache,
-                          void* v_cache, int num_rows, int max_len, const da_paged_kv* kv, cudaStream_t stream) {
+                          void* v_cache, int num_rows, int max_len, const da_paged_kv* kv, cudaStream_t stream,
+                          const da_rope_scaling* rs = nullptr, const int32_t* seq_len = nullptr) {
   int rc = check_layer(L);
   if (rc) return rc;
+  da::RopeFreqs f;
+  if (rs) {
+    rc = compute_freqs(rs, &f);
+    if (rc) return rc;
+    if (rs->rotary_dim != L->rotary_dim)
+      return fail(DA_ERR_INVALID_ARG, "the scaling's rotary_dim %d differs from the layer's %d", rs->rotary_dim,
+                  L->rotary_dim);
+    if (!da::kv_update_rope_supported(L->dtype == DA_BF16, L->head_dim, L->rotary_dim))
+      return fail(DA_ERR_UNSUPPORTED, "the fused rope form needs bf16, head_dim 128 and rotary_dim a multiple of 16");
+  }
   if (n < 0) return fail(DA_ERR_INVALID_ARG, "n = %d < 0", n);
   if (n == 0) return ok();
-  if (!q || !k || !v || !rows || !positions || !cos || !sin || !q_rot || !k_cache || !v_cache)
+  if (!q || !k || !v || !rows || !positions || (!rs && (!cos || !sin)) || !q_rot || !k_cache || !v_cache)
     return fail(DA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (rs && f.use_seq_len && !seq_len) return fail(DA_ERR_INVALID_ARG, "longrope needs seq_len per token");
   if (num_rows < 1 || max_len < 1) return fail(DA_ERR_INVALID_ARG, "num_rows and max_len must be >= 1");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      !aligned16(cos) || !aligned16(sin) || !aligned16(L->q_norm_w) || !aligned16(L->k_norm_w))
+      (!rs && (!aligned16(cos) || !aligned16(sin))) || !aligned16(L->q_norm_w) || !aligned16(L->k_norm_w))
     return fail(DA_ERR_INVALID_ARG, "q, k, v, q_rot, the caches, cos/sin and the norm weights must be 16-byte aligned");
   int* err = da::error_word_ptr();
   if (!err) return fail(DA_ERR_CUDA, "cannot locate the device error word (no CUDA device?)");
@@ -310,7 +323,8 @@ static int kv_update_impl(const da_layer* L, const void* q, const void* k, const
   a.max_len = max_len;
   set_paged(a, kv);
   a.err = err;
-  cudaError_t e = da::launch_kv_update(a, L->dtype == DA_BF16, stream);
+  a.seq_len = seq_len;
+  cudaError_t e = rs ? da::launch_kv_update_rope(a, f, stream) : da::launch_kv_update(a, L->dtype == DA_BF16, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kv_cache_update launch");
   return ok();
 }
@@ -332,6 +346,27 @@ int da_kv_cache_update_paged(const da_layer* L, const void* q, const void* k, co
   if (rc) return rc;
   return kv_update_impl(L, q, k, v, n, rows, positions, cos, sin, q_rot, kv->k_pool, kv->v_pool, kv->num_rows,
                         kv->max_blocks * kv->block_size, kv, stream);
+}
+
+int da_kv_cache_update_rope(const da_layer* L, const da_rope_scaling* rs, const void* q, const void* k, const void* v,
+                            int n, const int32_t* rows, const int32_t* positions, const int32_t* seq_len, void* q_rot,
+                            void* k_cache, void* v_cache, int num_rows, int max_len, cudaStream_t stream) {
+  if (!rs) return fail(DA_ERR_INVALID_ARG, "the rope scaling is NULL");
+  return kv_update_impl(L, q, k, v, n, rows, positions, nullptr, nullptr, q_rot, k_cache, v_cache, num_rows, max_len,
+                        nullptr, stream, rs, seq_len);
+}
+
+int da_kv_cache_update_rope_paged(const da_layer* L, const da_rope_scaling* rs, const void* q, const void* k,
+                                  const void* v, int n, const int32_t* rows, const int32_t* positions,
+                                  const int32_t* seq_len, void* q_rot, const da_paged_kv* kv, cudaStream_t stream) {
+  if (!rs) return fail(DA_ERR_INVALID_ARG, "the rope scaling is NULL");
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n == 0) return ok();
+  rc = check_paged(L, kv);
+  if (rc) return rc;
+  return kv_update_impl(L, q, k, v, n, rows, positions, nullptr, nullptr, q_rot, kv->k_pool, kv->v_pool, kv->num_rows,
+                        kv->max_blocks * kv->block_size, kv, stream, rs, seq_len);
 }
 
 static int attn_common_checks(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache,

@@ -73,8 +73,13 @@ struct KvUpdateArgs {
   int block_size, max_blocks, n_blocks;
   int* err;
   int wpt;                        // warps per token (set by the launcher)
+  const int32_t* seq_len;         // per token, for LongRoPE's table switch (fused form only)
 };
 cudaError_t launch_kv_update(const KvUpdateArgs& a, bool bf16, cudaStream_t stream);
+// The same update with each token's cos/sin formed in the kernel from its position (no tables); bf16, d 128,
+// r/2 a multiple of 8. cos/sin in a are unused.
+bool kv_update_rope_supported(bool bf16, int d, int rot);
+cudaError_t launch_kv_update_rope(const KvUpdateArgs& a, const RopeFreqs& freqs, cudaStream_t stream);
 
 // Query set of an attention call: prefill chunks (q_start/first_pos) or decode tokens (positions).
 struct AttnArgs {

@@ -313,8 +313,11 @@ static KbLayout kb_layout(int hq, int hkv, int d, int half, int es) {
   return L;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpdateArgs a, const KbLayout L) {
+// FUSED: no cos/sin tables; per token the computing threads form its cos/sin (one rotary pair each) in the
+// stage with the arithmetic of rope_tables_kernel, so the results are the same bits; bf16 with d = 128 only.
+template <typename T, int D, bool FUSED>
+__global__ void __launch_bounds__(KB_THREADS, 3) kv_update_bulk_kernel(const KvUpdateArgs a, const KbLayout L,
+                                                                   const __grid_constant__ RopeTurns f) {
   using V = Vec16<T>;
   constexpr int VEC = V::N;
   constexpr int TPV = D / VEC;
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpda
   }
   __syncthreads();
   const int es = static_cast<int>(sizeof(T));
-  const uint32_t in_bytes = static_cast<uint32_t>(L.hdr);   // q, k, v, cos, sin
+  const uint32_t in_bytes = static_cast<uint32_t>(FUSED ? L.cos : L.hdr);   // q, k, v (, cos, sin)
 
   if (warp == 8) {
     if (lane != 0) return;
@@ -350,8 +353,10 @@ __global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpda
       bulk_load(st, static_cast<const T*>(a.q) + static_cast<long long>(t) * a.hq * D, a.hq * D * es, full(s));
       bulk_load(st + L.k, static_cast<const T*>(a.k) + static_cast<long long>(t) * a.hkv * D, a.hkv * D * es, full(s));
       bulk_load(st + L.v, static_cast<const T*>(a.v) + static_cast<long long>(t) * a.hkv * D, a.hkv * D * es, full(s));
-      bulk_load(st + L.cos, a.cos + static_cast<long long>(t) * half, half * 4, full(s));
-      bulk_load(st + L.sin, a.sin + static_cast<long long>(t) * half, half * 4, full(s));
+      if (!FUSED) {
+        bulk_load(st + L.cos, a.cos + static_cast<long long>(t) * half, half * 4, full(s));
+        bulk_load(st + L.sin, a.sin + static_cast<long long>(t) * half, half * 4, full(s));
+      }
     };
     for (int kk = 0; kk < n_mine && kk < KB_STAGES; ++kk) issue(kk);
     for (int kk = 0; kk < n_mine; ++kk) {
@@ -400,12 +405,42 @@ __global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpda
       const int t = blockIdx.x + kk * gridDim.x;
       const int s = kk % KB_STAGES;
       uint8_t* st = kb_smem + s * L.bytes;
-      int row = 0, pos = 0;
-      if (warp == 0 && lane == 0) {
-        row = a.rows[t];
-        pos = a.positions[t];
+      int row = 0, pos = 0, len = 0;
+      if (warp == 0 && lane == 0) row = a.rows[t];
+      const bool tabler = FUSED && warp * 32 + lane < half;   // forms one of this token's cos/sin pairs
+      if (tabler || (warp == 0 && lane == 0)) pos = a.positions[t];
+      if (tabler && f.use_seq_len) len = a.seq_len[t];
+      if (FUSED) {
+        // this token's cos/sin into the stage, one rotary pair per computing thread (the tables' arithmetic);
+        // that part of the stage is not copied in, and the barrier below keeps the warps within one token, so
+        // the previous use of this stage has been read
+        const int i = warp * 32 + lane;
+        if (i < half) {
+          const bool use_long = f.use_seq_len && len > f.switch_len;
+          const unsigned long long turn = use_long ? f.turn_long[i] : f.turn_short[i];
+          const unsigned long long frac = static_cast<unsigned long long>(pos) * turn;   // mod 2^64
+          const int top = static_cast<int>(static_cast<unsigned int>(frac >> 32));
+          float cv, sv;
+          sincospif(static_cast<float>(top) * 4.656612873077393e-10f, &sv, &cv);
+          reinterpret_cast<float*>(st + L.cos)[i] = pos < 0 ? 0.f : cv * f.af;
+          reinterpret_cast<float*>(st + L.sin)[i] = pos < 0 ? 0.f : sv * f.af;
+          if (pos < 0 && i == 0) set_error(a.err, kErrIndex);
+        }
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(full(s), (kk / KB_STAGES) & 1, a.err))) break;
+      if (FUSED) {
+        // every computing warp goes on, or all leave together (a warp alone at the barrier would wait forever);
+        // the barrier also orders the cos/sin above before their reads
+        uint32_t all_ok;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(all_ok)
+            : "r"(mbar_wait(full(s), (kk / KB_STAGES) & 1, a.err) ? 1u : 0u)
+            : "memory");
+        if (!all_ok) break;
+      } else if (!__all_sync(0xffffffffu, mbar_wait(full(s), (kk / KB_STAGES) & 1, a.err))) {
+        break;
+      }
       if (warp == 0 && lane == 0) {
         // the token's cache slot, for the copy thread (published by this thread's arrival on done[s]); written
         // only now: the stage's full barrier is armed after the copy thread has read the previous token's slot
@@ -557,6 +592,20 @@ __global__ void __launch_bounds__(KB_THREADS) kv_update_bulk_kernel(const KvUpda
   }
 }
 
+template <typename T, int D, bool FUSED>
+static cudaError_t launch_bulk(const KvUpdateArgs& a, const KbLayout& L, const RopeTurns& f, int smem,
+                               cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kv_update_bulk_kernel<T, D, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int per_sm = 0, dev = 0, n_sm = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_update_bulk_kernel<T, D, FUSED>, KB_THREADS, smem);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(a.n, n_sm * std::max(per_sm, 1)));
+  kv_update_bulk_kernel<T, D, FUSED><<<grid, KB_THREADS, smem, stream>>>(a, L, f);
+  return cudaGetLastError();
+}
+
 template <typename T, int D>
 static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
   if (a.n == 0) return cudaSuccess;
@@ -571,15 +620,7 @@ static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
     const KbLayout L = kb_layout(a.hq, a.hkv, D, half, static_cast<int>(sizeof(T)));
     const int smem = KB_STAGES * L.bytes;
     if (smem <= 200 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(kv_update_bulk_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      int per_sm = 0, dev = 0, n_sm = 0;
-      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_update_bulk_kernel<T, D>, KB_THREADS, smem);
-      if (e == cudaSuccess) e = cudaGetDevice(&dev);
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return e;
-      const int grid = std::max(1, std::min(a.n, n_sm * std::max(per_sm, 1)));
-      kv_update_bulk_kernel<T, D><<<grid, KB_THREADS, smem, stream>>>(a, L);
-      return cudaGetLastError();
+      return launch_bulk<T, D, false>(a, L, RopeTurns{}, smem, stream);
     }
   }
   const long long warps = static_cast<long long>(a.n) * b.wpt;
@@ -594,6 +635,19 @@ static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
 cudaError_t launch_kv_update(const KvUpdateArgs& a, bool bf16, cudaStream_t stream) {
   if (bf16) return a.d == 64 ? launch_kv_t<__nv_bfloat16, 64>(a, stream) : launch_kv_t<__nv_bfloat16, 128>(a, stream);
   return a.d == 64 ? launch_kv_t<float, 64>(a, stream) : launch_kv_t<float, 128>(a, stream);
+}
+
+bool kv_update_rope_supported(bool bf16, int d, int rot) {
+  return bf16 && d == 128 && (rot / 2) % 8 == 0;
+}
+
+cudaError_t launch_kv_update_rope(const KvUpdateArgs& a, const RopeFreqs& freqs, cudaStream_t stream) {
+  if (a.n == 0) return cudaSuccess;
+  const int half = a.rot / 2;
+  const KbLayout L = kb_layout(a.hq, a.hkv, 128, half, 2);
+  const int smem = KB_STAGES * L.bytes;
+  if (!kv_update_rope_supported(true, a.d, a.rot) || smem > 200 * 1024) return cudaErrorNotSupported;
+  return launch_bulk<__nv_bfloat16, 128, true>(a, L, rope_turns(freqs), smem, stream);
 }
 
 }  // namespace da

@@ -1,9 +1,10 @@
-"""One layer's attention step through the C ABI: rope tables -> norm/rope/cache write -> attention.
+"""One layer's attention step through the C ABI: norm/rope/cache write -> attention.
 
 ``AttentionStep`` owns the per-call buffers (cos/sin tables, q_rot, out, decode workspace) that the caller
 must provide to the library, allocated once with torch; ``run()`` only enqueues the library's kernels.
 Prefill chunks and decode tokens of one batch go to da_attn_prefill and da_attn_decode respectively,
-after one da_kv_cache_update for all tokens.
+after one cache update for all tokens: da_kv_cache_update_rope (cos/sin formed in the kernel) where the layer
+allows it (bf16, head_dim 128, rotary_dim a multiple of 16), else da_rope_tables_build + da_kv_cache_update.
 """
 from __future__ import annotations
 
@@ -24,7 +25,7 @@ def rotary_dim_of(head_dim, partial_rotary_factor):
 class AttentionStep:
     """Buffers and C structs for one LayerCall (see decoder_attention_gb300.inputs)."""
 
-    def __init__(self, call, device=None):
+    def __init__(self, call, device=None, fused_rope=None):
         dev = torch.device(device) if device is not None else call.q.device
         self.call = c = call
         self.device = dev
@@ -35,6 +36,8 @@ class AttentionStep:
         self.sinks = c.sinks.to(dev, torch.float32).contiguous() if c.sinks is not None else None
         self.L = _abi.layer(c.dtype, c.head_dim, c.num_attention_heads, c.num_key_value_heads, self.rot,
                             self.q_norm_w, self.k_norm_w, c.eps, c.window, c.softcap, 0.0, self.sinks)
+        # fused_rope: None = whenever the layer allows it; False = the tables and the update as two calls
+        self.fused_rope = _abi.kv_rope_fused_supported(self.L) if fused_rope is None else bool(fused_rope)
         n = c.n_tokens
         self.cos = torch.empty((max(n, 1), self.rot // 2), dtype=torch.float32, device=dev)
         self.sin = torch.empty_like(self.cos)
@@ -49,13 +52,24 @@ class AttentionStep:
 
     # -- the three stages, separately callable for timing ------------------------------------------
     def rope(self, stream=None):
+        """cos/sin tables (the two-call form needs them; the fused update forms them itself)."""
         c = self.call
         _abi.rope_tables_build(self.rs, c.tok_pos, c.tok_seq_len, c.n_tokens, self.cos, self.sin, stream)
 
+    def update(self, stream=None):
+        """Norm, RoPE and the cache write for every token: one fused call, or the tables and the update."""
+        if not self.fused_rope:
+            self.rope(stream)
+        self.cache_update(stream)
+
     def cache_update(self, stream=None):
         c = self.call
-        _abi.kv_cache_update(self.L, c.q, c.k, c.v, c.n_tokens, c.tok_rows, c.tok_pos, self.cos, self.sin,
-                             self.q_rot, c.k_cache, c.v_cache, c.num_rows, c.max_len, stream)
+        if self.fused_rope:
+            _abi.kv_cache_update_rope(self.L, self.rs, c.q, c.k, c.v, c.n_tokens, c.tok_rows, c.tok_pos, c.tok_seq_len,
+                                      self.q_rot, c.k_cache, c.v_cache, c.num_rows, c.max_len, stream)
+        else:
+            _abi.kv_cache_update(self.L, c.q, c.k, c.v, c.n_tokens, c.tok_rows, c.tok_pos, self.cos, self.sin,
+                                 self.q_rot, c.k_cache, c.v_cache, c.num_rows, c.max_len, stream)
 
     def prefill(self, stream=None):
         c = self.call
@@ -72,16 +86,15 @@ class AttentionStep:
                              self.ws_bytes, stream)
 
     def run(self, stream=None):
-        self.rope(stream)
-        self.cache_update(stream)
+        self.update(stream)
         self.prefill(stream)
         self.decode(stream)
         return self.out
 
     def kernel_launches(self):
-        """Kernels one run() enqueues (rope tables, cache update, prefill, decode + merge)."""
+        """Kernels one run() enqueues (rope tables unless fused, cache update, prefill, decode + merge)."""
         c = self.call
-        n = (1 if c.n_tokens else 0) * 2
+        n = (1 if c.n_tokens else 0) * (1 if self.fused_rope else 2)
         if c.n_prefill:
             n += 1
         if c.n_decode:
@@ -93,8 +106,8 @@ class PagedAttentionStep(AttentionStep):
     """AttentionStep over a paged KV pool: k_pool/v_pool [n_blocks, Hkv, block_size, d] and an int32 block
     table [num_rows, max_blocks] on the device stand in for the call's contiguous caches."""
 
-    def __init__(self, call, k_pool, v_pool, block_table, block_size, device=None):
-        super().__init__(call, device)
+    def __init__(self, call, k_pool, v_pool, block_table, block_size, device=None, fused_rope=None):
+        super().__init__(call, device, fused_rope)
         self.k_pool, self.v_pool, self.block_table = k_pool, v_pool, block_table
         self.block_size = int(block_size)
         self.kv = _abi.paged_kv(k_pool, v_pool, block_table, block_size)
@@ -109,8 +122,12 @@ class PagedAttentionStep(AttentionStep):
 
     def cache_update(self, stream=None):
         c = self.call
-        _abi.kv_cache_update_paged(self.L, c.q, c.k, c.v, c.n_tokens, c.tok_rows, c.tok_pos, self.cos, self.sin,
-                                   self.q_rot, self.kv, stream)
+        if self.fused_rope:
+            _abi.kv_cache_update_rope_paged(self.L, self.rs, c.q, c.k, c.v, c.n_tokens, c.tok_rows, c.tok_pos,
+                                            c.tok_seq_len, self.q_rot, self.kv, stream)
+        else:
+            _abi.kv_cache_update_paged(self.L, c.q, c.k, c.v, c.n_tokens, c.tok_rows, c.tok_pos, self.cos, self.sin,
+                                       self.q_rot, self.kv, stream)
 
     def prefill(self, stream=None):
         c = self.call

@@ -152,6 +152,23 @@ int da_kv_cache_update(const da_layer* layer, const void* q, const void* k, cons
                        cudaStream_t stream);
 
 /*
+ * da_kv_cache_update_rope -- da_kv_cache_update with the rotation's cos/sin formed inside the kernel from
+ * each token's position (and seq_len, for LongRoPE's table switch) by the same arithmetic as
+ * da_rope_tables_build, so the outputs are the same bits as da_rope_tables_build followed by
+ * da_kv_cache_update, without the tables' round trip through memory or their launch.
+ *
+ *   rs         the layer's rotary scaling; rs->rotary_dim must equal layer->rotary_dim
+ *   seq_len    device int32 [n]; required for DA_ROPE_LONGROPE, ignored (may be NULL) otherwise
+ *   the rest   as for da_kv_cache_update (a position < 0 rotates by zero and sets DA_ERR_DEVICE_INDEX)
+ * Errors: as da_rope_tables_build and da_kv_cache_update; DA_ERR_UNSUPPORTED unless the layer is bf16 with
+ *         head_dim 128 and rotary_dim a multiple of 16 (use the two calls otherwise).
+ */
+int da_kv_cache_update_rope(const da_layer* layer, const da_rope_scaling* rs, const void* q, const void* k,
+                            const void* v, int n, const int32_t* rows, const int32_t* positions,
+                            const int32_t* seq_len, void* q_rot, void* k_cache, void* v_cache, int num_rows,
+                            int max_len, cudaStream_t stream);
+
+/*
  * da_attn_prefill -- causal GQA attention of prefill chunks over their cache rows (page 1,
  * DecoderAttention.forward: window_mask then causal_attention; "Model resolution" for soft-capping).
  *
@@ -261,6 +278,11 @@ typedef struct {
 int da_kv_cache_update_paged(const da_layer* layer, const void* q, const void* k, const void* v, int n,
                              const int32_t* rows, const int32_t* positions, const float* cos, const float* sin,
                              void* q_rot, const da_paged_kv* kv, cudaStream_t stream);
+
+/* da_kv_cache_update_rope_paged -- da_kv_cache_update_rope into a paged pool (as da_kv_cache_update_paged). */
+int da_kv_cache_update_rope_paged(const da_layer* layer, const da_rope_scaling* rs, const void* q, const void* k,
+                                  const void* v, int n, const int32_t* rows, const int32_t* positions,
+                                  const int32_t* seq_len, void* q_rot, const da_paged_kv* kv, cudaStream_t stream);
 
 /*
  * da_attn_prefill_paged -- da_attn_prefill over a paged pool (same arithmetic, sinks included). A chunk reads

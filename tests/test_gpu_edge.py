@@ -328,6 +328,8 @@ def test_yarn_prefill_with_sinks(cuda, window, truncate):
                          rope_scaling=sc, theta=150000.0, max_pos=131072)
     res = ostep.run_layer_call(call)
     st, _ = _run(call, cuda)
+    st.rope()                                   # the tables themselves (the step may fuse them)
+    torch.cuda.synchronize()
     n = call.n_tokens
     np.testing.assert_allclose(st.cos[:n].double().cpu().numpy(), res["cos"], atol=5e-7, rtol=0)
     np.testing.assert_allclose(st.sin[:n].double().cpu().numpy(), res["sin"], atol=5e-7, rtol=0)
@@ -341,5 +343,40 @@ def test_yarn_mscale_ratio_decode(cuda):
     call.rope_scaling, call.rope_theta, call.max_position_embeddings = sc, 150000.0, 131072
     res = ostep.run_layer_call(call)
     st, _ = _run(call, cuda)
+    st.rope()
+    torch.cuda.synchronize()
     np.testing.assert_allclose(st.cos[:2].double().cpu().numpy(), res["cos"], atol=5e-7, rtol=0)
     _close(st.out, res["out"])
+
+
+@pytest.mark.parametrize("number", [2, 3, 4, 5])
+def test_fused_rope_update_matches_two_calls(cuda, number):
+    """da_kv_cache_update_rope (cos/sin formed in the kernel) writes the same bits as da_rope_tables_build
+    followed by da_kv_cache_update: q/k norm, llama3, LongRoPE with its seq_len switch and partial rotary
+    (workload 5), contiguous caches and a paged pool."""
+    from decoder_attention_gb300 import _abi as ab_, inputs, step
+    wl = inputs.make(number, scale="small")
+    for call in wl.layers:
+        if call.dtype != torch.bfloat16:
+            continue
+        a, b = call.to(cuda), call.to(cuda)
+        sa, sb = step.AttentionStep(a, fused_rope=True), step.AttentionStep(b, fused_rope=False)
+        assert ab_.kv_rope_fused_supported(sa.L)
+        sa.update()
+        sb.update()
+        torch.cuda.synchronize()
+        ab_.check_device_error()
+        assert torch.equal(sa.q_rot, sb.q_rot)
+        assert torch.equal(a.k_cache, b.k_cache) and torch.equal(a.v_cache, b.v_cache)
+    call = wl.layers[0]
+    a, b = call.to(cuda), call.to(cuda)
+    kpa, vpa, ta = inputs.paged_from_contiguous(a.k_cache, a.v_cache, 64, seed=5)
+    kpb, vpb, tb = inputs.paged_from_contiguous(b.k_cache, b.v_cache, 64, seed=5)
+    pa = step.PagedAttentionStep(a, kpa, vpa, ta, 64, fused_rope=True)
+    pb = step.PagedAttentionStep(b, kpb, vpb, tb, 64, fused_rope=False)
+    pa.update()
+    pb.update()
+    torch.cuda.synchronize()
+    ab_.check_device_error()
+    bits = lambda t: t.view(torch.int16)                # the pools hold NaN in spare blocks: compare bits
+    assert torch.equal(pa.q_rot, pb.q_rot) and torch.equal(bits(kpa), bits(kpb)) and torch.equal(bits(vpa), bits(vpb))
