@@ -308,21 +308,33 @@ def main_native(args):
         e = ev[i]
         e[0].record(stream)
         for li, st in enumerate(steps):
+            # a stage with no tokens records no event (an empty event interval still costs ~2 us of the step)
             st.update()
             e[1 + 3 * li].record(stream)
-            st.prefill()
-            e[2 + 3 * li].record(stream)
-            st.decode()
-            e[3 + 3 * li].record(stream)
+            if st.call.n_prefill:
+                st.prefill()
+                e[2 + 3 * li].record(stream)
+            if st.call.n_decode:
+                st.decode()
+                e[3 + 3 * li].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
     clocks.mark_end()
     _abi.check_device_error()
-    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
-    pf_ms = [sum(e[1 + 3 * li].elapsed_time(e[2 + 3 * li]) for li in range(n_layers)) for e in ev]
-    dec_ms = [sum(e[2 + 3 * li].elapsed_time(e[3 + 3 * li]) for li in range(n_layers)) for e in ev]
-    pre_ms = [sum((e[0] if li == 0 else e[3 * li]).elapsed_time(e[1 + 3 * li]) for li in range(n_layers)) for e in ev]
+    def marks(e, li):   # (after update, after prefill, after decode) of layer li; an empty stage adds no event
+        a = e[1 + 3 * li]
+        b = e[2 + 3 * li] if steps[li].call.n_prefill else a
+        return a, b, (e[3 + 3 * li] if steps[li].call.n_decode else b)
+
+    def interval(x, y):
+        return 0.0 if x is y else x.elapsed_time(y)
+
+    step_ms = [e[0].elapsed_time(marks(e, n_layers - 1)[2]) for e in ev]
+    pf_ms = [sum(interval(*marks(e, li)[:2]) for li in range(n_layers)) for e in ev]
+    dec_ms = [sum(interval(*marks(e, li)[1:]) for li in range(n_layers)) for e in ev]
+    pre_ms = [sum((e[0] if li == 0 else marks(e, li - 1)[2]).elapsed_time(marks(e, li)[0]) for li in range(n_layers))
+              for e in ev]
     ms = statistics.mean(step_ms)
     ms_all = reduce_max(ms, world)
     clock_info = clocks.stop()

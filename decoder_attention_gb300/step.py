@@ -183,6 +183,11 @@ class MlaDecodeStep:
             _abi.mla_cache_update(self.L, c.latent, c.k_rope, c.n_seqs, c.rows, c.positions, self.cos, self.sin,
                                   self.q_rot, c.cache, c.num_rows, c.max_len, stream)
 
+
+    def update(self, stream=None):
+        """The rotary tables, then the cache rows and the queries' rotated part."""
+        self.rope(stream)
+        self.cache_update(stream)
     def decode(self, stream=None):
         c = self.call
         if self.kv is not None:
