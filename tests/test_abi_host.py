@@ -189,3 +189,29 @@ def test_mla_host_checks_and_scale():
     sc = _abi.mla_softmax_scale(128, 64, {"type": "yarn", "factor": 40, "mscale_all_dim": 1.0})
     assert abs(sc - 192 ** -0.5 * (0.1 * math.log(40) + 1) ** 2) < 1e-15
     assert math.isclose(_abi.mla_softmax_scale(128, 64), 192 ** -0.5, rel_tol=1e-15)
+
+
+def test_fused_rope_update_host_checks():
+    """da_kv_cache_update_rope refuses what it cannot take before anything reaches CUDA: a NULL scaling, a
+    scaling whose rotary_dim differs from the layer's, layers outside bf16 / head_dim 128 / rotary_dim a
+    multiple of 16, and LongRoPE without seq_len; n == 0 enqueues nothing."""
+    d = ctypes.c_void_p(16)
+
+    def rc(L, rs, n=4, seq_len=d):
+        return _abi.LIB.da_kv_cache_update_rope(ctypes.byref(L), ctypes.byref(rs) if rs is not None else None, d, d, d,
+                                                n, d, d, seq_len, d, d, d, 4, 4, None)
+    rs, keep = _abi.rope_scaling(1e6, 128)
+    assert rc(_layer(), rs, n=0) == _abi.DA_OK
+    assert rc(_layer(), None) == _abi.DA_ERR_INVALID_ARG
+    rs96, keep96 = _abi.rope_scaling(1e6, 96)
+    assert rc(_layer(), rs96) == _abi.DA_ERR_INVALID_ARG and "rotary_dim" in _abi.last_error()
+    assert rc(_layer(dtype=_abi.DA_FP32), rs) == _abi.DA_ERR_UNSUPPORTED
+    rs64, keep64 = _abi.rope_scaling(1e6, 64)
+    assert rc(_layer(head_dim=64, rotary_dim=64), rs64) == _abi.DA_ERR_UNSUPPORTED
+    rs40, keep40 = _abi.rope_scaling(1e6, 40)
+    assert rc(_layer(rotary_dim=40), rs40) == _abi.DA_ERR_UNSUPPORTED      # r/2 = 20: not a multiple of 8
+    sc = {"rope_type": "longrope", "short_factor": [1.0] * 64, "long_factor": [2.0] * 64,
+          "original_max_position_embeddings": 4096}
+    rsl, keepl = _abi.rope_scaling(1e4, 128, sc, 131072)
+    assert rc(_layer(), rsl, seq_len=None) == _abi.DA_ERR_INVALID_ARG and "seq_len" in _abi.last_error()
+    assert _abi.kv_rope_fused_supported(_layer()) and not _abi.kv_rope_fused_supported(_layer(head_dim=64, rotary_dim=64))
