@@ -315,8 +315,10 @@ static KbLayout kb_layout(int hq, int hkv, int d, int half, int es) {
 
 // FUSED: no cos/sin tables; per token the computing threads form its cos/sin (one rotary pair each) in the
 // stage with the arithmetic of rope_tables_kernel, so the results are the same bits; bf16 with d = 128 only.
+// Residency: the fused form fits 56 registers without spills, so four blocks share an SM (their stages,
+// 4 x 51 KB on the Qwen3-8B shape, fit too); the table forms keep three (the bf16 d = 64 one spills at 56).
 template <typename T, int D, bool FUSED>
-__global__ void __launch_bounds__(KB_THREADS, 3) kv_update_bulk_kernel(const KvUpdateArgs a, const KbLayout L,
+__global__ void __launch_bounds__(KB_THREADS, FUSED ? 4 : 3) kv_update_bulk_kernel(const KvUpdateArgs a, const KbLayout L,
                                                                    const __grid_constant__ RopeTurns f) {
   using V = Vec16<T>;
   constexpr int VEC = V::N;
