@@ -403,20 +403,23 @@ __global__ void __launch_bounds__(KB_THREADS, FUSED ? 4 : 3) kv_update_bulk_kern
       wk2[i] = norm ? f2_pack(a.k_norm_w[e], a.k_norm_w[e + 1]) : f2_pack(1.f, 1.f);
     }
     const int steps = (heads + 1) / 2;
+    // warps below steps % 8 take one more round per token than the others; the cos/sin fill goes to the others
+    // first (fill index fi: threads rotated so that warp steps % 8 starts at 0), off the token's critical path
+    const int fi = (warp * 32 + lane + 256 - 32 * (steps % 8)) & 255;
     for (int kk = 0; kk < n_mine; ++kk) {
       const int t = blockIdx.x + kk * gridDim.x;
       const int s = kk % KB_STAGES;
       uint8_t* st = kb_smem + s * L.bytes;
       int row = 0, pos = 0, len = 0;
       if (warp == 0 && lane == 0) row = a.rows[t];
-      const bool tabler = FUSED && warp * 32 + lane < half;   // forms one of this token's cos/sin pairs
+      const bool tabler = FUSED && fi < half;   // forms one of this token's cos/sin pairs
       if (tabler || (warp == 0 && lane == 0)) pos = a.positions[t];
       if (tabler && f.use_seq_len) len = a.seq_len[t];
       if (FUSED) {
         // this token's cos/sin into the stage, one rotary pair per computing thread (the tables' arithmetic);
         // that part of the stage is not copied in, and the barrier below keeps the warps within one token, so
         // the previous use of this stage has been read
-        const int i = warp * 32 + lane;
+        const int i = fi;
         if (i < half) {
           const bool use_long = f.use_seq_len && len > f.switch_len;
           const unsigned long long turn = use_long ? f.turn_long[i] : f.turn_short[i];
