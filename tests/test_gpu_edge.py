@@ -349,6 +349,26 @@ def test_yarn_mscale_ratio_decode(cuda):
     _close(st.out, res["out"])
 
 
+# (hq, hkv, rotated features): rounds per token = ceil((hq + hkv) / 2); rounds mod 8 = 2, 3, 5, 6, 7, 1, 0, 4
+@pytest.mark.parametrize("hq,hkv,rot", [(2, 1, 128), (4, 2, 64), (8, 1, 128), (10, 2, 128), (12, 2, 64),
+                                        (16, 2, 128), (24, 8, 96), (6, 2, 128)])
+def test_fused_rope_update_head_counts(cuda, hq, hkv, rot):
+    """The fused update hands each token's cos/sin fill to the warps with one round fewer (thread index rotated
+    by the rounds per token mod 8): every rotation, full and partial rotary, and more tokens than resident
+    blocks (stages reused) write the same bits as the table build followed by the plain update."""
+    from decoder_attention_gb300 import _abi as ab_, step
+    call = _prefill_call([900, 517], [0, 40], hq=hq, hkv=hkv, rot=rot, seed=50 + hq)
+    a, b = call.to(cuda), call.to(cuda)
+    sa, sb = step.AttentionStep(a, fused_rope=True), step.AttentionStep(b, fused_rope=False)
+    assert ab_.kv_rope_fused_supported(sa.L)
+    sa.update()
+    sb.update()
+    torch.cuda.synchronize()
+    ab_.check_device_error()
+    assert torch.equal(sa.q_rot, sb.q_rot)
+    assert torch.equal(a.k_cache, b.k_cache) and torch.equal(a.v_cache, b.v_cache)
+
+
 @pytest.mark.parametrize("number", [2, 3, 4, 5])
 def test_fused_rope_update_matches_two_calls(cuda, number):
     """da_kv_cache_update_rope (cos/sin formed in the kernel) writes the same bits as da_rope_tables_build
