@@ -122,6 +122,55 @@ def test_yarn_ramp_and_temperature():
     np.testing.assert_array_equal(inv_d, inv)
 
 
+def _yarn_golden():
+    return {k: float(v) for k, v in (ln.split() for ln in read_golden("yarn_ramp.txt"))}
+
+
+@pytest.mark.parametrize("truncate", [True, False])
+def test_yarn_ramp_golden(truncate):
+    """Page 1 "Scaled RoPE", yarn branch of rope_inv_freq, values derived by hand in the fixture: the
+    fractional pair index of 32 and 1 rotations over the original context, floor/ceil of the two ends
+    unless truncate is false, a ramp linear in the pair index between them."""
+    g = _yarn_golden()
+    tag = "truncate" if truncate else "no_truncate"
+    sc = {"rope_type": "yarn", "factor": 32.0, "original_max_position_embeddings": 4096,
+          "beta_fast": 32, "beta_slow": 1, "truncate": truncate}
+    base, _ = O.rope_inv_freq(128, 1e4)
+    inv, _ = O.rope_inv_freq(128, 1e4, sc)
+    ratio = inv / base
+    for i in (25, 33, 40):
+        assert ratio[i] == pytest.approx(g[f"ratio_{tag}_{i}"], abs=2e-9)
+    lo, hi = g[f"lo_{tag}"], g[f"hi_{tag}"]
+    i = np.arange(64)
+    np.testing.assert_allclose(ratio[i <= lo], 1.0, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(ratio[i >= hi], g["ratio_slow_end"], rtol=1e-15)
+    # the ramp is linear in i: recover its two ends from the interior and compare with the fixture
+    ramp = (1.0 - ratio) * 32.0 / 31.0
+    inner = (i > lo) & (i < hi)
+    slope, icpt = np.polyfit(i[inner], ramp[inner], 1)
+    np.testing.assert_allclose(ramp[inner], slope * i[inner] + icpt, atol=1e-12)
+    assert -icpt / slope == pytest.approx(lo, abs=1e-8)
+    assert (1.0 - icpt) / slope == pytest.approx(hi, abs=1e-8)
+    if not truncate:
+        assert lo == pytest.approx(g["dim_for_beta_fast"], abs=1e-9)
+        assert hi == pytest.approx(g["dim_for_beta_slow"], abs=1e-9)
+
+
+def test_yarn_attention_factor_golden():
+    """Page 1 "Scaled RoPE", yarn branch: the attention factor is mscale(s, mscale) / mscale(s, mscale_all_dim)
+    when both are stated, else mscale(s) = 0.1 ln s + 1; a stated attention_factor wins."""
+    g = _yarn_golden()
+    sc = {"rope_type": "yarn", "factor": 32.0, "original_max_position_embeddings": 4096}
+    _, af_pair = O.rope_inv_freq(128, 1e4, dict(sc, mscale=0.707, mscale_all_dim=1.0605))
+    _, af_alone = O.rope_inv_freq(128, 1e4, dict(sc, mscale=0.707))
+    _, af_none = O.rope_inv_freq(128, 1e4, sc)
+    _, af_given = O.rope_inv_freq(128, 1e4, dict(sc, mscale=0.707, mscale_all_dim=1.0605, attention_factor=1.25))
+    assert af_pair == pytest.approx(g["attention_mscale_pair"], abs=2e-9)
+    assert af_alone == pytest.approx(g["attention_mscale_alone"], abs=2e-9)
+    assert af_none == pytest.approx(g["attention_mscale_alone"], abs=2e-9)
+    assert af_given == 1.25
+
+
 def test_unknown_kind_refused():
     """Page 1 rope_inv_freq: an unimplemented type raises ValueError naming it."""
     with pytest.raises(ValueError, match="dynamic"):
