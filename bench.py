@@ -49,6 +49,15 @@ ORACLE_SAMPLES = {
         "llama31_8b_long_decode": ([], [0], 1),
         "phi4_gemma2_mixed": ([0], list(range(4)), 1),
     },
+    # split into (chunk or token, KV head) units over every host core: the whole Qwen3, Mistral and Llama
+    # workloads, a quarter of the mixed one's chunks and decode tokens
+    "allcores": {
+        "tiny_prefill_fp32": ([0], [], None),
+        "qwen3_8b_prefill": ([0, 1, 2, 3], [], None),
+        "mistral_swa_decode": ([], list(range(64)), None),
+        "llama31_8b_long_decode": ([], list(range(16)), None),
+        "phi4_gemma2_mixed": ([0, 1], list(range(30)), None),
+    },
 }
 
 
@@ -66,6 +75,8 @@ def parse_args(argv=None):
                          "(da_*_paged entry points)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", action="store_true",
+                    help="time only --workload (the default run also times the decode and mixed workloads)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)   # internal: child process
     ap.add_argument("--sample-kind", default="baseline", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -192,9 +203,34 @@ def headline(work, seconds):
 
 # ---------------------------------------------------------------------------------------------- oracle leg
 
+def cpu_model():
+    """The host CPU's model name (lscpu's "Model name", else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
 def oracle_sample_child(workload, kind, iters):
-    """Runs in a fresh single-threaded process: builds the workload once, times the oracle `iters` times on
-    the bounded sample, prints one JSON line with the per-iteration seconds."""
+    """Runs in a fresh process: builds the workload once, times the oracle `iters` times on the bounded
+    sample, prints one JSON line with the per-iteration seconds.
+
+    kind "baseline"/"step": single-threaded, the sample run in order. kind "allcores": the sample cut into
+    units of one (chunk or decode token, KV head group), run by a pool of one thread per host core (numpy
+    and BLAS release the interpreter lock in their array loops; BLAS itself is held to one thread per call),
+    timed from the first unit's start to the last unit's end."""
+    import concurrent.futures as cf
+
     import torch
 
     from decoder_attention_gb300 import inputs, work as W
@@ -204,22 +240,45 @@ def oracle_sample_child(workload, kind, iters):
     num = inputs.NUMBERS[workload]
     gen_dev = "cuda" if (num in (3, 4, 5) and torch.cuda.is_available()) else "cpu"
     wl = inputs.make(num, scale="full", device=gen_dev)
-    samples = [inputs.subset(c, chunks, dec, device="cpu", kv_heads=kvh) for c in wl.layers]
+    if kind == "allcores":
+        hkv = wl.layers[0].num_key_value_heads
+        samples = [inputs.subset(c, cs, ds, device="cpu", kv_heads=1, kv_first=g)
+                   for c in wl.layers for cs, ds in [([b], []) for b in chunks] + [([], [t]) for t in dec]
+                   for g in range(hkv)]
+    else:
+        samples = [inputs.subset(c, chunks, dec, device="cpu", kv_heads=kvh) for c in wl.layers]
+    n_layers = len(wl.layers)
     del wl
+    if gen_dev == "cuda":
+        torch.cuda.empty_cache()
     tot = {}
     for s in samples:
         for k, v in W.layer_call_work(s).items():
             tot[k] = tot.get(k, 0) + v
+    if kind == "allcores":      # each token was counted once per KV-head unit
+        for k in ("tokens", "prefill_tokens", "decode_tokens"):
+            tot[k] = tot.get(k, 0) // hkv
     secs = []
-    for _ in range(iters):
-        t0 = time.perf_counter()
-        for s in samples:
-            ostep.run_layer_call(s)
-        secs.append(time.perf_counter() - t0)
-    heads = "all heads" if kvh is None else f"{kvh} KV head(s) and their query heads"
-    desc = (f"{len(chunks)} prefill chunk(s) and {len(dec)} decode token(s), {heads}, per layer x {len(samples)} "
-            f"layer(s); single-threaded fp64 numpy")
-    print(json.dumps({"seconds": secs, "sample": desc, "work": tot}))
+    cores = 1
+    if kind == "allcores":
+        cores = os.cpu_count() or 1
+        with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+            for _ in range(iters):
+                t0 = time.perf_counter()
+                list(ex.map(ostep.run_layer_call, samples))
+                secs.append(time.perf_counter() - t0)
+        desc = (f"{len(chunks)} prefill chunk(s) and {len(dec)} decode token(s) per layer x {n_layers} layer(s), "
+                f"as {len(samples)} (chunk or token, KV head) units over {cores} threads; fp64 numpy")
+    else:
+        for _ in range(iters):
+            t0 = time.perf_counter()
+            for s in samples:
+                ostep.run_layer_call(s)
+            secs.append(time.perf_counter() - t0)
+        heads = "all heads" if kvh is None else f"{kvh} KV head(s) and their query heads"
+        desc = (f"{len(chunks)} prefill chunk(s) and {len(dec)} decode token(s), {heads}, per layer x "
+                f"{n_layers} layer(s); single-threaded fp64 numpy")
+    print(json.dumps({"seconds": secs, "sample": desc, "work": tot, "cores": cores}))
 
 
 def run_oracle_sample(workload, kind="baseline", iters=1):
@@ -242,7 +301,7 @@ def main_reference(args):
         return 0
     from decoder_attention_gb300 import inputs
     r = run_oracle_sample(args.workload, "step", args.warmup + args.steps)
-    sec = statistics.mean(r["seconds"][args.warmup:])
+    sec = statistics.median(r["seconds"][args.warmup:])
     value, unit, tps = headline(r["work"], sec)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
@@ -258,15 +317,16 @@ def main_reference(args):
 
 # ---------------------------------------------------------------------------------------------- native leg
 
-def main_native(args):
+def measure_native(args, workload, dev, world, rank, with_e2e=True):
+    """Times one workload through the C ABI on `dev` (inputs resident in HBM; L2 flushed before every timed
+    step, outside the step's events) and returns its record: the median step time (the mean beside it), the
+    step's breakdown, the roofline of the dominant kernel (and of both halves when the step has prefill and
+    decode), e2e through host buffers, launch count and clocks. The workload's tensors are freed on return."""
     import torch
 
     from decoder_attention_gb300 import _abi, inputs, step as S, work as W
 
-    rank, world, local = dist_init(args)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    num = inputs.NUMBERS[args.workload]
+    num = inputs.NUMBERS[workload]
     wl = inputs.make(num, scale=args.scale if num in (3, 4, 5) else "full", device=dev)
     pools = []
     if args.kv_block > 0:
@@ -288,7 +348,7 @@ def main_native(args):
         for st in steps:
             st.run()
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     time.sleep(0.3)
     clocks.mark_start()
     for _ in range(max(args.warmup, 3)):
@@ -322,6 +382,7 @@ def main_native(args):
     wall = time.perf_counter() - wall0
     clocks.mark_end()
     _abi.check_device_error()
+
     def marks(e, li):   # (after update, after prefill, after decode) of layer li; an empty stage adds no event
         a = e[1 + 3 * li]
         b = e[2 + 3 * li] if steps[li].call.n_prefill else a
@@ -335,31 +396,32 @@ def main_native(args):
     dec_ms = [sum(interval(*marks(e, li)[1:]) for li in range(n_layers)) for e in ev]
     pre_ms = [sum((e[0] if li == 0 else marks(e, li - 1)[2]).elapsed_time(marks(e, li)[0]) for li in range(n_layers))
               for e in ev]
-    ms = statistics.mean(step_ms)
+    ms = statistics.median(step_ms)
     ms_all = reduce_max(ms, world)
     clock_info = clocks.stop()
 
     value_1, unit, _ = headline(work, ms_all / 1e3)
-    value = value_1 * world
-    tokens_per_s = work["tokens"] * world / (ms_all / 1e3)
-
     peaks, peak_kind = load_peaks()
+    parts = {}
     if work["prefill_flops"] > 0:
-        kms = statistics.mean(pf_ms)
+        kms = statistics.median(pf_ms)
         achieved = work["prefill_flops"] / (kms / 1e3) / 1e12
-        roof = {"kernel": "prefill_kernel (tcgen05)", "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "peak_kind": f"bf16 dense burst, of {peak_kind}", "launch_ms": kms,
-                "algorithmic_flops_per_launch": work["prefill_flops"] / n_layers,
-                "traffic": None if pools else load_traffic("prefill_kernel", args.workload)}
-    else:
-        kms = statistics.mean(dec_ms)
+        parts["prefill"] = {
+            "kernel": "prefill_kernel (tcgen05)", "bound": "tensor", "achieved": achieved,
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "peak_kind": f"bf16 dense burst, of {peak_kind}", "launch_ms": kms / n_layers,
+            "launches_per_step": n_layers, "algorithmic_flops_per_launch": work["prefill_flops"] / n_layers,
+            "traffic": None if (pools or n_layers > 1) else load_traffic("prefill_kernel", workload)}
+    if work["decode_bytes"] > 0:
+        kms = statistics.median(dec_ms)
         achieved = work["decode_bytes"] / (kms / 1e3) / 1e9
-        roof = {"kernel": "decode_kernel + merge_kernel (one da_attn_decode call)", "bound": "hbm",
-                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "peak_kind": f"HBM copy, of {peak_kind}", "launch_ms": kms,
-                "algorithmic_bytes_per_launch": work["decode_bytes"] / n_layers,
-                "traffic": None if pools else load_traffic("decode_kernel", args.workload)}
+        parts["decode"] = {
+            "kernel": "decode_kernel + merge_kernel (one da_attn_decode call)", "bound": "hbm",
+            "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "peak_kind": f"HBM copy, of {peak_kind}", "launch_ms": kms / n_layers, "launches_per_step": n_layers,
+            "algorithmic_bytes_per_launch": work["decode_bytes"] / n_layers,
+            "traffic": None if (pools or n_layers > 1) else load_traffic("decode_kernel", workload)}
+    roof = parts["prefill"] if "prefill" in parts else parts["decode"]
 
     # ------------------------------------------------------------------ end to end (host buffers)
     # Each step uploads its inputs (new tokens' q/k/v, rows, positions, chunk offsets) from pinned host
@@ -368,7 +430,7 @@ def main_native(args):
     # and step i-1's download overlap step i's kernels. The KV caches stay resident (they are the layer's
     # state, shared by both buffer sets).
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         names = ["q", "k", "v", "tok_rows", "tok_pos", "tok_seq_len", "q_start", "pf_rows", "pf_first_pos",
                  "dec_rows", "dec_pos"]
         sets = []
@@ -439,39 +501,90 @@ def main_native(args):
                "ms_per_step": e2e_ms, "steps": n_e2e,
                "via": "AttentionStep.run (C ABI) with pinned host inputs/outputs; upload, kernels and download "
                       "on three streams, two buffer sets, L2 not flushed (each step moves more than L2 holds)"}
+        del sets, host_in, host_out
 
-    cpu_base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    rec = {
+        "value": value_1 * world, "unit": unit, "ms_per_step": ms_all,
+        "ms_per_step_mean": statistics.mean(step_ms), "timing": f"median of {args.steps} timed steps",
+        "dtype": "bf16" if wl.layers[0].dtype == torch.bfloat16 else "fp32",
+        "config": {"workload": workload, "number": num, "scale": args.scale, "description": wl.description,
+                   "l2": "flushed (256 MB write) before every timed step, outside the step's events",
+                   "kv": (f"paged pool, {args.kv_block}-position blocks in shuffled order" if pools
+                          else "contiguous caches"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": work["tokens"] * world / (ms_all / 1e3),
+        "breakdown_ms": {"rope_and_cache_update": statistics.median(pre_ms), "prefill": statistics.median(pf_ms),
+                         "decode": statistics.median(dec_ms),
+                         "wall_ms_per_step_incl_flush": wall * 1e3 / args.steps},
+        "work": {k: v for k, v in work.items() if v},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": sum(st.kernel_launches() for st in steps) * args.steps,
+        "clocks": clock_info,
+        "peaks": dict(peaks, kind=peak_kind),
+    }
+    if len(parts) > 1:
+        rec["roofline_parts"] = parts
+    del steps, pools, wl, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+# The workloads the default invocation times beside the headline (each as a sub-record of the same line):
+# the sliding-window decode, the long-context decode and the mixed prefill + decode layer pair.
+SIDE_WORKLOADS = ("mistral_swa_decode", "llama31_8b_long_decode", "phi4_gemma2_mixed")
+
+
+def cpu_baselines(workload, all_cores=True):
+    """The oracle on the host cores: single-threaded on the bounded sample, and (all_cores) the same kind of
+    sample spread over a process pool of every core. Reported, never fatal."""
+    out = {}
+    try:
+        r = run_oracle_sample(workload, "baseline", 1)
+        v, u, _ = headline(r["work"], r["seconds"][0])
+        out = {"value": v, "unit": u, "cores": 1, "kind": "oracle", "sample": r["sample"],
+               "seconds": r["seconds"][0], "host_cores": os.cpu_count(), "cpu_model": cpu_model()}
+    except Exception as exc:
+        return {"value": None, "unit": None, "cores": 1, "kind": "oracle", "error": str(exc)[-300:]}
+    if all_cores:
         try:
-            r = run_oracle_sample(args.workload, "baseline", 1)
+            r = run_oracle_sample(workload, "allcores", 1)
             v, u, _ = headline(r["work"], r["seconds"][0])
-            cpu_base = {"value": v, "unit": u, "cores": 1, "kind": "oracle", "sample": r["sample"],
-                        "seconds": r["seconds"][0], "host_cores": os.cpu_count()}
-        except Exception as exc:  # reported, not fatal
-            cpu_base = {"value": None, "unit": unit, "cores": 1, "kind": "oracle", "error": str(exc)[-300:]}
+            out["all_cores"] = {"value": v, "unit": u, "cores": r["cores"], "sample": r["sample"],
+                                "seconds": r["seconds"][0]}
+        except Exception as exc:
+            out["all_cores"] = {"value": None, "error": str(exc)[-300:]}
+    return out
 
+
+def main_native(args):
+    import torch
+
+    rank, world, local = dist_init(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    rec = measure_native(args, args.workload, dev, world, rank, with_e2e=not args.no_e2e)
+    side = {}
+    if args.workload == DEFAULT_WORKLOAD and not args.single and args.kv_block == 0 and args.scale == "full":
+        for w in SIDE_WORKLOADS:
+            side[w] = measure_native(args, w, dev, world, rank, with_e2e=not args.no_e2e)
+    cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if wl.layers[0].dtype == torch.bfloat16 else "fp32",
-            "data": "synthetic",
-            "config": {"workload": args.workload, "number": num, "scale": args.scale, "description": wl.description,
-                       "l2": "flushed (256 MB write) before every timed step, outside the step's events",
-                       "kv": (f"paged pool, {args.kv_block}-position blocks in shuffled order" if pools
-                              else "contiguous caches"),
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "tokens_per_s": tokens_per_s,
-            "breakdown_ms": {"rope_and_cache_update": statistics.mean(pre_ms), "prefill": statistics.mean(pf_ms),
-                             "decode": statistics.mean(dec_ms), "wall_ms_per_step_incl_flush": wall * 1e3 / args.steps},
-            "work": {k: v for k, v in work.items() if v},
-            "roofline": roof,
-            "e2e": e2e,
-            "gpu_launches": sum(st.kernel_launches() for st in steps) * args.steps,
-            "clocks": clock_info,
-            "cpu_baseline": cpu_base,
-            "peaks": dict(peaks, kind=peak_kind),
+            "metric": METRIC, "value": rec["value"], "unit": rec["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": rec["dtype"], "data": "synthetic",
         }
+        line.update({k: v for k, v in rec.items() if k not in line})
+        line["cpu_baseline"] = cpu_baselines(args.workload) if cpu else None
+        if side:
+            for w, r in side.items():
+                r.pop("peaks", None)
+                r["cpu_baseline"] = cpu_baselines(w, all_cores=False) if cpu else None
+            line["workloads"] = side
+            line["gpu_launches"] += sum(r["gpu_launches"] for r in side.values())
+            line["gpu_launches_note"] = "headline workload plus the side workloads' timed steps"
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -552,8 +665,8 @@ def main_native_mla(args):
     barrier(world)
     clocks.mark_end()
     _abi.check_device_error()
-    ms = reduce_max(statistics.mean(e[0].elapsed_time(e[2]) for e in ev), world)
-    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms = reduce_max(statistics.median(e[0].elapsed_time(e[2]) for e in ev), world)
+    dec_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     clock_info = clocks.stop()
     value = work["decode_bytes"] / (ms / 1e3) / 1e9 * world
     peaks, peak_kind = load_peaks()
@@ -628,7 +741,7 @@ def main_reference_mla(args):
     for _ in range(args.warmup + args.steps):
         v, sec, desc = mla_oracle_sample(call, [0])
         secs.append(sec)
-    sec = statistics.mean(secs[args.warmup:])
+    sec = statistics.median(secs[args.warmup:])
     keys = int(call.positions[0]) + 1
     value = keys * 576 * 2 / sec / 1e9
     print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
@@ -700,7 +813,7 @@ def main_native_block(args):
                 fn()
                 ev[i][j + 1].record(stream)
         torch.cuda.synchronize()
-        return [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(len(fn_parts))]
+        return [statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(len(fn_parts))]
 
     parts = [fused, st.prefill, lambda: _abi.linear(st.out.view(n, hq * 128), w_o, None, n, hidden, hq * 128, y)]
     timed(parts, max(args.warmup, 3))

@@ -357,10 +357,13 @@ DecodePlan decode_plan(int hkv, int n_seqs, int max_len, int window, bool aligne
   // keys a chunk sequence spans at most (aligned: from the window start rounded down to a 64-key tile)
   const int max_keys = (window > 0 ? std::min(window, max_len) : max_len) + (aligned ? dec::BK - 1 : 0);
   int chunk = 512;
-  const char* env = std::getenv("DA_DECODE_CHUNK");   // tuning override (multiple of 64)
+#ifdef DA_TUNING_HOOKS
+  const char* env = std::getenv("DA_DECODE_CHUNK");   // sweep override in tuning builds only (multiple of 64)
   if (env && std::atoi(env) >= 64 && std::atoi(env) % 64 == 0) {
     chunk = std::atoi(env);
-  } else {
+  } else
+#endif
+  {
     // Grow the chunk (fewer partials to write and merge) while the grid keeps >= 8 CTAs per SM of a
     // 152-SM GB300 busy.
     const long long target = 152LL * 8;
@@ -411,12 +414,9 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const DecodePlan& plan, void* 
   prm.n_splits = plan.n_splits;
   prm.err = a.err;
   const int smem = NST * STAGE_BYTES + 2 * NST * 8 + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // per device and cheap: set on every launch, so that a call on any device (or host thread) finds it
+  cudaError_t ea = cudaFuncSetAttribute(decode_kernel<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (ea != cudaSuccess) return ea;
   dim3 grid(plan.n_splits, a.hkv, a.n_seqs);
   decode_kernel<NST><<<grid, THREADS, smem, stream>>>(tmk, tmv, prm);
   cudaError_t e = cudaGetLastError();

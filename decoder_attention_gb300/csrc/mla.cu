@@ -521,12 +521,8 @@ cudaError_t launch_mla_decode(const MlaArgs& a, const MlaPlan& plan, void* works
   if (a.hq == 128) {
     e = launch_mla_pair_decode(a, plan, prm.ws_o, prm.ws_ml, stream);
   } else {
-    static bool attr_set = false;
-    if (!attr_set) {
-      e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      attr_set = true;
-    }
+    e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   // per device
+    if (e != cudaSuccess) return e;
     dim3 grid(plan.n_splits, (a.hq + HPC - 1) / HPC, a.n_seqs);
     mla_decode_kernel<<<grid, THREADS, smem, stream>>>(tmc, prm);
     e = cudaGetLastError();

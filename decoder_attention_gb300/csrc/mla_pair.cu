@@ -528,8 +528,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }  // namespace mlap
 
 int mla_pair_chunk(int n_seqs, int max_keys) {
-  const char* env = std::getenv("DA_MLA_CHUNK");   // tuning override (multiple of 256)
+#ifdef DA_TUNING_HOOKS
+  const char* env = std::getenv("DA_MLA_CHUNK");   // sweep override in tuning builds only (multiple of 256)
   if (env && std::atoi(env) >= mlap::PT && std::atoi(env) % mlap::PT == 0) return std::atoi(env);
+#endif
   int chunk = mlap::PT;
   // grow the chunk (fewer partials) while the grid keeps >= 4 waves of the 76 CTA pairs a 152-SM part holds
   while (chunk < 16384 && static_cast<long long>(n_seqs) * ((max_keys + 2 * chunk - 1) / (2 * chunk)) >= 4LL * 76)
@@ -567,12 +569,9 @@ cudaError_t launch_mla_pair_decode(const MlaArgs& a, const MlaPlan& plan, float*
   prm.hkv = 1;
   prm.oob_row = static_cast<int>(rows_total);
   prm.err = a.err;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // per device and cheap: set on every launch
+  cudaError_t ea = cudaFuncSetAttribute(mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (ea != cudaSuccess) return ea;
   mla_pair_kernel<<<dim3(2 * plan.n_splits, 1, a.n_seqs), THREADS, SMEM_BYTES, stream>>>(tmq, tmc, prm);
   return cudaGetLastError();
 }

@@ -360,12 +360,17 @@ __global__ void __launch_bounds__(KB_THREADS, FUSED ? 4 : 3) kv_update_bulk_kern
         bulk_load(st + L.sin, a.sin + static_cast<long long>(t) * half, half * 4, full(s));
       }
     };
-    for (int kk = 0; kk < n_mine && kk < KB_STAGES; ++kk) issue(kk);
+    int issued = 0;
+    for (; issued < n_mine && issued < KB_STAGES; ++issued) issue(issued);
     for (int kk = 0; kk < n_mine; ++kk) {
       const int t = blockIdx.x + kk * gridDim.x;
       const int s = kk % KB_STAGES;
       const uint32_t st = sbase + s * L.bytes;
-      if (!mbar_wait(done(s), (kk / KB_STAGES) & 1, a.err)) break;
+      if (!mbar_wait(done(s), (kk / KB_STAGES) & 1, a.err)) {
+        // gave up (the error word is set): let the loads already issued for stages kk.. land before exiting
+        for (int j = kk; j < issued; ++j) mbar_wait(full(j % KB_STAGES), (j / KB_STAGES) & 1, a.err);
+        break;
+      }
       const long long slot = *reinterpret_cast<const long long*>(kb_smem + s * L.bytes + L.hdr);
       bulk_store(static_cast<T*>(a.q_rot) + static_cast<long long>(t) * a.hq * D, st, a.hq * D * es);
       if (slot >= 0) {
@@ -379,6 +384,7 @@ __global__ void __launch_bounds__(KB_THREADS, FUSED ? 4 : 3) kv_update_bulk_kern
       if (kk + KB_STAGES < n_mine) {
         bulk_wait_read();   // the stage is refilled only after its stores have read it
         issue(kk + KB_STAGES);
+        issued = kk + KB_STAGES + 1;
       }
     }
     bulk_wait_all();

@@ -458,14 +458,17 @@ def make(workload, scale="full", device="cpu", **kw):
     return BUILDERS[num](scale=scale, device=device, **kw)
 
 
-def subset(call: LayerCall, chunks, decode_idx, device="cpu", kv_heads=None) -> LayerCall:
+def subset(call: LayerCall, chunks, decode_idx, device="cpu", kv_heads=None, kv_first=0) -> LayerCall:
     """A LayerCall holding only prefill chunks `chunks` and decode tokens `decode_idx` of `call`, with the
-    cache rows they use (renumbered 0..k-1) copied to `device`; with `kv_heads`, only the first kv_heads
-    KV heads and their query-head groups. Bookkeeping only: used to size bounded samples of a full
-    workload for the CPU oracle."""
+    cache rows they use (renumbered 0..k-1) copied to `device`; with `kv_heads`, only KV heads
+    kv_first .. kv_first + kv_heads - 1 and their query-head groups. Bookkeeping only: used to size bounded
+    samples of a full workload for the CPU oracle."""
     chunks = list(chunks)
     hkv = call.num_key_value_heads if kv_heads is None else int(kv_heads)
-    hq = hkv * (call.num_attention_heads // call.num_key_value_heads)
+    grp = call.num_attention_heads // call.num_key_value_heads
+    hq = hkv * grp
+    g0, g1 = kv_first, kv_first + hkv
+    q0, q1 = g0 * grp, g1 * grp
     decode_idx = list(decode_idx)
     qs = call.q_start.cpu().tolist()
     pf_rows = call.pf_rows.cpu().tolist()
@@ -490,13 +493,14 @@ def subset(call: LayerCall, chunks, decode_idx, device="cpu", kv_heads=None) -> 
     fields = {k: getattr(call, k) for k in call.__dataclass_fields__}
     fields.update(
         num_attention_heads=hq, num_key_value_heads=hkv,
-        q=call.q[idx.to(call.q.device), :hq].to(device), k=call.k[idx.to(call.k.device), :hkv].to(device),
-        v=call.v[idx.to(call.v.device), :hkv].to(device),
+        q=call.q[idx.to(call.q.device), q0:q1].to(device), k=call.k[idx.to(call.k.device), g0:g1].to(device),
+        v=call.v[idx.to(call.v.device), g0:g1].to(device),
         tok_rows=_i32(tr + d_rows, device), tok_pos=_i32(tp + d_pos, device), tok_seq_len=_i32(tl + d_len, device),
         n_prefill=n_pf, q_start=_i32(q_start, device), pf_rows=_i32([remap[pf_rows[b]] for b in chunks], device),
         pf_first_pos=_i32([pf_fp[b] for b in chunks], device), max_q_len=max(lens) if lens else 0,
         dec_rows=_i32(d_rows, device), dec_pos=_i32(d_pos, device),
-        k_cache=call.k_cache[ridx, :hkv].to(device), v_cache=call.v_cache[ridx, :hkv].to(device),
+        k_cache=call.k_cache[ridx, g0:g1].to(device), v_cache=call.v_cache[ridx, g0:g1].to(device),
+        sinks=call.sinks[q0:q1].to(device) if call.sinks is not None else None,
         q_norm_w=call.q_norm_w.to(device) if call.q_norm_w is not None else None,
         k_norm_w=call.k_norm_w.to(device) if call.k_norm_w is not None else None,
         meta=dict(call.meta))

@@ -355,9 +355,13 @@ def test_yarn_mscale_ratio_decode(cuda):
 def test_fused_rope_update_head_counts(cuda, hq, hkv, rot):
     """The fused update hands each token's cos/sin fill to the warps with one round fewer (thread index rotated
     by the rounds per token mod 8): every rotation, full and partial rotary, and more tokens than resident
-    blocks (stages reused) write the same bits as the table build followed by the plain update."""
+    blocks (stages reused) write the same bits as the table build followed by the plain update. 3517 tokens
+    exceed 4 stages x 4 resident blocks x 152 SMs, so every block refills its stages and runs both phases of
+    its full/done barriers."""
     from decoder_attention_gb300 import _abi as ab_, step
-    call = _prefill_call([900, 517], [0, 40], hq=hq, hkv=hkv, rot=rot, seed=50 + hq)
+    call = _prefill_call([2900, 617], [0, 40], hq=hq, hkv=hkv, rot=rot, seed=50 + hq)
+    props = torch.cuda.get_device_properties(cuda)
+    assert call.n_tokens > 4 * 4 * props.multi_processor_count
     a, b = call.to(cuda), call.to(cuda)
     sa, sb = step.AttentionStep(a, fused_rope=True), step.AttentionStep(b, fused_rope=False)
     assert ab_.kv_rope_fused_supported(sa.L)
