@@ -192,16 +192,19 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
       "};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63]) : "memory");
 }
 
-// One pass over a row's 128 scores: soft-cap (CAP), mask to the visible column range [lo_c, hi_c] (MASK),
-// and the row max with 8 independent partial maxima (one running max would be a 128-long dependency chain).
-// Soft-capped logits in log2 units: cap_l2 * tanh(z * cap_in) written as cap_l2 - 2 cap_l2 / (2^(z * cap_k) + 1)
-// with cap_k = 2 log2(e) * cap_in (tanh x = 1 - 2 / (e^2x + 1)). It saturates to -cap_l2 / +cap_l2 as the
-// power underflows to 0 / overflows to inf; its absolute error is a few ulp of cap_l2.
-__device__ __forceinline__ void cap_pass(uint32_t (&zr)[BN], float cap_k, float cap_l2) {
-  const float m2 = -2.f * cap_l2;
+// Soft-cap of a row's 128 raw scores: zr <- tanh(z * cap_in), cap_in = scale / cap, so that cap_l2 * zr is
+// the capped logit cap * tanh(scale z / cap) in log2 units; the softmax folds the factor cap_l2 into its
+// exponent's FMA (and into the row max, cap_l2 > 0). One packed multiply per two scores and one MUFU tanh
+// per score: the soft-capped layer's softmax is bound by the MUFU pipe and the softmax warps' issue.
+__device__ __forceinline__ void cap_pass(uint32_t (&zr)[BN], float cap_in) {
+  const uint64_t k2 = f2_pack(cap_in, cap_in);
 #pragma unroll
-  for (int c = 0; c < BN; ++c)
-    zr[c] = __float_as_uint(fmaf(rcp_approx(ex2(__uint_as_float(zr[c]) * cap_k) + 1.f), m2, cap_l2));
+  for (int c = 0; c < BN; c += 2) {
+    float a, b;
+    f2_unpack(f2_mul(f2_pack(__uint_as_float(zr[c]), __uint_as_float(zr[c + 1])), k2), a, b);
+    zr[c] = __float_as_uint(tanh_approx(a));
+    zr[c + 1] = __float_as_uint(tanh_approx(b));
+  }
 }
 
 // Columns outside [lo_c, hi_c] (keys this row does not see) set to -inf: one unsigned compare per column.
@@ -763,9 +766,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const uint32_t t_s = tmem + lane_addr + w * BN;
     const uint32_t t_o = tmem + lane_addr + 256 + w * D;
     const float cap = prm.softcap;
-    const float cap_k = cap > 0.f ? 2.f * kLog2e * prm.scale / cap : 0.f;
-    const float cap_l2 = cap * kLog2e;
-    const float zmul = cap > 0.f ? 1.f : prm.scale * kLog2e;   // z * zmul is the logit in log2 units
+    const float cap_in = cap > 0.f ? prm.scale / cap : 0.f;
+    // z * zmul is the logit in log2 units: z the raw score, or for capped layers tanh(scale z / cap)
+    const float zmul = cap > 0.f ? cap * kLog2e : prm.scale * kLog2e;
     int ns = 0, nod = 0;
     bool ok = true;
     // The epilogue of an item (O / l out through the warp's staging slot) is deferred into the first tile
@@ -900,11 +903,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const int kstart = t * BN;
         const bool need_mask = !(kstart + BN - 1 <= my_pmin &&
                                  (window == 0 || my_pmax - kstart <= window - 1) && kstart + BN <= kv_len);
-        // zr: the raw score q.k (scaled into log2 units inside the exponent), or for capped layers the
-        // capped logit already in log2 units. Visible keys of this row in the tile: columns [lo_c, hi_c].
+        // zr: the raw score q.k, or for capped layers tanh(scale q.k / cap); either way zr * zmul is the logit
+        // in log2 units (the factor is applied inside the exponent). Visible keys: columns [lo_c, hi_c].
         const int hi_c = min(p, kv_len - 1) - kstart;
         const int lo_c = window > 0 ? p - window + 1 - kstart : -BN;
-        if (cap > 0.f) cap_pass(zr, cap_k, cap_l2);
+        if (cap > 0.f) cap_pass(zr, cap_in);
         if (need_mask) mask_pass(zr, lo_c, hi_c);
         const float tmax = row_max(zr) * zmul;
         const float m_new = fmaxf(m, tmax);

@@ -404,8 +404,8 @@ def phi4_gemma2_mixed(scale="full", device="cpu", q_mult=1.0):
         n_chunks, chunk, n_dec, dlo, dhi, pmax, w, hq, hkv = 8, 1024, 120, 512, 65536, 64512, 4096, 24, 8
         M = 65536
     elif scale == "profile":
-        n_chunks, chunk, n_dec, dlo, dhi, pmax, w, hq, hkv = 2, 1024, 16, 512, 16384, 15360, 4096, 24, 8
-        M = 16384
+        n_chunks, chunk, n_dec, dlo, dhi, pmax, w, hq, hkv = 6, 1024, 8, 512, 24576, 23552, 4096, 24, 8
+        M = 24576
     else:
         n_chunks, chunk, n_dec, dlo, dhi, pmax, w, hq, hkv = 3, 100, 9, 50, 6000, 5800, 512, 6, 2
         M = 6000
