@@ -207,6 +207,43 @@ __device__ __forceinline__ void cap_pass(uint32_t (&zr)[BN], float cap_in) {
   }
 }
 
+// Soft-cap on the FMA pipe for tiles whose scores are all small: tanh(u) = u * P(u^2) with a cubic P fitted
+// here to minimise the relative error over |u| <= kCapPolyRange (6.2e-7 evaluated in fp32, against 1e-5 for the
+// MUFU tanh). Four packed multiplies or FMAs per two scores and no MUFU operation, which leaves the MUFU pipe
+// to the exponentials.
+constexpr float kCapPolyRange = 0.5f;
+constexpr float kTanhP0 = 0x1.ffffeep-1f, kTanhP1 = -0x1.5542f2p-2f, kTanhP2 = 0x1.0e2330p-3f,
+                kTanhP3 = -0x1.6bbec2p-5f;
+__device__ __forceinline__ float tanh_poly(float u) {
+  const float v = u * u;
+  return u * fmaf(fmaf(fmaf(kTanhP3, v, kTanhP2), v, kTanhP1), v, kTanhP0);
+}
+__device__ __forceinline__ void cap_poly_pass(uint32_t (&zr)[BN], float cap_in) {
+  const uint64_t k2 = f2_pack(cap_in, cap_in), p3 = f2_pack(kTanhP3, kTanhP3), p2 = f2_pack(kTanhP2, kTanhP2),
+                 p1 = f2_pack(kTanhP1, kTanhP1), p0 = f2_pack(kTanhP0, kTanhP0);
+#pragma unroll
+  for (int c = 0; c < BN; c += 2) {
+    const uint64_t u = f2_mul(f2_pack(__uint_as_float(zr[c]), __uint_as_float(zr[c + 1])), k2);
+    const uint64_t v = f2_mul(u, u);
+    const uint64_t p = f2_fma(f2_fma(f2_fma(p3, v, p2), v, p1), v, p0);
+    float a, b;
+    f2_unpack(f2_mul(p, u), a, b);
+    zr[c] = __float_as_uint(a);
+    zr[c + 1] = __float_as_uint(b);
+  }
+}
+
+// Largest |z| of a row's 128 scores (8 independent partial maxima).
+__device__ __forceinline__ float row_absmax(const uint32_t (&zr)[BN]) {
+  float mx[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mx[e] = fmaxf(fabsf(__uint_as_float(zr[2 * e])), fabsf(__uint_as_float(zr[2 * e + 1])));
+#pragma unroll
+  for (int c = 16; c < BN; c += 2)
+    mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], fabsf(__uint_as_float(zr[c])), fabsf(__uint_as_float(zr[c + 1])));
+  return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+}
+
 // Columns outside [lo_c, hi_c] (keys this row does not see) set to -inf: one unsigned compare per column.
 __device__ __forceinline__ void mask_pass(uint32_t (&zr)[BN], int lo_c, int hi_c) {
   if (hi_c < lo_c) lo_c = BN, hi_c = BN;   // no visible column: c - lo_c wraps above the span for every c
@@ -291,7 +328,7 @@ struct IssItem {
 
 // PAGED: keys come from a paged pool through the block table (a separate instantiation, so that the
 // contiguous form carries none of the lookups).
-template <bool PAGED>
+template <bool PAGED, bool CAP>
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmq,
                                                              const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
@@ -765,7 +802,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const uint32_t lane_addr = static_cast<uint32_t>(wi * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + w * BN;
     const uint32_t t_o = tmem + lane_addr + 256 + w * D;
-    const float cap = prm.softcap;
+    const float cap = CAP ? prm.softcap : 0.f;   // uncapped layers run an instantiation without the cap code
     const float cap_in = cap > 0.f ? prm.scale / cap : 0.f;
     // z * zmul is the logit in log2 units: z the raw score, or for capped layers tanh(scale z / cap)
     const float zmul = cap > 0.f ? cap * kLog2e : prm.scale * kLog2e;
@@ -907,9 +944,23 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         // in log2 units (the factor is applied inside the exponent). Visible keys: columns [lo_c, hi_c].
         const int hi_c = min(p, kv_len - 1) - kstart;
         const int lo_c = window > 0 ? p - window + 1 - kstart : -BN;
-        if (cap > 0.f) cap_pass(zr, cap_in);
-        if (need_mask) mask_pass(zr, lo_c, hi_c);
-        const float tmax = row_max(zr) * zmul;
+        float tmax, amax = 0.f;
+        bool poly = false;
+        if (!PAGED && cap > 0.f && !need_mask) {   // (the paged form has no registers to spare for it)
+          amax = row_absmax(zr);
+          poly = __all_sync(0xffffffffu, amax * cap_in <= kCapPolyRange);
+        }
+        if (poly) {
+          // every score of the warp's rows is small: the FMA-pipe tanh; the tile max is bounded by the cap of
+          // the row's largest |z| (an upper bound of its capped logits is all the online softmax needs: the
+          // exponents stay within 2 * cap * tanh(0.5) of it, far from underflow)
+          cap_poly_pass(zr, cap_in);
+          tmax = tanh_poly(amax * cap_in) * zmul;
+        } else {
+          if (cap > 0.f) cap_pass(zr, cap_in);
+          if (need_mask) mask_pass(zr, lo_c, hi_c);
+          tmax = row_max(zr) * zmul;
+        }
         const float m_new = fmaxf(m, tmax);
         const bool grow = m_new > m + kRescaleThreshold;
         float alpha = 1.f;
@@ -1013,6 +1064,17 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
 }  // namespace pf
 
+template <bool PAGED, bool CAP>
+static cudaError_t run_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                               const CUtensorMap& tmo, const pf::Params& prm, int grid, cudaStream_t stream) {
+  using namespace pf;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<PAGED, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<PAGED, CAP><<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   using namespace pf;
   if (a.n_seqs == 0 || a.max_q_len == 0 || a.n_tokens == 0) return cudaSuccess;
@@ -1056,21 +1118,19 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   prm.kbox = kbox;
   prm.scale = a.scale;
   prm.err = a.err;
-  const bool paged = a.block_table != nullptr;
-  cudaError_t e = cudaFuncSetAttribute(paged ? prefill_kernel<true> : prefill_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
   int dev = 0, n_sm = 0;
-  e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (shared memory and all 512 TMEM columns allow no second one)
   const int grid = static_cast<int>(std::min<long long>(n_items, n_sm));
-  if (paged)
-    prefill_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
-  else
-    prefill_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
-  return cudaGetLastError();
+  const bool paged = a.block_table != nullptr, capped = a.softcap > 0.f;
+  if (paged) {
+    return capped ? run_prefill<true, true>(tmq, tmk, tmv, tmo, prm, grid, stream)
+                  : run_prefill<true, false>(tmq, tmk, tmv, tmo, prm, grid, stream);
+  }
+  return capped ? run_prefill<false, true>(tmq, tmk, tmv, tmo, prm, grid, stream)
+                : run_prefill<false, false>(tmq, tmk, tmv, tmo, prm, grid, stream);
 }
 
 }  // namespace da

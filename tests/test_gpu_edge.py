@@ -404,3 +404,21 @@ def test_fused_rope_update_matches_two_calls(cuda, number):
     ab_.check_device_error()
     bits = lambda t: t.view(torch.int16)                # the pools hold NaN in spare blocks: compare bits
     assert torch.equal(pa.q_rot, pb.q_rot) and torch.equal(bits(kpa), bits(kpb)) and torch.equal(bits(vpa), bits(vpb))
+
+
+@pytest.mark.parametrize("hq,window", [(6, 0), (8, 256)])
+def test_softcap_both_tanh_forms(cuda, hq, window):
+    """Capped prefill tiles take one of two tanh forms per warp: a polynomial when every score of the warp's 32
+    rows is small against the cap, else the MUFU tanh. Query rows scaled by 1 and by 12 in alternate blocks of
+    32 send alternate warps down each form (cap 5: |scale q.k / cap| stays below 0.3 in the first and reaches
+    well past 0.5 in the second); both must match the oracle with its rotated q/k rounded to bf16 as stored."""
+    call = _prefill_call([300, 200], [0, 500], hq=hq, hkv=2, window=window, softcap=5.0, seed=70 + hq)
+    row = torch.cat([torch.arange(300), torch.arange(200)])
+    factor = torch.where((row // 32) % 2 == 0, 1.0, 12.0)
+    call.q = (call.q.float() * factor[:, None, None]).to(call.q.dtype)
+    st, _ = _run(call, cuda)
+    ref = ostep.run_layer_call(call, storage_rounding=True)
+    _close(st.out, ref["out"])
+    nocap = copy.copy(call)
+    nocap.softcap = 0.0
+    assert np.abs(ostep.run_layer_call(nocap, storage_rounding=True)["out"] - ref["out"]).max() > 0.1
