@@ -142,3 +142,44 @@ def test_phi4_gemma2_mixed_full(cuda):
         diffs += _prefill_samples(call, st, psnap, rng, 12)
         diffs += _decode_samples(call, st, dsnap, dec_idx)
     _check(diffs)
+
+
+def test_qwen3_8b_prefill_whole_sequence(cuda):
+    """One whole chunk of the Qwen3-8B-shaped prefill, every query and every head (2048 x 32 outputs),
+    element by element against the oracle on the chunk's own rotated keys (the chunks start at position 0)."""
+    from decoder_attention_gb300 import inputs
+    wl = inputs.make(2, scale="full", device=cuda)
+    call = wl.layers[0]
+    st = _run(wl)[0]
+    qs = call.q_start.cpu().numpy()
+    b = 2                                                 # a chunk in the middle of the batch
+    toks = np.arange(qs[b], qs[b + 1])
+    q_rot, k_rot = ostep.rotate_tokens(call, toks)
+    pos = np.arange(len(toks))
+    ref = A.causal_attention(q_rot, k_rot.transpose(1, 0, 2), _np64(call.v[toks]).transpose(1, 0, 2), pos, pos,
+                             call.window, call.softcap, 0.0)
+    got = st.out[int(qs[b]):int(qs[b + 1])].double().cpu().numpy()
+    _check([np.abs(got - ref)])
+
+
+def test_llama31_decode_every_sequence_one_kv_group(cuda):
+    """Every sequence of the Llama-3.1-8B-shaped decode (16 x 131072 keys, split-K over many chunks) for the
+    query heads of KV head 0, against the oracle on the cache rows copied before the step."""
+    from decoder_attention_gb300 import inputs
+    wl = inputs.make(4, scale="full", device=cuda)
+    call = wl.layers[0]
+    G = call.num_attention_heads // call.num_key_value_heads
+    pos = call.dec_pos.cpu().numpy()
+    rows = call.dec_rows.cpu().numpy()
+    snap = [(call.k_cache[int(r), 0:1, :int(p)].cpu(), call.v_cache[int(r), 0:1, :int(p)].cpu()) for r, p in zip(rows, pos)]
+    st = _run(wl)[0]
+    npf = call.n_prefill
+    diffs = []
+    for s in range(call.n_decode):
+        p = int(pos[s])
+        q_rot, k_rot = ostep.rotate_tokens(call, [npf + s])
+        K = np.concatenate([_np64(snap[s][0]), k_rot[0][0:1, None, :]], axis=1)
+        V = np.concatenate([_np64(snap[s][1]), _np64(call.v[npf + s])[0:1, None, :]], axis=1)
+        ref = A.causal_attention(q_rot[:, :G], K, V, [p], np.arange(p + 1), call.window, call.softcap, 0.0)[0]
+        diffs.append(np.abs(st.out[npf + s, :G].double().cpu().numpy() - ref))
+    _check(diffs)
