@@ -392,7 +392,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (ok) ok = mbar_wait_cluster(bar(B_SFULL + b), (t >> 1) & 1, prm.err);
       tc_fence_after();
       const uint32_t s_t = tmem + lane_addr + b * 128 + hh * 64;
-      // (1) per-head maximum over this CTA's 128 keys, then over the pair
+      // (1) per-head maximum over this CTA's 128 keys, sent to the other CTA (which needs it to decide alike)
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
         uint32_t v[32];
@@ -404,12 +404,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         wm[q4 * H + hh * 64 + jj * 32 + lane] = warp_colreduce32<true>(x, lane);
       }
       bar_sync_softmax();
-      bool grow = false;
+      float cm = -CUDART_INF_F;
+      bool need = false;   // this CTA's keys alone would move the running max
       if (head_owner) {
-        const float cm = fmaxf(fmaxf(wm[hd], wm[H + hd]), fmaxf(wm[2 * H + hd], wm[3 * H + hd]));
+        cm = fmaxf(fmaxf(wm[hd], wm[H + hd]), fmaxf(wm[2 * H + hd], wm[3 * H + hd]));
         st_cluster_f32(mx_peer + (b * H + hd) * 4, cm);
         __syncwarp();   // the warp's stores precede lane 0's release-arrive
         if (lane == 0) mbar_arrive_cluster(mxfull_peer + 8u * b);
+        need = cm != -CUDART_INF_F && cm * zmul > m_reg + kGrow;
+      }
+      const bool need_any = bar_or_softmax(need);
+      // (2) the previous tile's O^T MMAs are done: P^T may be overwritten (and O^T rescaled)
+      if (t >= 1 && ok) ok = mbar_wait(bar(B_ODONE), (t - 1) & 1, prm.err);
+      tc_fence_after();
+      // (3) probabilities of this warp's heads for this CTA's keys (P^T rows r * 128 + key) against the running
+      // max, and their sums over the keys; the exchanged maxima are read only after this (their trip between
+      // the CTAs overlaps it), and a tile on which the running max moves computes them again
+      const int prow = r * TK + kr;
+      float lt[2] = {0.f, 0.f};
+      auto p_pass = [&]() {
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          uint32_t v[32];
+          tmem_ld32(s_t + jj * 32, v);
+          tmem_wait_ld();
+          const float4* m4 = reinterpret_cast<const float4*>(m_s + hh * 64 + jj * 32);
+          float x[32];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 m = m4[e4];
+            const float mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              x[4 * e4 + k] = valid ? ex2(fmaf(__uint_as_float(v[4 * e4 + k]), zmul, -mm[k])) : 0.f;
+          }
+          const uint32_t dst = pt_dst + prow * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 pk;
+            pk.x = pack2(x[8 * i + 0], x[8 * i + 1]);
+            pk.y = pack2(x[8 * i + 2], x[8 * i + 3]);
+            pk.z = pack2(x[8 * i + 4], x[8 * i + 5]);
+            pk.w = pack2(x[8 * i + 6], x[8 * i + 7]);
+            const uint32_t a = dst + (((jj * 4 + i) ^ (prow & 7)) << 4);
+            if (remote)
+              st_cluster_v4(a, pk);
+            else
+              st_shared_v4(a, pk);
+          }
+          lt[jj] = warp_colreduce32<false>(x, lane);
+        }
+      };
+      if (!need_any) p_pass();   // optimistic: the running max holds unless the other CTA's keys move it
+      // (4) the pair's maxima: both CTAs take the same decision per head from the same numbers
+      bool grow = false;
+      if (head_owner) {
         if (ok) ok = mbar_wait_cluster(bar(B_MXFULL + b), (t >> 1) & 1, prm.err);
         const float gm = fmaxf(cm, mx[b * H + hd]);
         const float gz = gm == -CUDART_INF_F ? -CUDART_INF_F : gm * zmul;
@@ -423,9 +472,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         al_s[hd] = alpha;
       }
       const bool any_grow = bar_or_softmax(grow);
-      // (2) the previous tile's O^T MMAs are done: P^T may be overwritten and O^T rescaled
-      if (t >= 1 && ok) ok = mbar_wait(bar(B_ODONE), (t - 1) & 1, prm.err);
-      tc_fence_after();
       if (any_grow) {
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) l_acc[jj] *= al_s[hh * 64 + jj * 32 + lane];
@@ -443,40 +489,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           tmem_wait_st();
         }
+        p_pass();   // against the new running max (overwrites the optimistic pass, if any)
+      } else if (need_any) {
+        p_pass();   // cannot happen (a local need makes the pair's max grow); kept for safety
       }
-      // (3) probabilities of this warp's heads for this CTA's keys: P^T rows r * 128 + key
-      const int prow = r * TK + kr;
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        uint32_t v[32];
-        tmem_ld32(s_t + jj * 32, v);
-        tmem_wait_ld();
-        const float4* m4 = reinterpret_cast<const float4*>(m_s + hh * 64 + jj * 32);
-        float x[32];
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 m = m4[e4];
-          const float mm[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            x[4 * e4 + k] = valid ? ex2(fmaf(__uint_as_float(v[4 * e4 + k]), zmul, -mm[k])) : 0.f;
-        }
-        const uint32_t dst = pt_dst + prow * 128;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 pk;
-          pk.x = pack2(x[8 * i + 0], x[8 * i + 1]);
-          pk.y = pack2(x[8 * i + 2], x[8 * i + 3]);
-          pk.z = pack2(x[8 * i + 4], x[8 * i + 5]);
-          pk.w = pack2(x[8 * i + 6], x[8 * i + 7]);
-          const uint32_t a = dst + (((jj * 4 + i) ^ (prow & 7)) << 4);
-          if (remote)
-            st_cluster_v4(a, pk);
-          else
-            st_shared_v4(a, pk);
-        }
-        l_acc[jj] += warp_colreduce32<false>(x, lane);
-      }
+      for (int jj = 0; jj < 2; ++jj) l_acc[jj] += lt[jj];
       tc_fence_before();
       // this thread's P^T stores before the tensor core reads them (the other CTA's memory: cluster scope)
       if (remote)
