@@ -218,16 +218,24 @@ __device__ __forceinline__ float tanh_poly(float u) {
   const float v = u * u;
   return u * fmaf(fmaf(fmaf(kTanhP3, v, kTanhP2), v, kTanhP1), v, kTanhP0);
 }
-__device__ __forceinline__ void cap_poly_pass(uint32_t (&zr)[BN], float cap_in) {
-  const uint64_t k2 = f2_pack(cap_in, cap_in), p3 = f2_pack(kTanhP3, kTanhP3), p2 = f2_pack(kTanhP2, kTanhP2),
-                 p1 = f2_pack(kTanhP1, kTanhP1), p0 = f2_pack(kTanhP0, kTanhP0);
+// The same polynomial with the factor k = scale / cap folded into its coefficients, applied to the raw score z:
+// tanh(k z) = z * sum_i (P_i k^(2i+1)) (z^2)^i. cf holds the four folded coefficients (packed pairs).
+struct CapPoly {
+  uint64_t c0, c1, c2, c3;
+};
+__device__ __forceinline__ CapPoly cap_poly_coeffs(float k) {
+  const float k2 = k * k;
+  const float c0 = kTanhP0 * k, c1 = kTanhP1 * k * k2, c2 = kTanhP2 * k * k2 * k2, c3 = kTanhP3 * k * k2 * k2 * k2;
+  return CapPoly{f2_pack(c0, c0), f2_pack(c1, c1), f2_pack(c2, c2), f2_pack(c3, c3)};
+}
+__device__ __forceinline__ void cap_poly_pass(uint32_t (&zr)[BN], const CapPoly& cf) {
 #pragma unroll
   for (int c = 0; c < BN; c += 2) {
-    const uint64_t u = f2_mul(f2_pack(__uint_as_float(zr[c]), __uint_as_float(zr[c + 1])), k2);
-    const uint64_t v = f2_mul(u, u);
-    const uint64_t p = f2_fma(f2_fma(f2_fma(p3, v, p2), v, p1), v, p0);
+    const uint64_t z = f2_pack(__uint_as_float(zr[c]), __uint_as_float(zr[c + 1]));
+    const uint64_t v = f2_mul(z, z);
+    const uint64_t p = f2_fma(f2_fma(f2_fma(cf.c3, v, cf.c2), v, cf.c1), v, cf.c0);
     float a, b;
-    f2_unpack(f2_mul(p, u), a, b);
+    f2_unpack(f2_mul(p, z), a, b);
     zr[c] = __float_as_uint(a);
     zr[c + 1] = __float_as_uint(b);
   }
@@ -804,6 +812,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const uint32_t t_o = tmem + lane_addr + 256 + w * D;
     const float cap = CAP ? prm.softcap : 0.f;   // uncapped layers run an instantiation without the cap code
     const float cap_in = cap > 0.f ? prm.scale / cap : 0.f;
+    const CapPoly cap_cf = cap_poly_coeffs(cap_in);
     // z * zmul is the logit in log2 units: z the raw score, or for capped layers tanh(scale z / cap)
     const float zmul = cap > 0.f ? cap * kLog2e : prm.scale * kLog2e;
     int ns = 0, nod = 0;
@@ -954,7 +963,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           // every score of the warp's rows is small: the FMA-pipe tanh; the tile max is bounded by the cap of
           // the row's largest |z| (an upper bound of its capped logits is all the online softmax needs: the
           // exponents stay within 2 * cap * tanh(0.5) of it, far from underflow)
-          cap_poly_pass(zr, cap_in);
+          cap_poly_pass(zr, cap_cf);
           tmax = tanh_poly(amax * cap_in) * zmul;
         } else {
           if (cap > 0.f) cap_pass(zr, cap_in);
