@@ -194,6 +194,28 @@ def barrier(world):
         dist.barrier()
 
 
+def host_link_gbs(dev, nbytes=128 << 20, reps=5):
+    """Host <-> device bandwidth of plain pinned copies (128 MB, best of 5 each way, CUDA events): the bound on
+    `e2e`, whose steps move their inputs up and their outputs down through the same link."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dst.copy_(src, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out[name] = nbytes / (best / 1e3) / 1e9
+    del h, d
+    return out
+
+
 def headline(work, seconds):
     """(value, unit, tokens/s) of `work` done in `seconds`: TFLOP/s when the step has prefill, else GB/s."""
     if work["prefill_flops"] > 0:
@@ -500,7 +522,8 @@ def measure_native(args, workload, dev, world, rank, with_e2e=True):
         e2e = {"value": v * world, "unit": u, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms, "steps": n_e2e,
                "via": "AttentionStep.run (C ABI) with pinned host inputs/outputs; upload, kernels and download "
-                      "on three streams, two buffer sets, L2 not flushed (each step moves more than L2 holds)"}
+                      "on three streams, two buffer sets, L2 not flushed (each step moves more than L2 holds)",
+               "link_gbs": host_link_gbs(dev)}
         del sets, host_in, host_out
 
     rec = {
