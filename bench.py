@@ -592,6 +592,10 @@ def main_native(args):
     if args.workload == DEFAULT_WORKLOAD and not args.single and args.kv_block == 0 and args.scale == "full":
         for w in SIDE_WORKLOADS:
             side[w] = measure_native(args, w, dev, world, rank, with_e2e=not args.no_e2e)
+        # the two steps beside the attention step proper: the absorbed MLA decode and the attention block with
+        # its fused projections (their records keep their own keys; the MLA one carries its own CPU baseline)
+        side[MLA_WORKLOAD] = measure_mla(args, dev, world, rank)
+        side[BLOCK_WORKLOAD] = measure_block(args, dev, world, rank)
     cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     if rank == 0:
         line = {
@@ -604,7 +608,10 @@ def main_native(args):
         if side:
             for w, r in side.items():
                 r.pop("peaks", None)
-                r["cpu_baseline"] = cpu_baselines(w, all_cores=False) if cpu else None
+                for k in ("metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data"):
+                    r.pop(k, None)
+                if w in SIDE_WORKLOADS:
+                    r["cpu_baseline"] = cpu_baselines(w, all_cores=False) if cpu else None
             line["workloads"] = side
             line["gpu_launches"] += sum(r["gpu_launches"] for r in side.values())
             line["gpu_launches_note"] = "headline workload plus the side workloads' timed steps"
@@ -652,11 +659,24 @@ def mla_oracle_sample(call, seqs):
 def main_native_mla(args):
     import torch
 
-    from decoder_attention_gb300 import _abi, inputs, step as S
-
     rank, world, local = dist_init(args)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    rec = measure_mla(args, dev, world, rank)
+    if rank == 0:
+        print(json.dumps(rec))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_mla(args, dev, world, rank):
+    """The DeepSeek-V3-shaped MLA decode step through the C ABI on `dev`; returns its record."""
+    import torch
+
+    from decoder_attention_gb300 import _abi, inputs, step as S
+
     call = inputs.deepseek_v3_mla_decode("full", device=dev)
     pool = None
     if args.kv_block > 0:
@@ -666,7 +686,7 @@ def main_native_mla(args):
     work = mla_work(call)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     time.sleep(0.3)
     clocks.mark_start()
     for _ in range(max(args.warmup, 3)):
@@ -734,24 +754,23 @@ def main_native_mla(args):
         v, sec, desc = mla_oracle_sample(call, [0, 1])
         cpu_base = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc, "seconds": sec,
                     "host_cores": os.cpu_count()}
-    if rank == 0:
-        print(json.dumps({
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": MLA_WORKLOAD, "description": call.meta["description"],
-                       "l2": "flushed (256 MB write) before every timed step, outside the step's events",
-                       "kv": (f"paged pool, {args.kv_block}-position blocks in shuffled order" if pool
-                              else "contiguous latent rows"),
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "tokens_per_s": work["tokens"] * world / (ms / 1e3),
-            "breakdown_ms": {"rope_and_cache_update": ms - dec_ms, "decode": dec_ms},
-            "work": work, "roofline": roof, "e2e": e2e, "gpu_launches": st.kernel_launches() * args.steps,
-            "clocks": clock_info, "cpu_baseline": cpu_base, "peaks": dict(peaks, kind=peak_kind)}))
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+    rec = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": MLA_WORKLOAD, "description": call.meta["description"],
+                   "l2": "flushed (256 MB write) before every timed step, outside the step's events",
+                   "kv": (f"paged pool, {args.kv_block}-position blocks in shuffled order" if pool
+                          else "contiguous latent rows"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": work["tokens"] * world / (ms / 1e3),
+        "breakdown_ms": {"rope_and_cache_update": ms - dec_ms, "decode": dec_ms},
+        "work": work, "roofline": roof, "e2e": e2e, "gpu_launches": st.kernel_launches() * args.steps,
+        "clocks": clock_info, "cpu_baseline": cpu_base, "peaks": dict(peaks, kind=peak_kind)}
+    del st, call, pool, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
 
 def main_reference_mla(args):
@@ -785,15 +804,28 @@ def main_native_block(args):
     """The Qwen3-8B-shaped attention block: the fused q/k/v projection (norm, RoPE and cache write in the GEMM
     epilogue), the prefill attention and o_proj, all through the C ABI; the unfused form (a cuBLAS GEMM for
     q/k/v, then da_kv_cache_update; cuBLAS for o_proj) is timed beside it for comparison."""
+    import torch
+
+    rank, world, local = dist_init(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    rec = measure_block(args, dev, world, rank)
+    if rank == 0:
+        print(json.dumps(rec))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_block(args, dev, world, rank):
+    """The attention-block record on `dev` (see main_native_block)."""
     import math
 
     import torch
 
     from decoder_attention_gb300 import _abi, inputs, step as S, work as W
 
-    rank, world, local = dist_init(args)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     call = inputs.make(2, scale="full", device=dev).layers[0]          # 4 x 2048 tokens, Hq 32, Hkv 8
     n, hq, hkv, hidden = call.n_tokens, call.num_attention_heads, call.num_key_value_heads, 4096
     g = torch.Generator(device=dev).manual_seed(3002)
@@ -823,7 +855,7 @@ def main_native_block(args):
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     time.sleep(0.3)
     clocks.mark_start()
 
@@ -854,8 +886,7 @@ def main_native_block(args):
     total = proj_flops + attn_flops + o_flops
     peaks, peak_kind = load_peaks()
     achieved = proj_flops / (ms_parts[0] / 1e3) / 1e12
-    if rank == 0:
-        print(json.dumps({
+    rec = {
             "metric": METRIC, "value": total / (ms / 1e3) / 1e12 * world, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init projection weights)",
@@ -873,11 +904,11 @@ def main_native_block(args):
             "unfused_comparison_ms": {"rope_tables_cublas_qkv_and_cache_update": ms_cmp[0], "prefill": ms_cmp[1],
                                       "cublas_o_proj": ms_cmp[2]},
             "e2e": None, "gpu_launches": 5 * args.steps, "clocks": clock_info, "cpu_baseline": None,
-            "peaks": dict(peaks, kind=peak_kind)}))
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+            "peaks": dict(peaks, kind=peak_kind)}
+    del st, call, x, w_qkv, w_o, y, qkv, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
 
 def main(argv=None):

@@ -422,3 +422,44 @@ def test_softcap_both_tanh_forms(cuda, hq, window):
     nocap = copy.copy(call)
     nocap.softcap = 0.0
     assert np.abs(ostep.run_layer_call(nocap, storage_rounding=True)["out"] - ref["out"]).max() > 0.1
+
+
+@pytest.mark.parametrize("window", [0, 256])
+def test_cached_decode_equals_recompute(cuda, window):
+    """The [MoE/decoding guide] sanity check that cached decoding equals recomputing the whole sequence: token
+    T decoded against the cache a prefill of tokens 0..T-1 wrote gives row T of a prefill of tokens 0..T, both
+    through the C ABI (the decode and the prefill kernels), and both match the oracle."""
+    from decoder_attention_gb300 import inputs, step
+    T, hq, hkv = 700, 8, 2
+    full = _prefill_call([T + 1], [0], hq=hq, hkv=hkv, window=window, seed=80)
+    ref = ostep.run_layer_call(full)["out"]
+    st_full = step.AttentionStep(full.to(cuda))
+    st_full.run()
+
+    def sub(idx, prefill):
+        i = torch.as_tensor(idx)
+        n = len(idx)
+        qs, tr, tp, tl = inputs._prefill_meta([n], [0], [0]) if prefill else (None, [0], [idx[0]], [idx[0] + 1])
+        return inputs.LayerCall(
+            head_dim=128, num_attention_heads=hq, num_key_value_heads=hkv, partial_rotary_factor=1.0,
+            rope_theta=full.rope_theta, rope_scaling=None, max_position_embeddings=full.max_position_embeddings,
+            dtype=full.dtype, window=window, softcap=0.0, q=full.q[i], k=full.k[i], v=full.v[i],
+            tok_rows=inputs._i32(tr), tok_pos=inputs._i32(tp), tok_seq_len=inputs._i32(tl),
+            n_prefill=n if prefill else 0, q_start=inputs._i32(qs if prefill else [0]),
+            pf_rows=inputs._i32([0] if prefill else []), pf_first_pos=inputs._i32([0] if prefill else []),
+            max_q_len=n if prefill else 0, dec_rows=inputs._i32([] if prefill else [0]),
+            dec_pos=inputs._i32([] if prefill else [idx[0]]), k_cache=full.k_cache, v_cache=full.v_cache)
+
+    pre = sub(list(range(T)), True).to(cuda)
+    dec = sub([T], False)
+    dec.k_cache, dec.v_cache = pre.k_cache, pre.v_cache          # the cache the prefill writes
+    dec = step.AttentionStep(dec.to(cuda))
+    step.AttentionStep(pre).run()
+    dec.run()
+    torch.cuda.synchronize()
+    _abi().check_device_error()
+    got_dec = dec.out[0].double().cpu().numpy()
+    got_full = st_full.out[T].double().cpu().numpy()
+    _close(dec.out[0:1], ref[T:T + 1])
+    _close(st_full.out[T:T + 1], ref[T:T + 1])
+    assert np.abs(got_dec - got_full).max() <= BF16_MAX
