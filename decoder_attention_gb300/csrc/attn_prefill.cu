@@ -443,15 +443,40 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         int* cost = reinterpret_cast<int*>(smem + OFF_E);
         int* bin = cost + kMaxPairs;   // bin b: pairs of cost cmax - b, then the first rank they take
         int cmax = -1;
-        for (int p = lane; p < n_pairs; p += 32) {
+        // Each chunk's start, length, first position and row, read once: with at most 32 chunks lane s holds
+        // chunk s's (one round of independent loads, then shuffles), else every lane reads its pairs' own. The
+        // table is the first thing every CTA waits for, so its loads are not left to run one after another.
+        const bool few = prm.n_seqs <= 32;
+        int m_q0 = 0, m_q1 = 0, m_fp = 0, m_row = 0;
+        if (few && lane < prm.n_seqs) {
+          m_q0 = prm.q_start[lane];
+          m_q1 = prm.q_start[lane + 1];
+          m_fp = prm.first_pos[lane];
+          m_row = prm.rows[lane];
+        }
+        for (int p0 = 0; p0 < n_pairs; p0 += 32) {   // uniform trip count: the shuffles below take every lane
+          const int p = p0 + lane;
           const int y = p / prm.n_seqs, s = p - y * prm.n_seqs;
+          int q_a, q_b, fp, row;
+          if (few) {
+            const int src = p < n_pairs ? s : 0;
+            q_a = __shfl_sync(0xffffffffu, m_q0, src);
+            q_b = __shfl_sync(0xffffffffu, m_q1, src);
+            fp = __shfl_sync(0xffffffffu, m_fp, src);
+            row = __shfl_sync(0xffffffffu, m_row, src);
+          } else if (p < n_pairs) {
+            q_a = prm.q_start[s];
+            q_b = prm.q_start[s + 1];
+            fp = prm.first_pos[s];
+            row = prm.rows[s];
+          }
+          if (p >= n_pairs) continue;
           Item it;
-          it.n_b = prm.q_start[s + 1] - prm.q_start[s];
+          it.n_b = q_b - q_a;
           it.q0 = (prm.n_qt - 1 - y) * (hpair ? BM : NQT * BM);
-          it.fp = prm.first_pos[s];
+          it.fp = fp;
           int c = -1;
           if (it.q0 < it.n_b) {
-            const int row = prm.rows[s];
             const bool bad = row < 0 || row >= prm.num_rows || it.fp < 0 || it.fp + it.n_b > prm.max_len;
             c = bad ? 0 : tiles_of(it, window, hpair).n;
           }
