@@ -299,6 +299,7 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 // copies (V never passes through registers) and refills the stage once the stores have read it.
 constexpr int KB_STAGES = 4;
 constexpr int KB_THREADS = 288;           // 8 computing warps + 1 copy warp
+constexpr int KB_META = 64;               // tokens whose row / position a fused block reads ahead
 struct KbLayout {                         // byte offsets within a stage
   int k, v, cos, sin, hdr, bytes;         // q at 0; hdr: the token's cache slot (8 bytes, -1: none)
 };
@@ -326,6 +327,7 @@ __global__ void __launch_bounds__(KB_THREADS, FUSED ? 4 : 3) kv_update_bulk_kern
   constexpr int HPW = 32 / TPV;
   extern __shared__ __align__(128) uint8_t kb_smem[];
   __shared__ uint64_t bars[2 * KB_STAGES];   // full[s] (copy + bytes), done[s] (256 computing threads)
+  __shared__ int meta_row[FUSED ? KB_META : 1], meta_pos[FUSED ? KB_META : 1], meta_len[FUSED ? KB_META : 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int half = a.rot >> 1;
   const int heads = a.hq + a.hkv;
@@ -416,11 +418,31 @@ __global__ void __launch_bounds__(KB_THREADS, FUSED ? 4 : 3) kv_update_bulk_kern
       const int t = blockIdx.x + kk * gridDim.x;
       const int s = kk % KB_STAGES;
       uint8_t* st = kb_smem + s * L.bytes;
+      if (FUSED && kk % KB_META == 0) {
+        // the next KB_META tokens' row, position (and length) into shared memory, one token per thread: their
+        // loads overlap, instead of one dependent global load at the head of every token (the table fill and
+        // the barrier after it would wait for each). Entries are rewritten only here, after every computing
+        // thread has passed the previous token's barrier, and each token's entries are read before it.
+        const int i = warp * 32 + lane;
+        if (i < KB_META && kk + i < n_mine) {
+          const int ti = blockIdx.x + (kk + i) * gridDim.x;
+          meta_row[i] = a.rows[ti];
+          meta_pos[i] = a.positions[ti];
+          meta_len[i] = f.use_seq_len ? a.seq_len[ti] : 0;
+        }
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+      }
       int row = 0, pos = 0, len = 0;
-      if (warp == 0 && lane == 0) row = a.rows[t];
       const bool tabler = FUSED && fi < half;   // forms one of this token's cos/sin pairs
-      if (tabler || (warp == 0 && lane == 0)) pos = a.positions[t];
-      if (tabler && f.use_seq_len) len = a.seq_len[t];
+      if (FUSED) {
+        const int mi = kk % KB_META;
+        if (warp == 0 && lane == 0) row = meta_row[mi];
+        if (tabler || (warp == 0 && lane == 0)) pos = meta_pos[mi];
+        if (tabler) len = meta_len[mi];
+      } else {
+        if (warp == 0 && lane == 0) row = a.rows[t];
+        if (warp == 0 && lane == 0) pos = a.positions[t];
+      }
       if (FUSED) {
         // this token's cos/sin into the stage, one rotary pair per computing thread (the tables' arithmetic);
         // that part of the stage is not copied in, and the barrier below keeps the warps within one token, so

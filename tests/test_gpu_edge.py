@@ -373,6 +373,27 @@ def test_fused_rope_update_head_counts(cuda, hq, hkv, rot):
     assert torch.equal(a.k_cache, b.k_cache) and torch.equal(a.v_cache, b.v_cache)
 
 
+def test_fused_rope_update_many_tokens_per_block(cuda):
+    """A fused-update block reads its tokens' rows, positions and lengths 64 tokens ahead into shared memory and
+    rereads the next 64 once it has passed them. 47000 tokens over 4 x 152 resident blocks give every block more
+    than 64, so each one refills that table; three chunks put LongRoPE's seq_len switch on both sides (30000 and
+    15100 above the original 4096, 2000 below). Bits must equal the table build followed by the plain update."""
+    from decoder_attention_gb300 import _abi as ab_, inputs, step
+    call = _prefill_call([30000, 15000, 2000], [0, 100, 0], hq=2, hkv=1, rot=96, seed=91,
+                         rope_scaling=inputs.phi4_longrope_scaling(48), max_pos=131072)
+    props = torch.cuda.get_device_properties(cuda)
+    assert call.n_tokens > 64 * 4 * props.multi_processor_count
+    a, b = call.to(cuda), call.to(cuda)
+    sa, sb = step.AttentionStep(a, fused_rope=True), step.AttentionStep(b, fused_rope=False)
+    assert ab_.kv_rope_fused_supported(sa.L)
+    sa.update()
+    sb.update()
+    torch.cuda.synchronize()
+    ab_.check_device_error()
+    assert torch.equal(sa.q_rot, sb.q_rot)
+    assert torch.equal(a.k_cache, b.k_cache) and torch.equal(a.v_cache, b.v_cache)
+
+
 @pytest.mark.parametrize("number", [2, 3, 4, 5])
 def test_fused_rope_update_matches_two_calls(cuda, number):
     """da_kv_cache_update_rope (cos/sin formed in the kernel) writes the same bits as da_rope_tables_build
