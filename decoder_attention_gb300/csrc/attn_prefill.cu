@@ -855,15 +855,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       if (!__all_sync(0xffffffffu, mbar_wait(B(B_OD + w), nod & 1, prm.err))) return false;
       ++nod;
       tc_fence_after();
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        uint32_t ov[32];
-        tmem_ld32(t_o + j * 32, ov);
+      {
+        uint32_t ov[D];   // the whole O row in one tensor-memory load and one wait
+        tmem_ld128(t_o, ov);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pw[j * 16 + c] =
-              pack_bf16(__uint_as_float(ov[2 * c]) * pend_inv_l, __uint_as_float(ov[2 * c + 1]) * pend_inv_l);
+        for (int c = 0; c < D / 2; ++c)
+          pw[c] = pack_bf16(__uint_as_float(ov[2 * c]) * pend_inv_l, __uint_as_float(ov[2 * c + 1]) * pend_inv_l);
       }
       tc_fence_before();   // O_w has been read
       return true;
