@@ -7,7 +7,10 @@ One step = one pass of the whole step over one batch of synthetic input: da_rope
 da_kv_cache_update, then da_attn_prefill for the prefill chunks and da_attn_decode for the decode tokens,
 for every layer of the workload. Default workload: the Qwen3-8B-shaped prefill (4 x 2048 tokens, Hq 32,
 Hkv 8, d 128, q/k RMSNorm). Inputs are resident in HBM when timing starts; L2 (129 MB) is flushed by a
-256 MB write before every timed step, outside the timed events. Prints one JSON line (rank 0).
+256 MB write before every timed step, outside the timed events. Each timed step has events only around
+it (its kernels may overlap one another's launch through programmatic dependent launch); the per-stage
+breakdown and the kernel roofline come from a second pass with an event after every stage. Prints one JSON
+line (rank 0).
 
 Multi-GPU: the step does not exchange data between GPUs; N ranks run N independent replicas of the
 workload (weak scaling), and the time is the maximum over ranks.
@@ -380,11 +383,27 @@ def measure_native(args, workload, dev, world, rank, with_e2e=True):
     _abi.check_device_error()
 
     # ------------------------------------------------------------------ timed region
+    # Whole steps with events only around each step: the kernels of a step follow one another with no event
+    # in between, so a kernel may start (programmatic dependent launch) while the one before it finishes.
     n_layers = len(steps)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(1 + 3 * n_layers)] for _ in range(args.steps)]
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        sev[i][0].record(stream)
+        run_step()
+        sev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    _abi.check_device_error()
+    step_ms = [a.elapsed_time(b) for a, b in sev]
+
+    # Stage breakdown: a second pass of the same steps with an event after every stage (each event closes
+    # the stage before it, so these stages start only when the previous one has ended).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(1 + 3 * n_layers)] for _ in range(args.steps)]
     for i in range(args.steps):
         flush.zero_()
         e = ev[i]
@@ -400,8 +419,6 @@ def measure_native(args, workload, dev, world, rank, with_e2e=True):
                 st.decode()
                 e[3 + 3 * li].record(stream)
     torch.cuda.synchronize()
-    barrier(world)
-    wall = time.perf_counter() - wall0
     clocks.mark_end()
     _abi.check_device_error()
 
@@ -413,7 +430,6 @@ def measure_native(args, workload, dev, world, rank, with_e2e=True):
     def interval(x, y):
         return 0.0 if x is y else x.elapsed_time(y)
 
-    step_ms = [e[0].elapsed_time(marks(e, n_layers - 1)[2]) for e in ev]
     pf_ms = [sum(interval(*marks(e, li)[:2]) for li in range(n_layers)) for e in ev]
     dec_ms = [sum(interval(*marks(e, li)[1:]) for li in range(n_layers)) for e in ev]
     pre_ms = [sum((e[0] if li == 0 else marks(e, li - 1)[2]).elapsed_time(marks(e, li)[0]) for li in range(n_layers))
@@ -528,7 +544,8 @@ def measure_native(args, workload, dev, world, rank, with_e2e=True):
 
     rec = {
         "value": value_1 * world, "unit": unit, "ms_per_step": ms_all,
-        "ms_per_step_mean": statistics.mean(step_ms), "timing": f"median of {args.steps} timed steps",
+        "ms_per_step_mean": statistics.mean(step_ms), "timing": (f"median of {args.steps} timed steps (events around each step only); breakdown_ms and "
+                   f"roofline from a second pass of {args.steps} steps with an event after every stage"),
         "dtype": "bf16" if wl.layers[0].dtype == torch.bfloat16 else "fp32",
         "config": {"workload": workload, "number": num, "scale": args.scale, "description": wl.description,
                    "l2": "flushed (256 MB write) before every timed step, outside the step's events",
@@ -694,9 +711,18 @@ def measure_mla(args, dev, world, rank):
         st.run()
     torch.cuda.synchronize()
     _abi.check_device_error()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # whole steps (events around each step only), then a second pass with an event between the two stages
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        sev[i][0].record(stream)
+        st.run()
+        sev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
@@ -705,10 +731,9 @@ def measure_mla(args, dev, world, rank):
         st.decode()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
-    barrier(world)
     clocks.mark_end()
     _abi.check_device_error()
-    ms = reduce_max(statistics.median(e[0].elapsed_time(e[2]) for e in ev), world)
+    ms = reduce_max(statistics.median(a.elapsed_time(b) for a, b in sev), world)
     dec_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     clock_info = clocks.stop()
     value = work["decode_bytes"] / (ms / 1e3) / 1e9 * world
@@ -870,19 +895,31 @@ def measure_block(args, dev, world, rank):
         torch.cuda.synchronize()
         return [statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(len(fn_parts))]
 
+    def timed_whole(fn_parts, steps):   # events around each step only (kernels may overlap launches)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            for fn in fn_parts:
+                fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
     parts = [fused, st.prefill, lambda: _abi.linear(st.out.view(n, hq * 128), w_o, None, n, hidden, hq * 128, y)]
     timed(parts, max(args.warmup, 3))
     _abi.check_device_error()
     barrier(world)
-    ms_parts = timed(parts, args.steps)
+    ms_whole = timed_whole(parts, args.steps)
     barrier(world)
+    ms_parts = timed(parts, args.steps)
     clocks.mark_end()
     _abi.check_device_error()
     cmp_parts = [unfused, st.prefill, lambda: torch.matmul(st.out.view(n, hq * 128), w_o.t(), out=y)]
     timed(cmp_parts, 3)
     ms_cmp = timed(cmp_parts, max(3, min(args.steps, 20)))
     clock_info = clocks.stop()
-    ms = reduce_max(sum(ms_parts), world)
+    ms = reduce_max(ms_whole, world)
     total = proj_flops + attn_flops + o_flops
     peaks, peak_kind = load_peaks()
     achieved = proj_flops / (ms_parts[0] / 1e3) / 1e12

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const __grid_constant__
 
   const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();   // the stream's previous kernel (the cache update) has finished writing the caches
   const int p = prm.positions[s];
   const int row = prm.rows[s];
   if (row < 0 || row >= prm.num_rows || p < 0 || p >= prm.max_len) {
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(const __grid_constant__
 __global__ void __launch_bounds__(D) merge_kernel(const Params prm) {
   const int h = blockIdx.x, s = blockIdx.y, dd = threadIdx.x;
   __nv_bfloat16* out = prm.out + (static_cast<long long>(s) * prm.hq + h) * D;
+  pdl_wait();   // the decode kernel's partial results are complete
   const int p = prm.positions[s];
   const int row = prm.rows[s];
   if (row < 0 || row >= prm.num_rows || p < 0 || p >= prm.max_len) {
@@ -418,11 +420,9 @@ cudaError_t launch_decode_bf16(const AttnArgs& a, const DecodePlan& plan, void* 
   cudaError_t ea = cudaFuncSetAttribute(decode_kernel<NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (ea != cudaSuccess) return ea;
   dim3 grid(plan.n_splits, a.hkv, a.n_seqs);
-  decode_kernel<NST><<<grid, THREADS, smem, stream>>>(tmk, tmv, prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(decode_kernel<NST>, grid, dim3(THREADS), smem, stream, tmk, tmv, prm);
   if (e != cudaSuccess) return e;
-  merge_kernel<<<dim3(a.hq, a.n_seqs), D, 0, stream>>>(prm);
-  return cudaGetLastError();
+  return launch_dependent(merge_kernel, dim3(a.hq, a.n_seqs), dim3(D), 0, stream, prm);
 }
 
 }  // namespace da

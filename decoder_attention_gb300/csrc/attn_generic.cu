@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
   const int i = blockIdx.x;
   __shared__ float sm_m[4], sm_l[4];
   __shared__ float sm_o[4][D];
+  pdl_wait();   // inputs written by the stream's previous kernel are visible
 
   int t, p, kv_len;
   if (a.q_start) {
@@ -149,8 +150,7 @@ __global__ void __launch_bounds__(128) attn_generic_kernel(const AttnArgs a) {
 template <typename T, int D>
 static cudaError_t launch_generic_t(const AttnArgs& a, cudaStream_t stream) {
   dim3 grid(a.max_q_len, a.hq, a.n_seqs);
-  attn_generic_kernel<T, D><<<grid, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(attn_generic_kernel<T, D>, grid, dim3(128), 0, stream, a);
 }
 
 cudaError_t launch_attn_generic(const AttnArgs& a, bool bf16, cudaStream_t stream) {

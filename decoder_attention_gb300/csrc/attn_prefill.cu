@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const volatile int* vabort = &abort_flag;
+  pdl_wait();   // the stream's previous kernel (the cache update) has finished writing q and the caches
 
   // Cache row of key `key` of an item's plane: contiguous caches number rows plane + key; paged pools look
   // the key's block up (a K/V box of kbox rows never straddles two blocks); -1 when the block is missing.
@@ -1103,8 +1104,8 @@ static cudaError_t run_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, c
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<PAGED, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  prefill_kernel<PAGED, CAP><<<grid, THREADS, SMEM_BYTES, stream>>>(tmq, tmk, tmv, tmo, prm);
-  return cudaGetLastError();
+  return launch_dependent(prefill_kernel<PAGED, CAP>, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, tmq, tmk, tmv,
+                          tmo, prm);
 }
 
 cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {

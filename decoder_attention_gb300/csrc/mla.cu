@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(256) mla_update_kernel(const UpdateParams a) {
   const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= static_cast<long long>(a.n) * items) return;
+  pdl_wait();   // inputs written by the stream's previous kernel are visible
   const int t = static_cast<int>(w / items), item = static_cast<int>(w - static_cast<long long>(t) * items);
   const float c = a.cos[static_cast<long long>(t) * (ROPE / 2) + lane];
   const float s = a.sin[static_cast<long long>(t) * (ROPE / 2) + lane];
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_decode_kernel(const __grid_con
 
   const int c = blockIdx.x, hg = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();   // the stream's previous kernel (the cache update) has finished writing the cache
   const int p = prm.positions[s];
   const int row = prm.rows[s];
   if (row < 0 || row >= prm.num_rows || p < 0 || p >= prm.max_len) {
@@ -400,6 +402,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_decode_kernel(const __grid_con
 __global__ void __launch_bounds__(128) mla_merge_kernel(const Params prm) {
   const int h = blockIdx.x, s = blockIdx.y;
   __nv_bfloat16* out = prm.out + (static_cast<long long>(s) * prm.hq + h) * RANK;
+  pdl_wait();   // the decode kernel's partial results are complete
   const int p = prm.positions[s];
   const int row = prm.rows[s];
   if (row < 0 || row >= prm.num_rows || p < 0 || p >= prm.max_len) {
@@ -480,8 +483,7 @@ cudaError_t launch_mla_update(const MlaUpdateArgs& a, cudaStream_t stream) {
   const long long warps = static_cast<long long>(a.n) * (1 + (a.q ? a.hq : 0));
   const long long blocks = (warps * 32 + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  mla_update_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(u);
-  return cudaGetLastError();
+  return launch_dependent(mla_update_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, u);
 }
 
 cudaError_t launch_mla_decode(const MlaArgs& a, const MlaPlan& plan, void* workspace, cudaStream_t stream) {
@@ -524,12 +526,10 @@ cudaError_t launch_mla_decode(const MlaArgs& a, const MlaPlan& plan, void* works
     e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   // per device
     if (e != cudaSuccess) return e;
     dim3 grid(plan.n_splits, (a.hq + HPC - 1) / HPC, a.n_seqs);
-    mla_decode_kernel<<<grid, THREADS, smem, stream>>>(tmc, prm);
-    e = cudaGetLastError();
+    e = launch_dependent(mla_decode_kernel, grid, dim3(THREADS), smem, stream, tmc, prm);
   }
   if (e != cudaSuccess) return e;
-  mla_merge_kernel<<<dim3(a.hq, a.n_seqs), 128, 0, stream>>>(prm);
-  return cudaGetLastError();
+  return launch_dependent(mla_merge_kernel, dim3(a.hq, a.n_seqs), dim3(128), 0, stream, prm);
 }
 
 }  // namespace da

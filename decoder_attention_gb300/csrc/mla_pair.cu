@@ -138,6 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int r = static_cast<int>(cluster_rank());
   const int c = blockIdx.x >> 1, s = blockIdx.z;
 
+  pdl_wait();   // the stream's previous kernel (the cache update) has finished writing the cache
   // both CTAs of the pair see the same sequence and chunk, so they leave together
   const int p = prm.positions[s];
   const int row = prm.rows[s];
@@ -590,8 +591,8 @@ cudaError_t launch_mla_pair_decode(const MlaArgs& a, const MlaPlan& plan, float*
   // per device and cheap: set on every launch
   cudaError_t ea = cudaFuncSetAttribute(mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (ea != cudaSuccess) return ea;
-  mla_pair_kernel<<<dim3(2 * plan.n_splits, 1, a.n_seqs), THREADS, SMEM_BYTES, stream>>>(tmq, tmc, prm);
-  return cudaGetLastError();
+  return launch_dependent(mla_pair_kernel, dim3(2 * plan.n_splits, 1, a.n_seqs), dim3(THREADS), SMEM_BYTES, stream, tmq,
+                          tmc, prm);
 }
 
 }  // namespace da

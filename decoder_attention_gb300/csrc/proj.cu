@@ -107,6 +107,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int kb_n = prm.k / BK;
+  pdl_wait();   // inputs written by the stream's previous kernel are visible
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
@@ -319,6 +320,13 @@ cudaError_t launch_proj(const ProjArgs& a, cudaStream_t stream) {
   if (resident < 1) return cudaErrorInvalidConfiguration;
   const long long work = static_cast<long long>(((a.m + BM - 1) / BM + 1) / 2) * (a.n / BN);   // tile pairs
   cfg.gridDim = dim3(CLUSTER * static_cast<unsigned>(std::min<long long>(work, resident)));
+  // programmatic dependent launch: the kernel may start while the stream's previous kernel finishes (it waits
+  // in pdl_wait before touching memory)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return qkv ? cudaLaunchKernelEx(&cfg, gemm_kernel<EPI_QKV>, tma, tmb, p)
              : cudaLaunchKernelEx(&cfg, gemm_kernel<EPI_PLAIN>, tma, tmb, p);
 }

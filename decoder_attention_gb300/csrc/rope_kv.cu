@@ -55,6 +55,7 @@ __global__ void rope_tables_kernel(const __grid_constant__ RopeTurns f, const in
   if (idx >= static_cast<long long>(n) * groups) return;
   const int t = static_cast<int>(idx / groups);
   const int i0 = static_cast<int>(idx - static_cast<long long>(t) * groups) * kRopePairs;
+  pdl_wait();   // inputs written by the stream's previous kernel are visible
   const int p = positions[t];
   const bool use_long = f.use_seq_len && seq_len[t] > f.switch_len;
   float c[kRopePairs], s[kRopePairs];
@@ -96,8 +97,8 @@ cudaError_t launch_rope_tables(const RopeFreqs& f, const int32_t* positions, con
   const RopeTurns turns = rope_turns(f);
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
-  rope_tables_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(turns, positions, seq_len, n, cos, sin, err);
-  return cudaGetLastError();
+  return launch_dependent(rope_tables_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, turns,
+                          positions, seq_len, n, cos, sin, err);
 }
 
 // ---------------------------------------------------------------------------------------------- cache update
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(256) kv_update_kernel(const KvUpdateArgs a) {
   const int t = static_cast<int>(gw / a.wpt);
   const int part = static_cast<int>(gw - static_cast<long long>(t) * a.wpt);
   if (t >= a.n) return;                   // whole warps leave together
+  pdl_wait();                             // inputs written by the stream's previous kernel are visible
   const int sub = lane % TPV;
   const int slot = lane / TPV;
   const int e0 = sub * VEC;
@@ -343,6 +345,7 @@ __global__ void __launch_bounds__(KB_THREADS, FUSED ? 4 : 3) kv_update_bulk_kern
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();   // inputs written by the stream's previous kernel are visible
   const int es = static_cast<int>(sizeof(T));
   const uint32_t in_bytes = static_cast<uint32_t>(FUSED ? L.cos : L.hdr);   // q, k, v (, cos, sin)
 
@@ -635,8 +638,7 @@ static cudaError_t launch_bulk(const KvUpdateArgs& a, const KbLayout& L, const R
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(a.n, n_sm * std::max(per_sm, 1)));
-  kv_update_bulk_kernel<T, D, FUSED><<<grid, KB_THREADS, smem, stream>>>(a, L, f);
-  return cudaGetLastError();
+  return launch_dependent(kv_update_bulk_kernel<T, D, FUSED>, dim3(grid), dim3(KB_THREADS), smem, stream, a, L, f);
 }
 
 template <typename T, int D>
@@ -659,10 +661,8 @@ static cudaError_t launch_kv_t(const KvUpdateArgs& a, cudaStream_t stream) {
   const long long warps = static_cast<long long>(a.n) * b.wpt;
   const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);   // 8 warps per block
   if ((a.rot / 2) % Vec16<T>::N == 0)
-    kv_update_kernel<T, D, true><<<blocks, 256, 0, stream>>>(b);
-  else
-    kv_update_kernel<T, D, false><<<blocks, 256, 0, stream>>>(b);
-  return cudaGetLastError();
+    return launch_dependent(kv_update_kernel<T, D, true>, dim3(blocks), dim3(256), 0, stream, b);
+  return launch_dependent(kv_update_kernel<T, D, false>, dim3(blocks), dim3(256), 0, stream, b);
 }
 
 cudaError_t launch_kv_update(const KvUpdateArgs& a, bool bf16, cudaStream_t stream) {
