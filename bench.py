@@ -565,6 +565,14 @@ def measure_native(args, workload, dev, world, rank, with_e2e=True):
     }
     if len(parts) > 1:
         rec["roofline_parts"] = parts
+        # a mixed batch's two parts share the GPU within the step (da_attn_mixed): each part's work over the whole
+        # step's time, as a fraction of its own peak; the sum is how much of the two roofs the step uses at once
+        pf_t = work["prefill_flops"] / (ms_all / 1e3) / 1e12
+        dec_g = work["decode_bytes"] / (ms_all / 1e3) / 1e9
+        rec["parts_over_step"] = {
+            "prefill_tflops": pf_t, "prefill_frac": pf_t / peaks["bf16_tflops"],
+            "decode_gbs": dec_g, "decode_frac": dec_g / peaks["hbm_gbs"],
+            "sum_of_fracs": pf_t / peaks["bf16_tflops"] + dec_g / peaks["hbm_gbs"]}
     del steps, pools, wl, flush
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

@@ -80,6 +80,11 @@ def _load():
         "da_attn_prefill": (I, [ctypes.POINTER(DaLayer), P, I, P, P, I, I, I, P, P, P, I, P, P, P, Z, P]),
         "da_attn_decode": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, I, P, P, P, P, P, Z, P]),
         "da_decode_workspace_bytes": (Z, [ctypes.POINTER(DaLayer), I, I]),
+        "da_attn_mixed": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, I, I, P, P, P, I, I, P, P, ctypes.c_double,
+                              ctypes.c_double, P, P, Z, P]),
+        "da_attn_mixed_prefill_sms": (I, [ctypes.POINTER(DaLayer), I, ctypes.c_double, ctypes.c_double]),
+        "da_attn_mixed_paged": (I, [ctypes.POINTER(DaLayer), P, ctypes.POINTER(DaPagedKv), I, I, P, P, P, I, I, P, P,
+                                    ctypes.c_double, ctypes.c_double, P, P, Z, P]),
         "da_attn_decode_noalloc": (I, [ctypes.POINTER(DaLayer), P, P, P, I, I, I, P, P, P, P, P]),
         "da_decode_noalloc_max_scratch_bytes": (Z, []),
         "da_kv_cache_update_paged": (I, [ctypes.POINTER(DaLayer), P, P, P, I, P, P, P, P, P,
@@ -267,6 +272,31 @@ def attn_decode(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, pos
     _check(LIB.da_attn_decode(ctypes.byref(L), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), int(num_rows),
                               int(max_len), int(n_seqs), _ptr(rows), _ptr(positions), _ptr(key_positions), _ptr(out),
                               _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def attn_mixed(L, q_rot, k_cache, v_cache, num_rows, max_len, n_tokens, n_seqs, q_start, chunk_rows, first_pos,
+               max_q_len, n_decode, dec_rows, dec_positions, prefill_pairs, decode_keys, out, workspace, ws_bytes,
+               stream=None):
+    """da_attn_mixed: the chunks' tokens first in q_rot/out, then the decode tokens (see decattn.h)."""
+    _check(LIB.da_attn_mixed(ctypes.byref(L), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache), int(num_rows), int(max_len),
+                             int(n_tokens), int(n_seqs), _ptr(q_start), _ptr(chunk_rows), _ptr(first_pos),
+                             int(max_q_len), int(n_decode), _ptr(dec_rows), _ptr(dec_positions), float(prefill_pairs),
+                             float(decode_keys), _ptr(out), _ptr(workspace), int(ws_bytes), _stream(stream)))
+
+
+def attn_mixed_prefill_sms(L, n_sm, prefill_pairs, decode_keys) -> int:
+    r = int(LIB.da_attn_mixed_prefill_sms(ctypes.byref(L), int(n_sm), float(prefill_pairs), float(decode_keys)))
+    if r < 0:
+        raise DecAttnError(r, last_error())
+    return r
+
+
+def attn_mixed_paged(L, q_rot, kv, n_tokens, n_seqs, q_start, chunk_rows, first_pos, max_q_len, n_decode, dec_rows,
+                     dec_positions, prefill_pairs, decode_keys, out, workspace, ws_bytes, stream=None):
+    _check(LIB.da_attn_mixed_paged(ctypes.byref(L), _ptr(q_rot), ctypes.byref(kv), int(n_tokens), int(n_seqs),
+                                   _ptr(q_start), _ptr(chunk_rows), _ptr(first_pos), int(max_q_len), int(n_decode),
+                                   _ptr(dec_rows), _ptr(dec_positions), float(prefill_pairs), float(decode_keys),
+                                   _ptr(out), _ptr(workspace), int(ws_bytes), _stream(stream)))
 
 
 def attn_decode_noalloc(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, positions, key_positions, out,

@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/decattn.h: argument checks, fp64 RoPE frequency math,
 // tensor-map encoding and dispatch to the kernels.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -411,10 +412,12 @@ static da::AttnArgs make_args(const da_layer* L, const void* q_rot, const void* 
   return a;
 }
 
+// check_only: every host check, then return without enqueueing. max_ctas: cap on the tcgen05 prefill's
+// persistent grid (0: one CTA per SM).
 static int prefill_impl(const da_layer* L, const void* q_rot, int n_tokens, const void* k_cache, const void* v_cache,
                         int num_rows, int max_len, int n_seqs, const int32_t* q_start, const int32_t* rows,
                         const int32_t* first_pos, int max_q_len, const int32_t* key_positions, void* out,
-                        const da_paged_kv* kv, cudaStream_t stream) {
+                        const da_paged_kv* kv, cudaStream_t stream, bool check_only = false, int max_ctas = 0) {
   int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out, kv != nullptr);
   if (rc) return rc;
   if (n_tokens < 0 || max_q_len < 0) return fail(DA_ERR_INVALID_ARG, "n_tokens and max_q_len must be >= 0");
@@ -428,8 +431,10 @@ static int prefill_impl(const da_layer* L, const void* q_rot, int n_tokens, cons
   a.max_q_len = max_q_len;
   a.n_tokens = n_tokens;
   set_paged(a, kv);
+  a.max_ctas = max_ctas;
   const bool fast = L->dtype == DA_BF16 && L->head_dim == 128 && key_positions == nullptr &&
                     (kv == nullptr || kv->block_size % 64 == 0);
+  if (check_only) return ok();
   cudaError_t e = fast ? da::launch_prefill_bf16(a, stream) : da::launch_attn_generic(a, L->dtype == DA_BF16, stream);
   if (e != cudaSuccess) return cuda_fail(e, fast ? "prefill (tcgen05) launch" : "prefill (generic) launch");
   return ok();
@@ -480,7 +485,7 @@ size_t da_decode_workspace_bytes_paged(const da_layer* L, int n_seqs, int max_po
 static int decode_impl(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache, int num_rows,
                        int max_len, int n_seqs, const int32_t* rows, const int32_t* positions,
                        const int32_t* key_positions, void* out, void* workspace, size_t ws_bytes,
-                       const da_paged_kv* kv, cudaStream_t stream) {
+                       const da_paged_kv* kv, cudaStream_t stream, bool check_only = false) {
   int rc = attn_common_checks(L, q_rot, k_cache, v_cache, num_rows, max_len, n_seqs, rows, out, kv != nullptr);
   if (rc) return rc;
   if (n_seqs == 0) return ok();
@@ -493,6 +498,7 @@ static int decode_impl(const da_layer* L, const void* q_rot, const void* k_cache
   a.n_tokens = n_seqs;
   set_paged(a, kv);
   if (!decode_fast(L, key_positions) || (kv && kv->block_size % 64 != 0)) {
+    if (check_only) return ok();
     cudaError_t e = da::launch_attn_generic(a, L->dtype == DA_BF16, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode (generic) launch");
     return ok();
@@ -502,6 +508,7 @@ static int decode_impl(const da_layer* L, const void* q_rot, const void* k_cache
   if (!workspace || ws_bytes < need)
     return fail(DA_ERR_INVALID_ARG, "decode workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
   if (!aligned16(workspace)) return fail(DA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (check_only) return ok();
   cudaError_t e = da::launch_decode_bf16(a, p, workspace, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode (split-K) launch");
   return ok();
@@ -523,6 +530,169 @@ int da_attn_decode_paged(const da_layer* L, const void* q_rot, const da_paged_kv
   if (rc) return rc;
   return decode_impl(L, q_rot, kv->k_pool, kv->v_pool, kv->num_rows, kv->max_blocks * kv->block_size, n_seqs, rows,
                      positions, nullptr, out, workspace, ws_bytes, kv, stream);
+}
+
+// ------------------------------------------------------------------------------------------ mixed batches
+
+namespace {
+
+// The stream a mixed call forks onto and its fork/join events: one set per device, created on first use and
+// kept until the process exits. g_side_mu is held while a call enqueues, so that no other call records the
+// shared events between another's record and wait.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+// Rates of the two kernels on GB300 that the split below models (measured: the tcgen05 prefill at 1092
+// TFLOP/s over 152 SMs on contiguous caches, about 0.8 of that over a paged pool; the split-K decode at 7.2
+// TB/s on the whole GPU, ~100 GB/s per SM or more when it has a few dozen SMs to itself).
+constexpr double kPrefillFlopsPerSm = 7.2e12;
+constexpr double kPagedPrefillRate = 0.8;
+constexpr double kDecodeBytesPerSm = 1.0e11;
+constexpr double kDecodeBytesAll = 7.2e12;
+
+// Persistent prefill CTAs for a prefill and a decode that share the GPU; n_sm means one after the other.
+// With P prefill CTAs (one per SM: nothing else fits beside one) the decode's blocks get the other SMs, and
+// once the prefill ends they spread over all of them (the persistent prefill cannot grow into SMs that the
+// decode leaves). P minimises the modelled end of both, and is used only when that beats running them in turn
+// by more than 3% (the fork and join, and the model's own error, cost a few).
+int mixed_prefill_ctas(int n_sm, double flops, double bytes, bool paged) {
+  const double rate = kPrefillFlopsPerSm * (paged ? kPagedPrefillRate : 1.0);
+  const double serial = flops / (n_sm * rate) + bytes / kDecodeBytesAll;
+  double best = serial;
+  int best_p = n_sm;
+  for (int p = std::max(1, n_sm / 4); p < n_sm; ++p) {
+    const double t_pf = flops / (p * rate);
+    const double bw = std::min((n_sm - p) * kDecodeBytesPerSm, kDecodeBytesAll);
+    const double t = bytes <= t_pf * bw ? t_pf : t_pf + (bytes - t_pf * bw) / kDecodeBytesAll;
+    if (t < best) {
+      best = t;
+      best_p = p;
+    }
+  }
+  return best < 0.97 * serial ? best_p : n_sm;
+}
+
+}  // namespace
+
+// The split for a layer's hints: prefill FLOPs 4 d Hq pairs, decode bytes keys * 2 Hkv d * 2 (bf16).
+static int mixed_split(const da_layer* L, int n_sm, double prefill_pairs, double decode_keys, bool paged) {
+  const double flops = 4.0 * L->head_dim * L->num_attention_heads * prefill_pairs;
+  const double bytes = decode_keys * 2.0 * L->num_key_value_heads * L->head_dim * 2.0;
+  return mixed_prefill_ctas(n_sm, flops, bytes, paged);
+}
+
+int da_attn_mixed_prefill_sms(const da_layer* L, int n_sm, double prefill_pairs, double decode_keys) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n_sm < 1) return fail(DA_ERR_INVALID_ARG, "n_sm = %d < 1", n_sm);
+  if (!(prefill_pairs >= 0.0) || !(decode_keys >= 0.0) || !std::isfinite(prefill_pairs) ||
+      !std::isfinite(decode_keys))
+    return fail(DA_ERR_INVALID_ARG, "prefill_pairs and decode_keys must be finite and >= 0");
+  ok();
+  if (prefill_pairs == 0.0 || decode_keys == 0.0) return n_sm;
+  return mixed_split(L, n_sm, prefill_pairs, decode_keys, false);
+}
+
+static int mixed_impl(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache, int num_rows,
+                      int max_len, int n_tokens, int n_seqs, const int32_t* q_start, const int32_t* chunk_rows,
+                      const int32_t* first_pos, int max_q_len, int n_decode, const int32_t* dec_rows,
+                      const int32_t* dec_positions, double prefill_pairs, double decode_keys, void* out,
+                      void* workspace, size_t ws_bytes, const da_paged_kv* kv, cudaStream_t stream) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n_tokens < 0 || n_decode < 0) return fail(DA_ERR_INVALID_ARG, "n_tokens and n_decode must be >= 0");
+  if (!(prefill_pairs >= 0.0) || !(decode_keys >= 0.0) || !std::isfinite(prefill_pairs) ||
+      !std::isfinite(decode_keys))
+    return fail(DA_ERR_INVALID_ARG, "prefill_pairs and decode_keys must be finite and >= 0");
+  // decode tokens follow the chunks' tokens in q_rot and out
+  const size_t row_bytes =
+      static_cast<size_t>(L->num_attention_heads) * L->head_dim * (L->dtype == DA_BF16 ? 2 : 4);
+  const void* q_dec = q_rot ? static_cast<const uint8_t*>(q_rot) + static_cast<size_t>(n_tokens) * row_bytes : nullptr;
+  void* out_dec = out ? static_cast<uint8_t*>(out) + static_cast<size_t>(n_tokens) * row_bytes : nullptr;
+  auto prefill = [&](cudaStream_t st, bool check_only, int max_ctas) {
+    return prefill_impl(L, q_rot, n_tokens, k_cache, v_cache, num_rows, max_len, n_seqs, q_start, chunk_rows,
+                        first_pos, max_q_len, nullptr, out, kv, st, check_only, max_ctas);
+  };
+  auto decode = [&](cudaStream_t st, bool check_only) {
+    return decode_impl(L, q_dec, k_cache, v_cache, num_rows, max_len, n_decode, dec_rows, dec_positions, nullptr,
+                       out_dec, workspace, ws_bytes, kv, st, check_only);
+  };
+  // every check of both parts before anything is enqueued
+  rc = prefill(stream, true, 0);
+  if (rc) return rc;
+  rc = decode(stream, true);
+  if (rc) return rc;
+
+  const bool pf_work = n_seqs > 0 && n_tokens > 0 && max_q_len > 0, dec_work = n_decode > 0;
+  const bool tc = L->dtype == DA_BF16 && L->head_dim == 128 && L->num_attention_heads / L->num_key_value_heads <= 8 &&
+                  (kv == nullptr || kv->block_size % 64 == 0);
+  int dev = 0, n_sm = 0, p = 0;
+  if (pf_work && dec_work && tc && prefill_pairs > 0.0 && decode_keys > 0.0) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    p = mixed_split(L, n_sm, prefill_pairs, decode_keys, kv != nullptr);
+  }
+  if (p == 0 || p >= n_sm || dev >= kMaxDevices) {   // one after the other on `stream`
+    rc = prefill(stream, false, 0);
+    if (rc) return rc;
+    return decode(stream, false);
+  }
+
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream& ss = g_side[dev];
+  if (!ss.stream) {
+    cudaError_t e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      if (ss.join) cudaEventDestroy(ss.join);
+      if (ss.fork) cudaEventDestroy(ss.fork);
+      if (ss.stream) cudaStreamDestroy(ss.stream);
+      ss = SideStream{};
+      return cuda_fail(e, "mixed batch: side stream");
+    }
+  }
+  cudaError_t e = cudaEventRecord(ss.fork, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss.stream, ss.fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "mixed batch: fork");
+  // the prefill first, so that its persistent CTAs take their SMs before the decode's blocks fill the rest
+  rc = prefill(stream, false, p);
+  const int rc_dec = rc ? rc : decode(ss.stream, false);
+  e = cudaEventRecord(ss.join, ss.stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ss.join, 0);
+  if (rc || rc_dec) return rc ? rc : rc_dec;
+  if (e != cudaSuccess) return cuda_fail(e, "mixed batch: join");
+  return ok();
+}
+
+int da_attn_mixed(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache, int num_rows,
+                  int max_len, int n_tokens, int n_seqs, const int32_t* q_start, const int32_t* chunk_rows,
+                  const int32_t* first_pos, int max_q_len, int n_decode, const int32_t* dec_rows,
+                  const int32_t* dec_positions, double prefill_pairs, double decode_keys, void* out, void* workspace,
+                  size_t ws_bytes, cudaStream_t stream) {
+  return mixed_impl(L, q_rot, k_cache, v_cache, num_rows, max_len, n_tokens, n_seqs, q_start, chunk_rows, first_pos,
+                    max_q_len, n_decode, dec_rows, dec_positions, prefill_pairs, decode_keys, out, workspace, ws_bytes,
+                    nullptr, stream);
+}
+
+int da_attn_mixed_paged(const da_layer* L, const void* q_rot, const da_paged_kv* kv, int n_tokens, int n_seqs,
+                        const int32_t* q_start, const int32_t* chunk_rows, const int32_t* first_pos, int max_q_len,
+                        int n_decode, const int32_t* dec_rows, const int32_t* dec_positions, double prefill_pairs,
+                        double decode_keys, void* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_layer(L);
+  if (rc) return rc;
+  if (n_seqs == 0 && n_decode == 0) return ok();
+  rc = check_paged(L, kv);
+  if (rc) return rc;
+  return mixed_impl(L, q_rot, kv->k_pool, kv->v_pool, kv->num_rows, kv->max_blocks * kv->block_size, n_tokens, n_seqs,
+                    q_start, chunk_rows, first_pos, max_q_len, n_decode, dec_rows, dec_positions, prefill_pairs,
+                    decode_keys, out, workspace, ws_bytes, kv, stream);
 }
 
 int da_attn_decode_noalloc(const da_layer* L, const void* q_rot, const void* k_cache, const void* v_cache,

@@ -1156,7 +1156,8 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (shared memory and all 512 TMEM columns allow no second one)
-  const int grid = static_cast<int>(std::min<long long>(n_items, n_sm));
+  int grid = static_cast<int>(std::min<long long>(n_items, n_sm));
+  if (a.max_ctas > 0) grid = std::min(grid, a.max_ctas);   // the rest of the SMs left to a concurrent decode
   const bool paged = a.block_table != nullptr, capped = a.softcap > 0.f;
   if (paged) {
     return capped ? run_prefill<true, true>(tmq, tmk, tmv, tmo, prm, grid, stream)

@@ -104,6 +104,7 @@ struct AttnArgs {
   float scale;
   const float* sinks;             // [Hq] sink logits (natural units) or NULL
   int* err;
+  int max_ctas;                   // tcgen05 prefill: at most this many persistent CTAs (0: one per SM)
 };
 cudaError_t launch_attn_generic(const AttnArgs& a, bool bf16, cudaStream_t stream);
 

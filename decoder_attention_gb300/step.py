@@ -2,7 +2,8 @@
 
 ``AttentionStep`` owns the per-call buffers (cos/sin tables, q_rot, out, decode workspace) that the caller
 must provide to the library, allocated once with torch; ``run()`` only enqueues the library's kernels.
-Prefill chunks and decode tokens of one batch go to da_attn_prefill and da_attn_decode respectively,
+Prefill chunks and decode tokens of one batch go to da_attn_prefill and da_attn_decode respectively, or
+together to da_attn_mixed when the batch holds both (the library may then run the two side by side),
 after one cache update for all tokens: da_kv_cache_update_rope (cos/sin formed in the kernel) where the layer
 allows it (bf16, head_dim 128, rotary_dim a multiple of 16), else da_rope_tables_build + da_kv_cache_update.
 """
@@ -12,7 +13,7 @@ import math
 
 import torch
 
-from . import _abi
+from . import _abi, work
 
 
 def rotary_dim_of(head_dim, partial_rotary_factor):
@@ -49,6 +50,13 @@ class AttentionStep:
             self.ws_bytes = _abi.decode_workspace_bytes(self.L, c.n_decode, c.max_len)
             if self.ws_bytes:
                 self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        # host hints of a mixed batch's two parts for da_attn_mixed: visible (query, key) pairs of one query head
+        # over the chunks, visible keys over the decode tokens (read once here from the call's metadata)
+        self.hint_pairs = self.hint_keys = 0.0
+        if c.n_prefill and c.n_decode:
+            w = work.layer_call_work(c)
+            self.hint_pairs = w["prefill_pairs"] / c.num_attention_heads
+            self.hint_keys = float(w["decode_keys"])
 
     # -- the three stages, separately callable for timing ------------------------------------------
     def rope(self, stream=None):
@@ -85,10 +93,24 @@ class AttentionStep:
                              c.n_decode, c.dec_rows, c.dec_pos, None, self.out[c.n_prefill:], self.workspace,
                              self.ws_bytes, stream)
 
+    def attend(self, stream=None):
+        """Attention of every token: one da_attn_mixed call when the batch has chunks and decode tokens."""
+        c = self.call
+        if c.n_prefill and c.n_decode:
+            self.mixed(stream)
+        else:
+            self.prefill(stream)
+            self.decode(stream)
+
+    def mixed(self, stream=None):
+        c = self.call
+        _abi.attn_mixed(self.L, self.q_rot, c.k_cache, c.v_cache, c.num_rows, c.max_len, c.n_prefill, len(c.pf_rows),
+                        c.q_start, c.pf_rows, c.pf_first_pos, c.max_q_len, c.n_decode, c.dec_rows, c.dec_pos,
+                        self.hint_pairs, self.hint_keys, self.out, self.workspace, self.ws_bytes, stream)
+
     def run(self, stream=None):
         self.update(stream)
-        self.prefill(stream)
-        self.decode(stream)
+        self.attend(stream)
         return self.out
 
     def kernel_launches(self):
@@ -140,6 +162,12 @@ class PagedAttentionStep(AttentionStep):
         if c.n_decode:
             _abi.attn_decode_paged(self.L, self.q_rot[c.n_prefill:], self.kv, c.n_decode, c.dec_rows, c.dec_pos,
                                    self.out[c.n_prefill:], self.workspace, self.ws_bytes, stream)
+
+    def mixed(self, stream=None):
+        c = self.call
+        _abi.attn_mixed_paged(self.L, self.q_rot, self.kv, c.n_prefill, len(c.pf_rows), c.q_start, c.pf_rows,
+                              c.pf_first_pos, c.max_q_len, c.n_decode, c.dec_rows, c.dec_pos, self.hint_pairs,
+                              self.hint_keys, self.out, self.workspace, self.ws_bytes, stream)
 
 
 

@@ -226,6 +226,40 @@ int da_attn_decode(const da_layer* layer, const void* q_rot, const void* k_cache
 size_t da_decode_workspace_bytes(const da_layer* layer, int n_seqs, int max_len);
 
 /*
+ * da_attn_mixed -- da_attn_prefill and da_attn_decode of one layer's mixed batch (prefill chunks and decode
+ * tokens in the same step, as DecoderAttention.forward on page 1 takes a batch of both) in one call, the two
+ * running side by side on the GPU.
+ *
+ * Token layout of q_rot and out: the chunks' tokens first (rows 0 .. n_tokens-1, as da_attn_prefill takes
+ * them), then one token per decoding sequence (rows n_tokens .. n_tokens + n_decode - 1, as da_attn_decode).
+ * The results are bit for bit those of da_attn_prefill followed by da_attn_decode with the same arguments:
+ * the same kernels compute every output, and no output depends on how the GPU is shared.
+ *
+ * When both parts run on the tensor-core paths (bf16, d = 128, no key_positions) and both work hints are
+ * positive, the prefill's persistent grid is given part of the SMs and the decode's blocks the rest, so that
+ * the compute-bound prefill and the memory-bound decode overlap. The split minimises the modelled time of the
+ * two on this GPU (prefill ~7.2 TFLOP/s per SM, 0.8 of that over a paged pool; decode ~100 GB/s per SM up to
+ * ~7.2 TB/s in all), and the call runs the two one after the other on `stream` when that model says overlap
+ * does not pay (by 3% or more). To overlap, the call forks onto a stream the library owns (created, with two
+ * events, on the first such call on each device and kept until the process exits) and joins back to `stream`
+ * before returning: work enqueued on `stream` afterwards sees both results. Calls from several host threads
+ * are serialised while they enqueue.
+ *
+ *   n_tokens, n_seqs, q_start, chunk_rows, first_pos, max_q_len   the prefill part, as da_attn_prefill
+ *   n_decode, dec_rows, dec_positions                             the decode part, as da_attn_decode
+ *   prefill_pairs  host hint: visible (query, key) pairs summed over the chunks' tokens (one query head);
+ *                  0 when unknown (then the parts run one after the other)
+ *   decode_keys    host hint: visible keys summed over the decode tokens; 0 when unknown
+ *   workspace, ws_bytes  decode scratch of at least da_decode_workspace_bytes(layer, n_decode, max_len)
+ * Errors: every check of both calls, made before anything is enqueued.
+ */
+int da_attn_mixed(const da_layer* layer, const void* q_rot, const void* k_cache, const void* v_cache, int num_rows,
+                  int max_len, int n_tokens, int n_seqs, const int32_t* q_start, const int32_t* chunk_rows,
+                  const int32_t* first_pos, int max_q_len, int n_decode, const int32_t* dec_rows,
+                  const int32_t* dec_positions, double prefill_pairs, double decode_keys, void* out, void* workspace,
+                  size_t ws_bytes, cudaStream_t stream);
+
+/*
  * da_attn_decode_noalloc -- da_attn_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart: this entry point exists for callers of this library that may not call
@@ -302,6 +336,20 @@ int da_attn_prefill_paged(const da_layer* layer, const void* q_rot, int n_tokens
 int da_attn_decode_paged(const da_layer* layer, const void* q_rot, const da_paged_kv* kv, int n_seqs,
                          const int32_t* rows, const int32_t* positions, void* out, void* workspace, size_t ws_bytes,
                          cudaStream_t stream);
+
+/* How many SMs da_attn_mixed (contiguous caches) gives the prefill's persistent grid, for these hints, on a GPU
+ * of n_sm SMs: n_sm
+ * when the two parts would run one after the other. Pure host arithmetic (the model described at
+ * da_attn_mixed), for callers that plan batches and for tests. DA_ERR_INVALID_ARG (negative) for an invalid
+ * layer, n_sm < 1, or hints that are negative or not finite. */
+int da_attn_mixed_prefill_sms(const da_layer* layer, int n_sm, double prefill_pairs, double decode_keys);
+
+/* da_attn_mixed over a paged pool (the prefill and decode parts as da_attn_prefill_paged and
+ * da_attn_decode_paged; workspace per da_decode_workspace_bytes_paged). */
+int da_attn_mixed_paged(const da_layer* layer, const void* q_rot, const da_paged_kv* kv, int n_tokens, int n_seqs,
+                        const int32_t* q_start, const int32_t* chunk_rows, const int32_t* first_pos, int max_q_len,
+                        int n_decode, const int32_t* dec_rows, const int32_t* dec_positions, double prefill_pairs,
+                        double decode_keys, void* out, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* Scratch bytes da_attn_decode_paged needs for n_seqs sequences of a pool whose rows hold max_positions
  * (= max_blocks * block_size) positions (0 when the layer is invalid or decode needs none). Host arithmetic. */

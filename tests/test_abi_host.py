@@ -215,3 +215,36 @@ def test_fused_rope_update_host_checks():
     rsl, keepl = _abi.rope_scaling(1e4, 128, sc, 131072)
     assert rc(_layer(), rsl, seq_len=None) == _abi.DA_ERR_INVALID_ARG and "seq_len" in _abi.last_error()
     assert _abi.kv_rope_fused_supported(_layer()) and not _abi.kv_rope_fused_supported(_layer(head_dim=64, rotary_dim=64))
+
+
+def test_mixed_split_model():
+    """da_attn_mixed_prefill_sms (host arithmetic): no hint or a decode too small to pay for the fork gives the
+    prefill every SM (the parts run in turn); a decode of comparable time takes SMs from the prefill, more of
+    them the more bytes it moves; the prefill keeps at least a quarter of the SMs."""
+    import torch
+    L = _abi.layer(torch.bfloat16, 128, 24, 8, 96, None, None, 1e-6, 0, 50.0, 0.0, None)
+    pairs, keys = 8 * 1024 * 33000.0, 120 * 33000.0
+    assert _abi.attn_mixed_prefill_sms(L, 152, 0.0, keys) == 152
+    assert _abi.attn_mixed_prefill_sms(L, 152, pairs, 0.0) == 152
+    assert _abi.attn_mixed_prefill_sms(L, 152, pairs, 8 * 4096.0) == 152
+    p = [_abi.attn_mixed_prefill_sms(L, 152, pairs, keys * f) for f in (0.5, 1.0, 1.5)]
+    assert all(152 // 4 <= x < 152 for x in p), p
+    assert p[0] >= p[1] >= p[2], p
+    assert 76 // 4 <= _abi.attn_mixed_prefill_sms(L, 76, pairs, keys) <= 76
+    for bad in ((152, float("nan"), keys), (152, -1.0, keys), (0, pairs, keys)):
+        with pytest.raises(_abi.DecAttnError):
+            _abi.attn_mixed_prefill_sms(L, *bad)
+
+
+def test_mixed_argument_checks():
+    L = _layer()
+    d = ctypes.c_void_p(16)
+    P = ctypes.c_double
+    rc = _abi.LIB.da_attn_mixed(ctypes.byref(L), d, d, d, 4, 4, 8, 1, d, d, d, 8, -1, d, d, P(0), P(0), d, None, 0,
+                                None)
+    assert rc == _abi.DA_ERR_INVALID_ARG                                   # n_decode < 0
+    rc = _abi.LIB.da_attn_mixed(ctypes.byref(L), d, d, d, 4, 4, 8, 1, d, d, d, 8, 2, d, d, P(float("nan")), P(0), d,
+                                None, 0, None)
+    assert rc == _abi.DA_ERR_INVALID_ARG                                   # hint not finite
+    rc = _abi.LIB.da_attn_mixed(None, d, d, d, 4, 4, 8, 1, d, d, d, 8, 2, d, d, P(0), P(0), d, None, 0, None)
+    assert rc == _abi.DA_ERR_INVALID_ARG                                   # no layer
