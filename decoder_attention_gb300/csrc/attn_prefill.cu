@@ -389,29 +389,40 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   // key (a pool that recycles out-of-window blocks) or wholly past the row's last key is skipped: its keys
   // are masked for every query of the item and the softmax warps zero its V rows. Any other missing block
   // is reported and read from row 0, so that the copy still delivers the bytes its barrier expects.
-  auto load_kv_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int plane, int key, int first_vis,
-                          int kv_len) {
+  // tile_rows looks the boxes up (paged pools: a block-table read each), issue_tile copies them; a producer
+  // looks a tile up before it waits for the ring slot, so the table reads overlap that wait.
+  struct TileRows {
+    int r[BN / 64];
+  };
+  auto tile_rows = [&](int plane, int key, int first_vis, int kv_len) -> TileRows {
+    TileRows t;
     if constexpr (!PAGED) {
-      const int r = plane + key;
-      mbar_arrive_expect_tx(bar, TILE);
-      tma_load_2d(dst, tm, bar, 0, r);
-      tma_load_2d(dst + HALF, tm, bar, 64, r);
+      t.r[0] = plane + key;
     } else {
-      int rows[BN / 64];
-      uint32_t bytes = 0;
       for (int j = 0, b = 0; j < BN; j += prm.kbox, ++b) {
-        rows[b] = key_row(plane, key + j);
-        if (rows[b] < 0 && key + j + prm.kbox > first_vis && key + j < kv_len) {
+        t.r[b] = key_row(plane, key + j);
+        if (t.r[b] < 0 && key + j + prm.kbox > first_vis && key + j < kv_len) {
           set_error(prm.err, kErrIndex);
-          rows[b] = 0;
+          t.r[b] = 0;
         }
-        if (rows[b] >= 0) bytes += prm.kbox * 2 * 128;
       }
+    }
+    return t;
+  };
+  auto issue_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, const TileRows& t) {
+    if constexpr (!PAGED) {
+      mbar_arrive_expect_tx(bar, TILE);
+      tma_load_2d(dst, tm, bar, 0, t.r[0]);
+      tma_load_2d(dst + HALF, tm, bar, 64, t.r[0]);
+    } else {
+      uint32_t bytes = 0;
+      for (int j = 0, b = 0; j < BN; j += prm.kbox, ++b)
+        if (t.r[b] >= 0) bytes += prm.kbox * 2 * 128;
       mbar_arrive_expect_tx(bar, bytes);
       for (int j = 0, b = 0; j < BN; j += prm.kbox, ++b) {
-        if (rows[b] < 0) continue;
-        tma_load_2d(dst + j * 128, tm, bar, 0, rows[b]);
-        tma_load_2d(dst + HALF + j * 128, tm, bar, 64, rows[b]);
+        if (t.r[b] < 0) continue;
+        tma_load_2d(dst + j * 128, tm, bar, 0, t.r[b]);
+        tma_load_2d(dst + HALF + j * 128, tm, bar, 64, t.r[b]);
       }
     }
   };
@@ -591,9 +602,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       };
       auto fill_k = [&](int plane, int key, int first_vis, int kv_len) -> bool {   // plane < 0: no K tile
         const int st = kj % NS;
+        TileRows rows{};
+        if (plane >= 0) rows = tile_rows(plane, key, first_vis, kv_len);
         if (kj >= NS && !mbar_wait(B(B_EM + st), ((kj / NS) - 1) & 1, prm.err)) return false;
         if (plane >= 0) {
-          load_kv_tile(sbase + OFF_R + st * 2 * TILE, &tmk, B(B_FU + st), plane, key, first_vis, kv_len);
+          issue_tile(sbase + OFF_R + st * 2 * TILE, &tmk, B(B_FU + st), rows);
         } else {
           mbar_arrive(B(B_FU + st));
         }
@@ -613,7 +626,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           tma_prefetch_3d(&tmq, 0, hd, tok);
           tma_prefetch_3d(&tmq, 64, hd, tok);
         }
-        const int key = key_row(nx.plane, first_visible(nx) / prm.kbox * prm.kbox);
+        // (paged pools: Q only; the block-table read that the first K/V box needs would hold this producer
+        // up for longer than the prefetch saves)
+        const int key = PAGED ? -1 : key_row(nx.plane, first_visible(nx) / prm.kbox * prm.kbox);
         if (key >= 0) {
           tma_prefetch_2d(&tmk, 0, key);
           tma_prefetch_2d(&tmk, 64, key);
@@ -650,9 +665,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       bool ok = true;
       auto fill_v = [&](int plane, int key, int first_vis, int kv_len) -> bool {   // plane < 0: no V tile
         const int st = vj % NS;
+        TileRows rows{};
+        if (plane >= 0) rows = tile_rows(plane, key, first_vis, kv_len);
         if (vj >= NS && !mbar_wait(B(B_EM + st), ((vj / NS) - 1) & 1, prm.err)) return false;
         if (plane >= 0) {
-          load_kv_tile(sbase + OFF_R + st * 2 * TILE + TILE, &tmv, B(B_FU + st), plane, key, first_vis, kv_len);
+          issue_tile(sbase + OFF_R + st * 2 * TILE + TILE, &tmv, B(B_FU + st), rows);
         } else {
           mbar_arrive(B(B_FU + st));
         }
