@@ -142,3 +142,47 @@ def test_mixed_matches_the_oracle(cuda):
         d = np.abs(st.out.double().cpu().numpy() - ref["out"])
         assert np.isfinite(d).all()
         assert d.max() <= 2e-2 and d.mean() <= 2e-3, (d.max(), d.mean())
+
+
+def test_mixed_from_two_host_threads(cuda):
+    """Two host threads, each with its own stream and layer call, enqueue mixed calls at once: the library's
+    one fork stream per device and its shared events are used under a lock, so every call still joins its own
+    stream after its own two parts (results equal to the two calls made in turn, for every repetition)."""
+    import threading
+    from decoder_attention_gb300 import _abi, step
+    calls = _mixed_layers()
+    runs = []
+    for call in calls:
+        a, b = call.to(cuda), call.to(cuda)
+        sa, sb = step.AttentionStep(a), step.AttentionStep(b)
+        sa.update()
+        sb.update()
+        _sequential(sb)
+        runs.append((sa, sb))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(sa, sb):
+        try:
+            torch.cuda.set_device(cuda)
+            s = torch.cuda.Stream()
+            snaps = []
+            with torch.cuda.stream(s):
+                for _ in range(8):
+                    sa.out.fill_(float("nan"))
+                    _forced_mixed(sa, s)
+                    snaps.append(sa.out.clone())
+            s.synchronize()
+            for x in snaps:
+                if not torch.equal(x, sb.out):
+                    errors.append("mismatch")
+        except Exception as e:   # reported to the main thread
+            errors.append(repr(e))
+
+    ts = [threading.Thread(target=worker, args=r) for r in runs]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    _abi.check_device_error()
+    assert not errors, errors
