@@ -243,7 +243,8 @@ size_t da_decode_workspace_bytes(const da_layer* layer, int n_seqs, int max_len)
  * does not pay (by 3% or more). To overlap, the call forks onto a stream the library owns (created, with two
  * events, on the first such call on each device and kept until the process exits) and joins back to `stream`
  * before returning: work enqueued on `stream` afterwards sees both results. Calls from several host threads
- * are serialised while they enqueue.
+ * are serialised while they enqueue. The fork and join are capturable into a CUDA graph; make the first
+ * overlapping call on each device (the one that creates the stream and events) outside any capture.
  *
  *   n_tokens, n_seqs, q_start, chunk_rows, first_pos, max_q_len   the prefill part, as da_attn_prefill
  *   n_decode, dec_rows, dec_positions                             the decode part, as da_attn_decode
