@@ -572,7 +572,11 @@ def measure_native(args, workload, dev, world, rank, with_e2e=True):
         rec["parts_over_step"] = {
             "prefill_tflops": pf_t, "prefill_frac": pf_t / peaks["bf16_tflops"],
             "decode_gbs": dec_g, "decode_frac": dec_g / peaks["hbm_gbs"],
-            "sum_of_fracs": pf_t / peaks["bf16_tflops"] + dec_g / peaks["hbm_gbs"]}
+            "sum_of_fracs": pf_t / peaks["bf16_tflops"] + dec_g / peaks["hbm_gbs"],
+            # SMs the library's split model gives each layer's prefill (the rest run the decode; all SMs: in turn)
+            "prefill_sms_per_layer": None if pools else [
+                _abi.attn_mixed_prefill_sms(st.L, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                            st.hint_pairs, st.hint_keys) for st in steps]}
     del steps, pools, wl, flush
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
