@@ -794,6 +794,8 @@ def measure_mla(args, dev, world, rank):
     rec = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "timing": (f"median of {args.steps} timed steps (events around each step only); breakdown_ms and "
+                   f"roofline from a second pass of {args.steps} steps with an event between the stages"),
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": MLA_WORKLOAD, "description": call.meta["description"],
                    "l2": "flushed (256 MB write) before every timed step, outside the step's events",
@@ -938,6 +940,8 @@ def measure_block(args, dev, world, rank):
     rec = {
             "metric": METRIC, "value": total / (ms / 1e3) / 1e12 * world, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "timing": (f"median of {args.steps} timed blocks (events around each block only); breakdown_ms and "
+                       f"roofline from a second pass of {args.steps} blocks with an event after every part"),
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init projection weights)",
             "config": {"workload": BLOCK_WORKLOAD, "description": "Qwen3-8B-shaped attention block: 4 x 2048 tokens, "
                        "hidden 4096, fused q/k/v projection + norm + RoPE + cache write, prefill attention, o_proj",
