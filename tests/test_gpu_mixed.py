@@ -186,3 +186,35 @@ def test_mixed_from_two_host_threads(cuda):
         t.join()
     _abi.check_device_error()
     assert not errors, errors
+
+
+def test_mixed_with_one_part_or_none(cuda):
+    """A mixed call whose batch has only prefill chunks, only decode tokens, or nothing at all runs what there
+    is (in turn on the caller's stream) and writes what the separate calls write."""
+    from decoder_attention_gb300 import _abi, step
+    call = _mixed_layers()[1]
+    a, b = call.to(cuda), call.to(cuda)
+    sa, sb = step.AttentionStep(a), step.AttentionStep(b)
+    sa.update()
+    sb.update()
+    _sequential(sb)
+    torch.cuda.synchronize()
+    c = sa.call
+    for n_tokens, n_seqs, n_dec in ((c.n_prefill, len(c.pf_rows), 0), (0, 0, c.n_decode), (0, 0, 0)):
+        sa.out.fill_(float("nan"))
+        # the decode part reads its tokens after the chunks' n_tokens rows: with no chunks, from row 0
+        q_rot = sa.q_rot if n_tokens or not n_dec else sa.q_rot[c.n_prefill:]
+        out = sa.out if n_tokens or not n_dec else sa.out[c.n_prefill:]
+        _abi.attn_mixed(sa.L, q_rot, c.k_cache, c.v_cache, c.num_rows, c.max_len, n_tokens, n_seqs, c.q_start,
+                        c.pf_rows, c.pf_first_pos, c.max_q_len, n_dec, c.dec_rows, c.dec_pos, OVERLAP_PAIRS,
+                        OVERLAP_KEYS, out, sa.workspace, sa.ws_bytes)
+        torch.cuda.synchronize()
+        _abi.check_device_error()
+        if n_tokens:
+            assert torch.equal(sa.out[:c.n_prefill], sb.out[:c.n_prefill])
+            assert torch.isnan(sa.out[c.n_prefill:].float()).all()
+        elif n_dec:
+            assert torch.equal(sa.out[c.n_prefill:], sb.out[c.n_prefill:])
+            assert torch.isnan(sa.out[:c.n_prefill].float()).all()
+        else:
+            assert torch.isnan(sa.out.float()).all()
